@@ -1,0 +1,5 @@
+"""CPU oracle (test infrastructure only; see spec_oracle's header)."""
+from .spec_oracle import (  # noqa: F401
+    accept_probability, acceptance_rate, argmax_lowest, inverse_cdf, lm_head, residual,
+    softmax_t, spec_verify, verify_greedy, verify_sampling,
+)

@@ -1,0 +1,177 @@
+"""Seeded synthetic inputs for the verify-and-accept step.
+
+This module is the one piece that the CUDA path and the CPU oracle both
+consume.  It holds no arithmetic of the verify step itself: only random
+draws and the stand-in for the draft model (a noisy copy of the target's
+hidden state pushed through the same LM-head weight, whose tokens are drawn
+with the Gumbel-max trick rather than with the inverse-CDF rule the verify
+step uses).
+
+Workloads (the five synthetic configurations the step is measured on):
+
+=====================  ==============================================================
+name                   recipe
+=====================  ==============================================================
+tiny_logits            B=1, K=4, V=1000, no LM head: target logits z_p ~ N(0, std 2)
+                       for K+1 rows; draft logits z_q = z_p[:K] + N(0, std 0.5);
+                       T = 1
+head_B1_K5_V32000      B=1, K=5, d=4096, V=32000; h ~ N(0,1) bf16, W ~ N(0, 1/sqrt d)
+                       bf16; z_q = (h[:K] + 0.3 eps) W^T in fp32; T = 1
+head_B8_K4_V128256     B=8, K=4, d=4096, V=128256 (Llama-3-8B-shaped head);
+                       noise 0.3; T = 0.8
+head_B64_K8_V152064    B=64, K=8, d=8192, V=152064 (70B-class head); noise 1.0; T = 1
+greedy_B256_K4_V128256 B=256, K=4, d=4096, V=128256; T = 0; drafts are the argmax of
+                       (h + 0.2 eps) W^T; no draft logits, no uniforms
+=====================  ==============================================================
+
+"N(0, s)" names the standard deviation.  Draft tokens at T > 0 are sampled
+from softmax(z_q / T) (Gumbel-max); uniforms are U[0, 1) fp32, K accept
+uniforms and one draw uniform per sequence.  The seed of workload i (in the
+table order, from 1) is 6700 + i.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    K: int
+    d: int            # 0 = no LM head (logits are given)
+    V: int
+    temperature: float
+    noise: float      # draft-side noise on the hidden state (std)
+    logit_std: float = 2.0      # tiny_logits only: std of z_p
+    draft_logit_noise: float = 0.5  # tiny_logits only: std of z_q - z_p
+    seed: int = 0
+
+    @property
+    def M(self) -> int:
+        return self.B * (self.K + 1)
+
+    @property
+    def greedy(self) -> bool:
+        return self.temperature == 0.0
+
+
+WORKLOADS = {
+    w.name: w
+    for w in (
+        Workload("tiny_logits", B=1, K=4, d=0, V=1000, temperature=1.0, noise=0.0, seed=6701),
+        Workload("head_B1_K5_V32000", B=1, K=5, d=4096, V=32000, temperature=1.0, noise=0.3, seed=6702),
+        Workload("head_B8_K4_V128256", B=8, K=4, d=4096, V=128256, temperature=0.8, noise=0.3, seed=6703),
+        Workload("head_B64_K8_V152064", B=64, K=8, d=8192, V=152064, temperature=1.0, noise=1.0, seed=6704),
+        Workload("greedy_B256_K4_V128256", B=256, K=4, d=4096, V=128256, temperature=0.0, noise=0.2, seed=6705),
+    )
+}
+
+
+def custom(name: str, B: int, K: int, d: int, V: int, temperature: float, noise: float = 0.3,
+           seed: int = 1) -> Workload:
+    """A workload of the same recipe at other sizes (parity cases, edge cases)."""
+    return Workload(name, B=B, K=K, d=d, V=V, temperature=temperature, noise=noise, seed=seed)
+
+
+def _gen(device: torch.device, seed: int) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _randn(shape, g, device, chunk_rows: int = 16384) -> torch.Tensor:
+    """Standard normal fp32 drawn in row chunks (bounded scratch for big W)."""
+    out = torch.empty(shape, dtype=torch.float32, device=device)
+    rows = shape[0]
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        out[r0:r1] = torch.randn((r1 - r0,) + tuple(shape[1:]), generator=g, device=device)
+    return out
+
+
+def _randn_bf16(shape, scale: float, g, device, chunk_rows: int = 16384) -> torch.Tensor:
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    rows = shape[0]
+    for r0 in range(0, rows, chunk_rows):
+        r1 = min(rows, r0 + chunk_rows)
+        x = torch.randn((r1 - r0,) + tuple(shape[1:]), generator=g, device=device)
+        out[r0:r1] = (x * scale).to(torch.bfloat16)
+    return out
+
+
+def _project(x: torch.Tensor, W: torch.Tensor, chunk_rows: int = 16384) -> torch.Tensor:
+    """Draft-model stand-in: fp32 x times the bf16 weight (upcast), fp32 result.
+
+    Plain fp32 matmul with TF32 disabled; the result is an input of the verify
+    step, read byte-for-byte the same by the CUDA path and the oracle."""
+    prev = torch.get_float32_matmul_precision()
+    torch.set_float32_matmul_precision("highest")
+    try:
+        out = torch.empty((x.shape[0], W.shape[0]), dtype=torch.float32, device=x.device)
+        for v0 in range(0, W.shape[0], chunk_rows):
+            v1 = min(W.shape[0], v0 + chunk_rows)
+            out[:, v0:v1] = x @ W[v0:v1].float().t()
+        return out
+    finally:
+        torch.set_float32_matmul_precision(prev)
+
+
+def gumbel_max_tokens(logits: torch.Tensor, temperature: float, g: torch.Generator) -> torch.Tensor:
+    """Draw one token per row from softmax(logits / T) with the Gumbel-max trick."""
+    u = torch.rand(logits.shape, generator=g, device=logits.device, dtype=torch.float64)
+    u = u.clamp_min(1e-300)
+    gumbel = -torch.log(-torch.log(u))
+    return torch.argmax(logits.double() / temperature + gumbel, dim=-1).to(torch.int32)
+
+
+def make_inputs(w: Workload, device="cpu", seed: int | None = None) -> dict:
+    """All inputs of one verify call for workload ``w`` on ``device``.
+
+    Returns a dict with (absent keys are None):
+      hidden        bf16 [B*(K+1), d]   (row b*(K+1)+j is position j of sequence b)
+      W             bf16 [V, d]         (LM-head weight, nn.Linear layout)
+      target_logits fp32 [B*(K+1), V]   (tiny_logits only: the given z_p)
+      draft_logits  fp32 [B*K, V]       (T > 0)
+      draft_tokens  int32 [B, K]
+      uniforms      fp32 [B, K+1]       (T > 0)
+    """
+    device = torch.device(device)
+    g = _gen(device, w.seed if seed is None else seed)
+    B, K, d, V = w.B, w.K, w.d, w.V
+    out = dict(hidden=None, W=None, target_logits=None, draft_logits=None,
+               draft_tokens=None, uniforms=None)
+    if d == 0:
+        zp = _randn((B * (K + 1), V), g, device) * w.logit_std
+        zp3 = zp.view(B, K + 1, V)
+        eps = _randn((B * K, V), g, device).view(B, K, V)
+        zq = (zp3[:, :K, :] + w.draft_logit_noise * eps).reshape(B * K, V).contiguous()
+        out["target_logits"] = zp.contiguous()
+        draft_logits = zq
+    else:
+        h = _randn_bf16((B * (K + 1), d), 1.0, g, device)
+        W = _randn_bf16((V, d), 1.0 / math.sqrt(d), g, device)
+        out["hidden"], out["W"] = h, W
+        hk = h.view(B, K + 1, d)[:, :K, :].reshape(B * K, d).float()
+        eps = _randn((B * K, d), g, device) if B * K > 0 else torch.zeros((0, d), device=device)
+        draft_logits = _project(hk + w.noise * eps, W) if B * K > 0 else \
+            torch.zeros((0, V), dtype=torch.float32, device=device)
+    if w.greedy:
+        out["draft_tokens"] = torch.argmax(draft_logits, dim=-1).to(torch.int32).view(B, K).contiguous()
+    else:
+        out["draft_logits"] = draft_logits.contiguous()
+        if B * K > 0:
+            out["draft_tokens"] = gumbel_max_tokens(draft_logits, w.temperature, g).view(B, K).contiguous()
+        else:
+            out["draft_tokens"] = torch.zeros((B, 0), dtype=torch.int32, device=device)
+        out["uniforms"] = torch.rand((B, K + 1), generator=g, device=device, dtype=torch.float32)
+    return out
+
+
+def fresh_uniforms(B: int, K: int, count: int, device="cpu", seed: int = 99) -> torch.Tensor:
+    """``count`` independent sets of uniforms [count, B, K+1] (repeat draws over fixed logits)."""
+    g = _gen(torch.device(device), seed)
+    return torch.rand((count, B, K + 1), generator=g, device=device, dtype=torch.float32)
