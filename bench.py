@@ -1,0 +1,377 @@
+"""Benchmark of the verify-and-accept step on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one call of the whole step (LM head, softmax statistics, accept
+test, accepted prefix, residual / bonus draw) on one batch of the workload,
+inputs resident in HBM.  Prints ONE JSON line on rank 0.
+
+  value      verified positions/s = B*(K+1) per step per GPU, summed over GPUs
+  roofline   the LM-head kernel (dominant): algorithmic bytes per launch
+             (2*V*d weight + 2*M*d hidden + 4*M*V logits written) over its
+             CUDA-event launch time, against the measured HBM copy peak
+  e2e        the same metric through spec_verify_host: pinned host inputs
+             copied in and the tokens copied out inside the timed region
+  cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload
+
+With N > 1 (torchrun) every rank runs its own copy of the workload (the
+sequences of different ranks are independent problems): weak scaling, no
+collective on the data path; the ranks meet only for the barrier and the
+max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from speculative_decoding_verification_67_gb300 import synth  # noqa: E402
+
+METRIC = "verified positions/sec at V=128256; achieved HBM GB/s vs GB300 peak"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def step_bytes(w) -> dict:
+    """Algorithmic bytes of one step and of the LM-head launch."""
+    M, d, V, B, K = w.M, w.d, w.V, w.B, w.K
+    head = 2 * V * d + 2 * M * d + (0 if w.greedy else 4 * M * V)
+    step = head + (0 if w.greedy else 4 * B * K * V)
+    return dict(head=head, step=step, flops=2 * M * d * V)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_setup(n_gpus: int):
+    if n_gpus > 1 or int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        rank, world = dist.get_rank(), dist.get_world_size()
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        torch.cuda.set_device(local)
+        return rank, world, local
+    torch.cuda.set_device(0)
+    return 0, 1, 0
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def host_arrays(inp) -> dict:
+    """The workload's tensors as host numpy arrays for the oracle."""
+    out = {}
+    for k, v in inp.items():
+        if v is None:
+            out[k] = None
+        elif v.dtype in (torch.bfloat16, torch.float32):
+            out[k] = v.float().cpu().numpy()
+        else:
+            out[k] = v.cpu().numpy()
+    return out
+
+
+def oracle_one_sequence(w, a: dict, b: int) -> None:
+    """The oracle's whole step for sequence b of the workload."""
+    import oracle
+    K, V = w.K, w.V
+    rows = slice(b * (K + 1), (b + 1) * (K + 1))
+    zq = None if a["draft_logits"] is None else a["draft_logits"][b * K:(b + 1) * K]
+    u = None if a["uniforms"] is None else a["uniforms"][b:b + 1].astype("float64")
+    x = a["draft_tokens"][b:b + 1]
+    if w.d == 0:
+        oracle.verify_sampling(a["target_logits"][rows].reshape(1, K + 1, V), zq.reshape(1, K, V), x, u,
+                               w.temperature)
+    else:
+        oracle.spec_verify(a["hidden"][rows], a["W"], zq, x, u, w.temperature, 1, K)
+
+
+def cpu_oracle_sample(w, inp, budget_s: float = 12.0) -> dict:
+    """Time the fp64 oracle (as it stands) on whole sequences of the workload,
+    one at a time, until about `budget_s` of CPU work has been done."""
+    a = host_arrays(inp)
+    K, V = w.K, w.V
+    done_seqs, t0 = 0, time.perf_counter()
+    while True:
+        oracle_one_sequence(w, a, done_seqs % w.B)
+        done_seqs += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    try:
+        import threadpoolctl
+        threads = max((i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()), default=1)
+    except Exception:
+        threads = os.cpu_count()
+    return {"value": done_seqs * (K + 1) / el, "unit": "verified positions/s", "cores": threads,
+            "kind": "oracle", "sample": f"{done_seqs} whole sequences (K+1={K + 1} positions each, full V={V}) "
+                                        f"of {w.name}, {el:.1f} s, numpy fp64 on the host cores"}
+
+
+def run_reference(args, w, total_budget_s: float = 90.0):
+    """The oracle timed as the reference arm: every step is the oracle's whole
+    step for one sequence of the workload on a slice of the vocabulary sized
+    so that the whole --steps/--warmup run takes about total_budget_s; the
+    rate is scaled to full-vocabulary positions (the oracle's cost is linear
+    in V)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    if w.V * max(w.d, 1) <= 64 * 2**20 or not torch.cuda.is_available():
+        inp = synth.make_inputs(w, device="cpu")
+    else:
+        inp = {k: (v.cpu() if isinstance(v, torch.Tensor) else v)
+               for k, v in synth.make_inputs(w, device="cuda").items()}
+    a = host_arrays(inp)
+    K, V = w.K, w.V
+
+    def sliced(vs: int) -> dict:
+        out = dict(a)
+        if a["W"] is not None:
+            out["W"] = a["W"][:vs]
+        if a["target_logits"] is not None:
+            out["target_logits"] = a["target_logits"][:, :vs]
+        if a["draft_logits"] is not None:
+            out["draft_logits"] = a["draft_logits"][:, :vs]
+        out["draft_tokens"] = a["draft_tokens"] % vs
+        return out
+
+    probe = min(V, 8192)
+    t0 = time.perf_counter()
+    oracle_one_sequence(dataclasses_replace(w, V=probe), sliced(probe), 0)
+    per_elem = (time.perf_counter() - t0) / probe
+    per_step = total_budget_s / max(1, args.steps + args.warmup)
+    vs = int(min(V, max(1024, per_step / max(per_elem, 1e-12))))
+    ws, arr = dataclasses_replace(w, V=vs), sliced(vs)
+    for i in range(args.warmup):
+        oracle_one_sequence(ws, arr, i % w.B)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle_one_sequence(ws, arr, i % w.B)
+    el = time.perf_counter() - t0
+    value = args.steps * (K + 1) * (vs / V) / el
+    try:
+        import threadpoolctl
+        threads = max((i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()), default=1)
+    except Exception:
+        threads = os.cpu_count()
+    sample = (f"per step: the oracle's whole step for one sequence (K+1={K + 1} positions) on the first {vs} "
+              f"of V={V} vocabulary rows, rate scaled by V/{vs}")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "verified positions/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "K": w.K, "d": w.d, "V": w.V, "T": w.temperature,
+                       "step": sample},
+            "cpu_baseline": {"value": value, "unit": "verified positions/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "verified positions/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def dataclasses_replace(w, **kw):
+    import dataclasses
+    return dataclasses.replace(w, **kw)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="head_B8_K4_V128256", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import speculative_decoding_verification_67_gb300 as sv
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    inp = synth.make_inputs(w, device=dev, seed=w.seed + rank)
+    T = w.temperature
+    B, K, d, V, M = w.B, w.K, w.d, w.V, w.M
+    stream = torch.cuda.current_stream(dev)
+    ver = sv.Verifier(B, K, d, V, T, device=dev)
+
+    def step():
+        ver(inp["hidden"], inp["W"], inp["draft_logits"], inp["draft_tokens"], inp["uniforms"], stream=stream)
+
+    peak_gbs, peak_tf, peak_kind = load_peaks()
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    ms = max_over_ranks(ms, world)
+    ms_per_step = ms / args.steps
+    value = world * M * args.steps / (ms / 1e3)
+
+    # dominant kernel alone: the LM head, same shapes, same stream, CUDA events
+    logits = torch.empty((M, V), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        sv.spec_lm_head(inp["hidden"], inp["W"], logits, stream=stream)
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    head_iters = max(20, min(args.steps, 500))
+    h0.record(stream)
+    for _ in range(head_iters):
+        sv.spec_lm_head(inp["hidden"], inp["W"], logits, stream=stream)
+    h1.record(stream)
+    torch.cuda.synchronize()
+    head_ms = h0.elapsed_time(h1) / head_iters
+    nb = step_bytes(w)
+    head_bytes = 2 * V * d + 2 * M * d + 4 * M * V   # logits mode, as timed here
+    achieved = head_bytes / (head_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak_gbs, "unit": "GB/s", "frac": achieved / peak_gbs,
+                "traffic": None, "kernel": "head_kernel (LM head, logits epilogue)",
+                "launch_ms": head_ms, "bytes_per_launch": head_bytes, "peak_kind": peak_kind}
+    if w.greedy:
+        flops = nb["flops"]
+        tf = flops / (ms_per_step * 1e-3) / 1e12
+        roofline_step = {"bound": "tensor", "achieved_tflops": tf, "peak_tflops": peak_tf, "frac": tf / peak_tf}
+    else:
+        gbs = nb["step"] / (ms_per_step * 1e-3) / 1e9
+        roofline_step = {"bound": "hbm", "achieved_gbs": gbs, "peak_gbs": peak_gbs, "frac": gbs / peak_gbs,
+                         "bytes_per_step": nb["step"]}
+
+    # end to end through the host-buffer entry point
+    host = {k: (v.cpu().pin_memory() if isinstance(v, torch.Tensor) and k != "W" else v) for k, v in inp.items()}
+    out_t = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    out_n = torch.empty((B,), dtype=torch.int32).pin_memory()
+    hws = torch.empty(sv.host_workspace_bytes(B, K, d, V, T), dtype=torch.uint8, device=dev)
+
+    def e2e_step():
+        sv.spec_verify_host(host["hidden"], inp["W"], host["draft_logits"], host["draft_tokens"], host["uniforms"], T,
+                            workspace=hws, out_tokens=out_t, out_num_accepted=out_n, stream=stream)
+
+    for _ in range(3):
+        e2e_step()
+    e2e_steps = max(10, min(args.steps, 500))
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    h2d = M * d * 2 + B * K * 4 + (0 if w.greedy else B * K * V * 4 + M * 4)
+    d2h = M * 4 + B * 4
+    e2e = {"value": world * M * e2e_steps / e2e_s, "unit": "verified positions/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": e2e_steps, "ms_per_step": 1e3 * e2e_s / e2e_steps,
+           "timer": "host wall clock around spec_verify_host (which synchronises)"}
+
+    # tokens committed per step (the pages' measure of useful work)
+    tok, n = ver(inp["hidden"], inp["W"], inp["draft_logits"], inp["draft_tokens"], inp["uniforms"], stream=stream)
+    torch.cuda.synchronize()
+    committed = int((n.clamp_min(0) + 1).sum().item())
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "verified positions/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "K": K, "d": d, "V": V, "T": T, "positions_per_step": M,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": f"inputs exceed L2: W_lm {2 * V * d / 1e9:.2f} GB is streamed every step"},
+        "tokens_committed_per_s": world * committed * args.steps / (ms / 1e3),
+        "mean_accepted": float(n.float().mean().item()),
+        "roofline": roofline, "roofline_step": roofline_step,
+        "e2e": e2e, "gpu_launches": args.steps * (2 if w.greedy else 3), "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(w, inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,260 @@
+"""Target-side verify-and-accept step of speculative decoding on one GB300.
+
+Python binding of the C-ABI library ``libspec_verify.so`` (declared in
+``include/spec_verify.h``).  The functions here only check and marshal
+arguments (torch tensors -> device pointers, the current CUDA stream); every
+step of the computation runs in the library's sm_103a kernels.  There is no
+fallback: if the library has not been built, every call raises.
+
+Names follow the C ABI:
+
+* :func:`spec_verify` -- LM head + verify-and-accept from hidden states;
+* :func:`spec_verify_from_logits` -- verify-and-accept on given logits;
+* :func:`spec_lm_head` -- the LM-head contraction alone;
+* :func:`spec_verify_host` -- :func:`spec_verify` with host (CPU) tensors;
+* :func:`read_error` -- the device error word of a workspace.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "SPEC_DEBUG_FIELDS", "SpecError", "library", "workspace_bytes", "host_workspace_bytes",
+    "spec_verify", "spec_verify_from_logits", "spec_lm_head", "spec_verify_host", "read_error",
+    "Verifier",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspec_verify.so")
+SPEC_DEBUG_FIELDS = 6
+DEVERR_TOKEN_RANGE, DEVERR_NONFINITE, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+
+
+class SpecDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("K", ctypes.c_int32), ("d", ctypes.c_int32), ("V", ctypes.c_int32)]
+
+
+class SpecError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+_lib = None
+
+_VP, _I32, _F32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "spec_abi_version": (_I32, []),
+    "spec_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "spec_verify_workspace_bytes": (_SZ, [SpecDims, _F32, _I32]),
+    "spec_verify": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _SZ, _VP, _VP, _VP]),
+    "spec_verify_from_logits": (ctypes.c_int, [_VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _SZ, _VP, _VP]),
+    "spec_lm_head": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, _VP]),
+    "spec_verify_host_workspace_bytes": (_SZ, [SpecDims, _F32]),
+    "spec_verify_host": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _SZ, _VP]),
+    "spec_verify_read_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32), _VP]),
+}
+
+
+def library() -> ctypes.CDLL:
+    """The loaded C-ABI library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()' "
+                "or python -m speculative_decoding_verification_67_gb300._build)")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        msg = library().spec_status_string(status).decode()
+        raise SpecError(status, msg)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(None if t is None else t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype, shape, device=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device == "cuda" and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device == "cpu" and t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    return t
+
+
+def workspace_bytes(B: int, K: int, V: int, temperature: float, logits_in_workspace: bool = True) -> int:
+    n = library().spec_verify_workspace_bytes(SpecDims(B, K, 0, V), float(temperature), int(logits_in_workspace))
+    if n == 0:
+        raise ValueError("invalid sizes")
+    return int(n)
+
+
+def host_workspace_bytes(B: int, K: int, d: int, V: int, temperature: float) -> int:
+    n = library().spec_verify_host_workspace_bytes(SpecDims(B, K, d, V), float(temperature))
+    if n == 0:
+        raise ValueError("invalid sizes")
+    return int(n)
+
+
+def _outputs(B, K, device, out_tokens, out_num_accepted):
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=device)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=device)
+    _need(out_tokens, "out_tokens", torch.int32, (B, K + 1), "cuda")
+    _need(out_num_accepted, "out_num_accepted", torch.int32, (B,), "cuda")
+    return out_tokens, out_num_accepted
+
+
+def spec_verify(hidden, W_lm, draft_logits, draft_tokens, uniforms, temperature: float, *,
+                out_tokens=None, out_num_accepted=None, workspace=None, out_target_logits=None,
+                out_debug=None, stream=None):
+    """LM head + verify-and-accept.  hidden bf16 [B*(K+1), d], W_lm bf16 [V, d],
+    draft_logits f32 [B*K, V] (None when temperature == 0), draft_tokens int32
+    [B, K], uniforms f32 [B, K+1] (None when temperature == 0).
+    Returns (out_tokens int32 [B, K+1], out_num_accepted int32 [B])."""
+    B, K = draft_tokens.shape
+    V, d = W_lm.shape
+    T = float(temperature)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, K), "cuda")
+    _need(hidden, "hidden", torch.bfloat16, (B * (K + 1), d), "cuda")
+    _need(W_lm, "W_lm", torch.bfloat16, (V, d), "cuda")
+    if T > 0:
+        _need(draft_logits, "draft_logits", torch.float32, (B * K, V), "cuda")
+        _need(uniforms, "uniforms", torch.float32, (B, K + 1), "cuda")
+    if out_target_logits is not None:
+        _need(out_target_logits, "out_target_logits", torch.float32, (B * (K + 1), V), "cuda")
+    if out_debug is not None:
+        _need(out_debug, "out_debug", torch.float32, (B, K + 1, SPEC_DEBUG_FIELDS), "cuda")
+    out_tokens, out_num_accepted = _outputs(B, K, hidden.device, out_tokens, out_num_accepted)
+    need = library().spec_verify_workspace_bytes(SpecDims(B, K, d, V), T, int(out_target_logits is None))
+    if workspace is None:
+        workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=hidden.device)
+    _check(library().spec_verify(
+        _ptr(hidden), _ptr(W_lm), _ptr(draft_logits if T > 0 else None), _ptr(draft_tokens if K > 0 else None),
+        _ptr(uniforms if T > 0 else None), T, _ptr(out_tokens), _ptr(out_num_accepted), SpecDims(B, K, d, V),
+        _ptr(workspace), workspace.numel(), _ptr(out_target_logits), _ptr(out_debug), _stream(stream)))
+    return out_tokens, out_num_accepted
+
+
+def spec_verify_from_logits(target_logits, draft_logits, draft_tokens, uniforms, temperature: float, *,
+                            out_tokens=None, out_num_accepted=None, workspace=None, out_debug=None,
+                            stream=None):
+    """Verify-and-accept on given target logits f32 [B*(K+1), V]."""
+    B, K = draft_tokens.shape
+    V = target_logits.shape[1]
+    T = float(temperature)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, K), "cuda")
+    _need(target_logits, "target_logits", torch.float32, (B * (K + 1), V), "cuda")
+    if T > 0:
+        _need(draft_logits, "draft_logits", torch.float32, (B * K, V), "cuda")
+        _need(uniforms, "uniforms", torch.float32, (B, K + 1), "cuda")
+    if out_debug is not None:
+        _need(out_debug, "out_debug", torch.float32, (B, K + 1, SPEC_DEBUG_FIELDS), "cuda")
+    out_tokens, out_num_accepted = _outputs(B, K, target_logits.device, out_tokens, out_num_accepted)
+    need = library().spec_verify_workspace_bytes(SpecDims(B, K, 0, V), T, 0)
+    if workspace is None:
+        workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=target_logits.device)
+    _check(library().spec_verify_from_logits(
+        _ptr(target_logits), _ptr(draft_logits if T > 0 else None), _ptr(draft_tokens if K > 0 else None),
+        _ptr(uniforms if T > 0 else None), T, _ptr(out_tokens), _ptr(out_num_accepted), SpecDims(B, K, 0, V),
+        _ptr(workspace), workspace.numel(), _ptr(out_debug), _stream(stream)))
+    return out_tokens, out_num_accepted
+
+
+def spec_lm_head(hidden, W_lm, logits=None, stream=None):
+    """logits f32 [M, V] = hidden bf16 [M, d] @ W_lm bf16 [V, d]^T."""
+    M, d = hidden.shape
+    V = W_lm.shape[0]
+    _need(hidden, "hidden", torch.bfloat16, (M, d), "cuda")
+    _need(W_lm, "W_lm", torch.bfloat16, (V, d), "cuda")
+    if logits is None:
+        logits = torch.empty((M, V), dtype=torch.float32, device=hidden.device)
+    _need(logits, "logits", torch.float32, (M, V), "cuda")
+    _check(library().spec_lm_head(_ptr(hidden), _ptr(W_lm), _ptr(logits), M, d, V, _stream(stream)))
+    return logits
+
+
+def spec_verify_host(hidden, W_lm, draft_logits, draft_tokens, uniforms, temperature: float, *,
+                     workspace=None, out_tokens=None, out_num_accepted=None, stream=None):
+    """spec_verify with the per-step tensors (hidden, draft_logits, draft_tokens,
+    uniforms) and the outputs in host memory (pin them for asynchronous
+    copies); W_lm stays on the device.  Returns host tensors once they are
+    ready."""
+    B, K = draft_tokens.shape
+    V, d = W_lm.shape
+    T = float(temperature)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, K), "cpu")
+    _need(hidden, "hidden", torch.bfloat16, (B * (K + 1), d), "cpu")
+    _need(W_lm, "W_lm", torch.bfloat16, (V, d), "cuda")
+    if T > 0:
+        _need(draft_logits, "draft_logits", torch.float32, (B * K, V), "cpu")
+        _need(uniforms, "uniforms", torch.float32, (B, K + 1), "cpu")
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32).pin_memory()
+    _need(out_tokens, "out_tokens", torch.int32, (B, K + 1), "cpu")
+    _need(out_num_accepted, "out_num_accepted", torch.int32, (B,), "cpu")
+    if workspace is None:
+        workspace = torch.empty(host_workspace_bytes(B, K, d, V, T), dtype=torch.uint8, device=W_lm.device)
+    _check(library().spec_verify_host(
+        _ptr(hidden), _ptr(W_lm), _ptr(draft_logits if T > 0 else None), _ptr(draft_tokens if K > 0 else None),
+        _ptr(uniforms if T > 0 else None), T, _ptr(out_tokens), _ptr(out_num_accepted), SpecDims(B, K, d, V),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out_tokens, out_num_accepted
+
+
+def read_error(workspace, stream=None) -> int:
+    """Synchronises the stream and returns the workspace's device error word."""
+    word = ctypes.c_int32(0)
+    st = library().spec_verify_read_error(_ptr(workspace), ctypes.byref(word), _stream(stream))
+    if st not in (0, 7):
+        _check(st)
+    return int(word.value)
+
+
+class Verifier:
+    """Holds a workspace (and output buffers) sized for one shape, for
+    repeated calls of :func:`spec_verify` without per-call allocation."""
+
+    def __init__(self, B: int, K: int, d: int, V: int, temperature: float, device="cuda",
+                 keep_logits: bool = False):
+        self.B, self.K, self.d, self.V, self.T = B, K, d, V, float(temperature)
+        self.target_logits = (torch.empty((B * (K + 1), V), dtype=torch.float32, device=device)
+                              if keep_logits and self.T > 0 else None)
+        n = library().spec_verify_workspace_bytes(SpecDims(B, K, d, V), self.T, int(self.target_logits is None))
+        self.workspace = torch.empty(max(int(n), 16), dtype=torch.uint8, device=device)
+        self.out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=device)
+        self.out_num_accepted = torch.empty((B,), dtype=torch.int32, device=device)
+
+    def __call__(self, hidden, W_lm, draft_logits, draft_tokens, uniforms, out_debug=None, stream=None):
+        return spec_verify(hidden, W_lm, draft_logits, draft_tokens, uniforms, self.T,
+                           out_tokens=self.out_tokens, out_num_accepted=self.out_num_accepted,
+                           workspace=self.workspace, out_target_logits=self.target_logits,
+                           out_debug=out_debug, stream=stream)

@@ -1,0 +1,374 @@
+// C ABI of the verify-and-accept step: argument checks, workspace layout and
+// the launch sequence.  Declared in include/spec_verify.h.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "spec_verify.h"
+
+namespace {
+
+using sv::DeviceInfo;
+
+constexpr size_t kAlign = 256;
+constexpr int kAbiVersion = 1;
+constexpr int kMaxRows = 65535;  // grid.y of the per-row passes
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Workspace layout.  The control block (error word, tickets) is zeroed by a
+// memset at the start of every call; everything else is written before it
+// is read.
+struct Layout {
+  size_t ctrl_bytes = 0;
+  size_t seq = 0, parts = 0, res = 0, logits = 0;  // sampling
+  size_t pmax = 0, pidx = 0, gscratch = 0;         // greedy
+  int CA = 0, CB = 0, P = 0;
+  size_t total = 0;
+};
+
+// int[0] error word, int[1] greedy ticket, int[2 .. 2+B) tickets of pass 1,
+// int[2+B .. 2+2B) tickets of pass 2.
+constexpr int kCtrlErr = 0, kCtrlGreedyTicket = 1, kCtrlTickets = 2;
+
+Layout make_layout(int B, int K, int V, bool greedy, bool logits_in_ws, bool from_logits) {
+  Layout L;
+  const size_t M = static_cast<size_t>(B) * (K + 1);
+  size_t off = round_up(sizeof(int) * (kCtrlTickets + 2 * static_cast<size_t>(B)));
+  L.ctrl_bytes = off;
+  if (!greedy) {
+    L.CA = (V + sv::kRowChunk - 1) / sv::kRowChunk;
+    L.CB = (V + sv::kResChunk - 1) / sv::kResChunk;
+    const size_t R = M + static_cast<size_t>(B) * K;
+    L.seq = off;
+    off += round_up(sizeof(sv::SeqState) * B);
+    L.parts = off;
+    off += round_up(sizeof(sv::RowPart) * R * L.CA);
+    L.res = off;
+    off += round_up(sizeof(double) * static_cast<size_t>(B) * L.CB);
+    if (logits_in_ws) {
+      L.logits = off;
+      off += round_up(sizeof(float) * M * static_cast<size_t>(V));
+    }
+  } else {
+    L.P = from_logits ? (V + sv::kRowChunk - 1) / sv::kRowChunk : (V + sv::kHeadTileV - 1) / sv::kHeadTileV;
+    L.pmax = off;
+    off += round_up(sizeof(float) * static_cast<size_t>(L.P) * M);
+    L.pidx = off;
+    off += round_up(sizeof(int) * static_cast<size_t>(L.P) * M);
+    L.gscratch = off;
+    off += round_up(sv::greedy_scratch_bytes(static_cast<int>(M)));
+  }
+  L.total = off;
+  return L;
+}
+
+bool dims_ok(const spec_dims& d, bool need_head) {
+  if (d.B < 1 || d.K < 0 || d.K > sv::kMaxK || d.V < 1) return false;
+  const long long M = static_cast<long long>(d.B) * (d.K + 1);
+  const long long R = M + static_cast<long long>(d.B) * d.K;
+  if (R > kMaxRows) return false;
+  if (static_cast<long long>(d.V) * M > (1ll << 40)) return false;
+  if (need_head && (d.d < 8 || d.d % 8 != 0 || d.d > (1 << 20))) return false;
+  return true;
+}
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+spec_status current_device(DeviceInfo& out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return SPEC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (di.device < 0) {
+    DeviceInfo t;
+    t.device = dev;
+    if (cudaDeviceGetAttribute(&t.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    di = t;
+  }
+  out = di;
+  if (out.cc_major != 10 || out.cc_minor != 3) return SPEC_ERR_ARCH;
+  return SPEC_OK;
+}
+
+spec_status check_sampling_inputs(const spec_dims& d, float T, const float* draft_logits,
+                                  const int32_t* draft_tokens, const float* uniforms, const int32_t* out_tokens,
+                                  const int32_t* out_n, const float* out_debug) {
+  if (!(T >= 0.f) || !std::isfinite(T)) return SPEC_ERR_ARG;
+  if (!out_tokens || !out_n) return SPEC_ERR_ARG;
+  if (d.K > 0 && !draft_tokens) return SPEC_ERR_ARG;
+  if (T > 0.f) {
+    if (!uniforms) return SPEC_ERR_ARG;
+    if (d.K > 0 && !draft_logits) return SPEC_ERR_ARG;
+    if (draft_logits && !aligned(draft_logits, 16)) return SPEC_ERR_ALIGN;
+    if (!aligned(uniforms, 4)) return SPEC_ERR_ALIGN;
+  }
+  if ((draft_tokens && !aligned(draft_tokens, 4)) || !aligned(out_tokens, 4) || !aligned(out_n, 4) ||
+      (out_debug && !aligned(out_debug, 4)))
+    return SPEC_ERR_ALIGN;
+  return SPEC_OK;
+}
+
+sv::VerifyArgs sampling_args(const Layout& L, const spec_dims& d, float T, const float* zp, const float* zq,
+                             const int32_t* x, const float* u, int32_t* out_tokens, int32_t* out_n,
+                             float* out_debug, char* ws) {
+  sv::VerifyArgs a;
+  a.B = d.B;
+  a.K = d.K;
+  a.V = d.V;
+  a.T = T;
+  a.zp = zp;
+  a.zq = zq;
+  a.x = x;
+  a.u = u;
+  a.out_tokens = out_tokens;
+  a.out_n = out_n;
+  a.out_debug = out_debug;
+  int* ctrl = reinterpret_cast<int*>(ws);
+  a.err = ctrl + kCtrlErr;
+  a.tickets_a = reinterpret_cast<unsigned*>(ctrl + kCtrlTickets);
+  a.tickets_b = reinterpret_cast<unsigned*>(ctrl + kCtrlTickets + d.B);
+  a.parts = reinterpret_cast<sv::RowPart*>(ws + L.parts);
+  a.seq = reinterpret_cast<sv::SeqState*>(ws + L.seq);
+  a.res_sums = reinterpret_cast<double*>(ws + L.res);
+  a.CA = L.CA;
+  a.CB = L.CB;
+  return a;
+}
+
+sv::GreedyArgs greedy_args(const Layout& L, const spec_dims& d, const int32_t* x, int32_t* out_tokens,
+                           int32_t* out_n, float* out_debug, char* ws) {
+  sv::GreedyArgs g;
+  g.B = d.B;
+  g.K = d.K;
+  g.V = d.V;
+  g.P = L.P;
+  g.part_max = reinterpret_cast<const float*>(ws + L.pmax);
+  g.part_idx = reinterpret_cast<const int*>(ws + L.pidx);
+  g.x = x;
+  g.out_tokens = out_tokens;
+  g.out_n = out_n;
+  g.out_debug = out_debug;
+  g.err = reinterpret_cast<int*>(ws) + kCtrlErr;
+  return g;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t spec_abi_version(void) { return kAbiVersion; }
+
+const char* spec_status_string(spec_status s) {
+  switch (s) {
+    case SPEC_OK: return "SPEC_OK";
+    case SPEC_ERR_ARG: return "SPEC_ERR_ARG: invalid argument (null pointer or temperature)";
+    case SPEC_ERR_DIMS: return "SPEC_ERR_DIMS: size out of range";
+    case SPEC_ERR_ALIGN: return "SPEC_ERR_ALIGN: misaligned pointer or hidden size";
+    case SPEC_ERR_WORKSPACE: return "SPEC_ERR_WORKSPACE: workspace missing or too small";
+    case SPEC_ERR_CUDA: return "SPEC_ERR_CUDA: CUDA call failed";
+    case SPEC_ERR_ARCH: return "SPEC_ERR_ARCH: current device is not sm_103 (GB300)";
+    case SPEC_ERR_DEVICE_INPUT: return "SPEC_ERR_DEVICE_INPUT: invalid input found on the device";
+  }
+  return "SPEC_ERR_UNKNOWN";
+}
+
+size_t spec_verify_workspace_bytes(spec_dims dims, float temperature, int32_t logits_in_workspace) {
+  if (!dims_ok(dims, false) || !(temperature >= 0.f)) return 0;
+  return make_layout(dims.B, dims.K, dims.V, temperature == 0.f, logits_in_workspace != 0, false).total;
+}
+
+spec_status spec_verify(const void* hidden, const void* W_lm, const float* draft_logits,
+                        const int32_t* draft_tokens, const float* uniforms, float temperature,
+                        int32_t* out_tokens, int32_t* out_num_accepted, spec_dims dims, void* workspace,
+                        size_t workspace_bytes, float* out_target_logits, float* out_debug,
+                        spec_stream_t stream) {
+  if (!dims_ok(dims, true)) return SPEC_ERR_DIMS;
+  if (!hidden || !W_lm) return SPEC_ERR_ARG;
+  if (!aligned(hidden, 16) || !aligned(W_lm, 16)) return SPEC_ERR_ALIGN;
+  spec_status st = check_sampling_inputs(dims, temperature, draft_logits, draft_tokens, uniforms, out_tokens,
+                                         out_num_accepted, out_debug);
+  if (st != SPEC_OK) return st;
+  const bool greedy = temperature == 0.f;
+  if (greedy && out_target_logits) return SPEC_ERR_ARG;
+  if (out_target_logits && !aligned(out_target_logits, 16)) return SPEC_ERR_ALIGN;
+  const Layout L = make_layout(dims.B, dims.K, dims.V, greedy, !greedy && !out_target_logits, false);
+  if (!workspace || workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return SPEC_ERR_ALIGN;
+  DeviceInfo dev;
+  st = current_device(dev);
+  if (st != SPEC_OK) return st;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const int M = dims.B * (dims.K + 1);
+  if (cudaMemsetAsync(ws, 0, L.ctrl_bytes, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  int* err = reinterpret_cast<int*>(ws) + kCtrlErr;
+  bool enc_fail = false;
+  cudaError_t e;
+  if (greedy) {
+    e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kArgmax, nullptr,
+                        reinterpret_cast<float*>(ws + L.pmax), reinterpret_cast<int*>(ws + L.pidx), err, dev, s,
+                        &enc_fail);
+    if (enc_fail) return SPEC_ERR_CUDA;
+    if (e != cudaSuccess) return SPEC_ERR_CUDA;
+    const sv::GreedyArgs g = greedy_args(L, dims, draft_tokens, out_tokens, out_num_accepted, out_debug, ws);
+    e = sv::launch_greedy_finish_ws(g, ws + L.gscratch, reinterpret_cast<unsigned*>(ws) + kCtrlGreedyTicket, s);
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  }
+  float* logits = out_target_logits ? out_target_logits : reinterpret_cast<float*>(ws + L.logits);
+  e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kLogits, logits, nullptr, nullptr, err, dev,
+                      s, &enc_fail);
+  if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
+  const sv::VerifyArgs a = sampling_args(L, dims, temperature, logits, draft_logits, draft_tokens, uniforms,
+                                         out_tokens, out_num_accepted, out_debug, ws);
+  e = sv::launch_verify_sampling(a, s);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status spec_verify_from_logits(const float* target_logits, const float* draft_logits,
+                                    const int32_t* draft_tokens, const float* uniforms, float temperature,
+                                    int32_t* out_tokens, int32_t* out_num_accepted, spec_dims dims,
+                                    void* workspace, size_t workspace_bytes, float* out_debug,
+                                    spec_stream_t stream) {
+  if (!dims_ok(dims, false)) return SPEC_ERR_DIMS;
+  if (!target_logits) return SPEC_ERR_ARG;
+  if (!aligned(target_logits, 16)) return SPEC_ERR_ALIGN;
+  spec_status st = check_sampling_inputs(dims, temperature, draft_logits, draft_tokens, uniforms, out_tokens,
+                                         out_num_accepted, out_debug);
+  if (st != SPEC_OK) return st;
+  const bool greedy = temperature == 0.f;
+  const Layout L = make_layout(dims.B, dims.K, dims.V, greedy, false, true);
+  if (!workspace || workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return SPEC_ERR_ALIGN;
+  DeviceInfo dev;
+  st = current_device(dev);
+  if (st != SPEC_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  if (cudaMemsetAsync(ws, 0, L.ctrl_bytes, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaError_t e;
+  if (greedy) {
+    const int M = dims.B * (dims.K + 1);
+    e = sv::launch_row_argmax(target_logits, M, dims.V, reinterpret_cast<float*>(ws + L.pmax),
+                              reinterpret_cast<int*>(ws + L.pidx), s);
+    if (e != cudaSuccess) return SPEC_ERR_CUDA;
+    const sv::GreedyArgs g = greedy_args(L, dims, draft_tokens, out_tokens, out_num_accepted, out_debug, ws);
+    e = sv::launch_greedy_finish_ws(g, ws + L.gscratch, reinterpret_cast<unsigned*>(ws) + kCtrlGreedyTicket, s);
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  }
+  const sv::VerifyArgs a = sampling_args(L, dims, temperature, target_logits, draft_logits, draft_tokens,
+                                         uniforms, out_tokens, out_num_accepted, out_debug, ws);
+  e = sv::launch_verify_sampling(a, s);
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status spec_lm_head(const void* hidden, const void* W_lm, float* logits, int32_t M, int32_t d, int32_t V,
+                         spec_stream_t stream) {
+  if (M < 1 || M > kMaxRows || V < 1 || d < 8 || d % 8 != 0 || d > (1 << 20)) return SPEC_ERR_DIMS;
+  if (!hidden || !W_lm || !logits) return SPEC_ERR_ARG;
+  if (!aligned(hidden, 16) || !aligned(W_lm, 16) || !aligned(logits, 16)) return SPEC_ERR_ALIGN;
+  DeviceInfo dev;
+  spec_status st = current_device(dev);
+  if (st != SPEC_OK) return st;
+  bool enc_fail = false;
+  const cudaError_t e = sv::launch_head(hidden, W_lm, M, d, V, sv::HeadOut::kLogits, logits, nullptr, nullptr,
+                                        nullptr, dev, reinterpret_cast<cudaStream_t>(stream), &enc_fail);
+  if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+// Host-buffer variant: staging areas follow the regular workspace.
+namespace {
+struct HostStage {
+  size_t base = 0, hidden = 0, dl = 0, tok = 0, u = 0, out_tok = 0, out_n = 0, total = 0;
+};
+HostStage host_stage(const spec_dims& d, float T) {
+  HostStage h;
+  const bool greedy = T == 0.f;
+  const size_t M = static_cast<size_t>(d.B) * (d.K + 1);
+  size_t off = make_layout(d.B, d.K, d.V, greedy, !greedy, false).total;
+  h.base = off;
+  h.hidden = off;
+  off += round_up(M * static_cast<size_t>(d.d) * 2);
+  h.dl = off;
+  if (!greedy) off += round_up(static_cast<size_t>(d.B) * d.K * static_cast<size_t>(d.V) * 4);
+  h.tok = off;
+  off += round_up(static_cast<size_t>(d.B) * d.K * 4 + 4);
+  h.u = off;
+  if (!greedy) off += round_up(M * 4);
+  h.out_tok = off;
+  off += round_up(M * 4);
+  h.out_n = off;
+  off += round_up(static_cast<size_t>(d.B) * 4);
+  h.total = off;
+  return h;
+}
+}  // namespace
+
+size_t spec_verify_host_workspace_bytes(spec_dims dims, float temperature) {
+  if (!dims_ok(dims, true) || !(temperature >= 0.f)) return 0;
+  return host_stage(dims, temperature).total;
+}
+
+spec_status spec_verify_host(const void* hidden_host, const void* W_lm_device, const float* draft_logits_host,
+                             const int32_t* draft_tokens_host, const float* uniforms_host, float temperature,
+                             int32_t* out_tokens_host, int32_t* out_num_accepted_host, spec_dims dims,
+                             void* device_workspace, size_t workspace_bytes, spec_stream_t stream) {
+  if (!dims_ok(dims, true)) return SPEC_ERR_DIMS;
+  if (!hidden_host || !W_lm_device || !out_tokens_host || !out_num_accepted_host) return SPEC_ERR_ARG;
+  if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SPEC_ERR_ARG;
+  const bool greedy = temperature == 0.f;
+  if (dims.K > 0 && !draft_tokens_host) return SPEC_ERR_ARG;
+  if (!greedy && (!uniforms_host || (dims.K > 0 && !draft_logits_host))) return SPEC_ERR_ARG;
+  const HostStage h = host_stage(dims, temperature);
+  if (!device_workspace || workspace_bytes < h.total) return SPEC_ERR_WORKSPACE;
+  if (!aligned(device_workspace, 16)) return SPEC_ERR_ALIGN;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(device_workspace);
+  const size_t M = static_cast<size_t>(dims.B) * (dims.K + 1);
+  const size_t nx = static_cast<size_t>(dims.B) * dims.K;
+  if (cudaMemcpyAsync(ws + h.hidden, hidden_host, M * dims.d * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (nx > 0 && cudaMemcpyAsync(ws + h.tok, draft_tokens_host, nx * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (!greedy) {
+    if (nx > 0 && cudaMemcpyAsync(ws + h.dl, draft_logits_host, nx * static_cast<size_t>(dims.V) * 4,
+                                  cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    if (cudaMemcpyAsync(ws + h.u, uniforms_host, M * 4, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+  }
+  spec_status st = spec_verify(ws + h.hidden, W_lm_device, greedy ? nullptr : reinterpret_cast<float*>(ws + h.dl),
+                               nx > 0 ? reinterpret_cast<int32_t*>(ws + h.tok) : nullptr,
+                               greedy ? nullptr : reinterpret_cast<float*>(ws + h.u), temperature,
+                               reinterpret_cast<int32_t*>(ws + h.out_tok), reinterpret_cast<int32_t*>(ws + h.out_n),
+                               dims, ws, h.base, nullptr, nullptr, stream);
+  if (st != SPEC_OK) return st;
+  if (cudaMemcpyAsync(out_tokens_host, ws + h.out_tok, M * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(out_num_accepted_host, ws + h.out_n, static_cast<size_t>(dims.B) * 4,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+spec_status spec_verify_read_error(const void* workspace, int32_t* error_word, spec_stream_t stream) {
+  if (!workspace || !error_word) return SPEC_ERR_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaMemcpy(error_word, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return *error_word == 0 ? SPEC_OK : SPEC_ERR_DEVICE_INPUT;
+}
+
+}  // extern "C"

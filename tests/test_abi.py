@@ -1,0 +1,91 @@
+"""The C-ABI library: it builds for sm_103a, loads without a GPU, exports every
+symbol include/spec_verify.h declares, and rejects bad host-side arguments
+before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_67_gb300 as sv
+from speculative_decoding_verification_67_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return sv.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SPEC_API\s+[\w\s\*]*?\b(spec_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 9, names
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.spec_abi_version() == 1
+    for s in range(8):
+        assert lib.spec_status_string(s).decode().startswith("SPEC_")
+    assert lib.spec_status_string(99).decode() == "SPEC_ERR_UNKNOWN"
+
+
+def test_workspace_sizes(lib):
+    small = sv.workspace_bytes(1, 4, 1000, 1.0, logits_in_workspace=False)
+    with_logits = sv.workspace_bytes(1, 4, 1000, 1.0, logits_in_workspace=True)
+    assert with_logits - small >= 5 * 1000 * 4
+    greedy = sv.workspace_bytes(256, 4, 128256, 0.0)
+    assert greedy >= 1280 * ((128256 + 127) // 128) * 8
+    assert lib.spec_verify_workspace_bytes(sv.SpecDims(0, 4, 0, 1000), 1.0, 1) == 0
+    assert lib.spec_verify_workspace_bytes(sv.SpecDims(1, 33, 0, 1000), 1.0, 1) == 0
+    assert lib.spec_verify_workspace_bytes(sv.SpecDims(1, 4, 0, 1000), -1.0, 1) == 0
+
+
+def _fake(addr):
+    return ctypes.c_void_p(addr)
+
+
+def test_host_side_argument_errors(lib):
+    """Errors that are returned before any CUDA call (safe without a GPU)."""
+    good = _fake(0x10000)
+    d = sv.SpecDims(2, 3, 64, 1000)
+    ws = sv.workspace_bytes(2, 3, 1000, 0.8)
+    args = lambda **kw: dict(dict(h=good, W=good, dl=good, x=good, u=good, T=0.8, ot=good, on=good, dims=d,
+                                  ws=good, nws=ws, otl=_fake(None), dbg=_fake(None), s=_fake(None)), **kw)
+
+    def call(**kw):
+        a = args(**kw)
+        return lib.spec_verify(a["h"], a["W"], a["dl"], a["x"], a["u"], a["T"], a["ot"], a["on"], a["dims"],
+                               a["ws"], a["nws"], a["otl"], a["dbg"], a["s"])
+
+    assert call(dims=sv.SpecDims(0, 3, 64, 1000)) == 2          # B < 1
+    assert call(dims=sv.SpecDims(2, 40, 64, 1000)) == 2         # K > 32
+    assert call(dims=sv.SpecDims(2, 3, 60, 1000)) == 2          # d % 8
+    assert call(h=_fake(None)) == 1                              # null hidden
+    assert call(h=_fake(0x10008)) == 3                           # misaligned
+    assert call(T=float("nan")) == 1
+    assert call(T=-1.0) == 1
+    assert call(dl=_fake(None)) == 1                             # sampling needs draft logits
+    assert call(u=_fake(None)) == 1
+    assert call(ws=_fake(None)) == 4
+    assert call(nws=ws - 1) == 4
+    assert call(T=0.0, otl=good) == 1                            # greedy never writes logits
+    assert lib.spec_lm_head(good, good, good, 0, 64, 1000, _fake(None)) == 2
+    assert lib.spec_lm_head(good, good, _fake(None), 4, 64, 1000, _fake(None)) == 1
+    assert lib.spec_verify_from_logits(_fake(None), good, good, good, 1.0, good, good, d, good, ws,
+                                       _fake(None), _fake(None)) == 1
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(sv, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(sv, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        sv.library()

@@ -1,0 +1,326 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Every case draws seeded synthetic inputs once, runs the library and the
+oracle on the same bytes, and compares under the tolerances of _helpers.
+Small cases span several tiles and a ragged tail; the full-size cases run the
+workloads in the launch configuration the benchmark times and compare
+sampled sequences.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_67_gb300 as sv
+from speculative_decoding_verification_67_gb300 import synth
+
+from _helpers import (LOGIT_ATOL, compare_debug, compare_greedy, compare_sampling, logits_error, np64, np_int)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from speculative_decoding_verification_67_gb300 import _build
+    _build.build()
+    sv.library()
+
+
+def _run_head_case(w, seed=None, keep_debug=True):
+    inp = synth.make_inputs(w, device="cuda", seed=seed)
+    B, K, d, V, T = w.B, w.K, w.d, w.V, w.temperature
+    logits = torch.empty((B * (K + 1), V), dtype=torch.float32, device="cuda") if T > 0 else None
+    dbg = torch.zeros((B, K + 1, sv.SPEC_DEBUG_FIELDS), dtype=torch.float32, device="cuda")
+    tok, n = sv.spec_verify(inp["hidden"], inp["W"], inp["draft_logits"], inp["draft_tokens"], inp["uniforms"], T,
+                            out_target_logits=logits, out_debug=dbg if keep_debug else None)
+    torch.cuda.synchronize()
+    return inp, tok, n, logits, dbg
+
+
+# ---------------------------------------------------------------- LM head
+@pytest.mark.parametrize("M,d,V", [(1, 64, 128), (6, 4096, 1000), (7, 200, 1000), (40, 512, 3001),
+                                   (100, 1024, 2500), (300, 256, 777), (576, 512, 1500), (1280, 128, 700)])
+def test_lm_head_matches_oracle(M, d, V):
+    g = torch.Generator(device="cuda").manual_seed(1000 + M + d + V)
+    h = torch.randn((M, d), generator=g, device="cuda").to(torch.bfloat16)
+    W = (torch.randn((V, d), generator=g, device="cuda") / math.sqrt(d)).to(torch.bfloat16)
+    z = sv.spec_lm_head(h, W)
+    torch.cuda.synchronize()
+    ref = oracle.lm_head(np64(h), np64(W))
+    err = logits_error(np64(z), ref)
+    print(f"\nlm_head M={M} d={d} V={V}: {err}")
+    assert err["max_abs"] <= LOGIT_ATOL, err
+
+
+def test_lm_head_identity_slice_is_exact():
+    M, d, V = 40, 256, 200
+    h = torch.randn((M, d), device="cuda").to(torch.bfloat16)
+    W = torch.eye(d, device="cuda")[:V].to(torch.bfloat16).contiguous()
+    z = sv.spec_lm_head(h, W)
+    torch.cuda.synchronize()
+    assert torch.equal(z, h[:, :V].float())
+    e = torch.zeros((d, d), device="cuda")
+    e.fill_diagonal_(1.0)
+    W2 = torch.randn((V, d), device="cuda").to(torch.bfloat16)
+    z2 = sv.spec_lm_head(e.to(torch.bfloat16), W2)
+    torch.cuda.synchronize()
+    assert torch.equal(z2, W2.float().t())
+
+
+def test_lm_head_is_deterministic():
+    w = synth.custom("det", B=8, K=4, d=1024, V=5000, temperature=0.8)
+    inp = synth.make_inputs(w, device="cuda")
+    a = sv.spec_lm_head(inp["hidden"], inp["W"])
+    b = sv.spec_lm_head(inp["hidden"], inp["W"])
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------- sampling from logits
+def _from_logits_case(B, K, V, T, seed, std=2.0, noise=0.5):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    zp = torch.randn((B * (K + 1), V), generator=g, device="cuda") * std
+    zq = (zp.view(B, K + 1, V)[:, :K] + noise * torch.randn((B, K, V), generator=g, device="cuda")).reshape(B * K, V)
+    x = synth.gumbel_max_tokens(zq, T, g).view(B, K).contiguous() if K > 0 else \
+        torch.zeros((B, 0), dtype=torch.int32, device="cuda")
+    u = torch.rand((B, K + 1), generator=g, device="cuda")
+    return zp.contiguous(), zq.contiguous(), x, u
+
+
+@pytest.mark.parametrize("B,K,V,T", [(1, 4, 1000, 1.0), (64, 4, 1000, 1.0), (33, 7, 8193, 0.8),
+                                     (16, 0, 5000, 1.0), (8, 32, 3000, 1.3), (200, 3, 1001, 0.7)])
+def test_verify_from_logits_matches_oracle(B, K, V, T):
+    zp, zq, x, u = _from_logits_case(B, K, V, T, seed=B * 131 + K * 7 + V)
+    dbg = torch.zeros((B, K + 1, sv.SPEC_DEBUG_FIELDS), device="cuda")
+    tok, n = sv.spec_verify_from_logits(zp, zq, x, u, T, out_debug=dbg)
+    torch.cuda.synchronize()
+    ref = oracle.verify_sampling(np64(zp).reshape(B, K + 1, V), np64(zq).reshape(B, K, V), np_int(x), np64(u), T)
+    st = compare_sampling(np_int(tok), np_int(n), ref, K)
+    print(f"\nfrom_logits B={B} K={K} V={V} T={T}: {st}")
+    compare_debug(np64(dbg), ref, np_int(n), K)
+
+
+def test_tiny_logits_workload():
+    w = synth.WORKLOADS["tiny_logits"]
+    inp = synth.make_inputs(w, device="cuda")
+    B, K, V, T = w.B, w.K, w.V, w.temperature
+    dbg = torch.zeros((B, K + 1, sv.SPEC_DEBUG_FIELDS), device="cuda")
+    tok, n = sv.spec_verify_from_logits(inp["target_logits"], inp["draft_logits"], inp["draft_tokens"],
+                                        inp["uniforms"], T, out_debug=dbg)
+    torch.cuda.synchronize()
+    ref = oracle.verify_sampling(np64(inp["target_logits"]).reshape(B, K + 1, V),
+                                 np64(inp["draft_logits"]).reshape(B, K, V), np_int(inp["draft_tokens"]),
+                                 np64(inp["uniforms"]), T)
+    compare_sampling(np_int(tok), np_int(n), ref, K)
+    compare_debug(np64(dbg), ref, np_int(n), K)
+
+
+def test_many_draws_over_fixed_logits():
+    """Thousands of decisions on one set of logits: every accept count and
+    token must agree outside the bands, and band cases stay under 0.1%."""
+    B, K, V, T = 256, 4, 32000, 0.8
+    zp, zq, x, _ = _from_logits_case(B, K, V, T, seed=77, std=1.0, noise=0.3)
+    zp64, zq64, x64 = np64(zp).reshape(B, K + 1, V), np64(zq).reshape(B, K, V), np_int(x)
+    totals = dict(draws=0, accept_exempt=0, draw_exempt=0, draw_mismatch_exempt=0, accept_mismatch_exempt=0)
+    us = synth.fresh_uniforms(B, K, 8, device="cuda", seed=5)
+    for i in range(us.shape[0]):
+        u = us[i].contiguous()
+        tok, n = sv.spec_verify_from_logits(zp, zq, x, u, T)
+        torch.cuda.synchronize()
+        ref = oracle.verify_sampling(zp64, zq64, x64, np64(u), T)
+        st = compare_sampling(np_int(tok), np_int(n), ref, K)
+        for k in totals:
+            totals[k] += st[k]
+    print(f"\nmany draws: {totals}")
+    assert totals["accept_exempt"] + totals["draw_exempt"] <= max(1, 0.001 * totals["draws"])
+
+
+def test_chi_square_exactness_on_gpu():
+    """The GPU path's output at every slot follows p (chi-square, alpha 0.001,
+    10^6 rounds at V=16, K=4), the same test the oracle is pinned by."""
+    from scipy import stats
+    V, K = 16, 4
+    rng = np.random.default_rng(21)
+    p = np.exp(rng.normal(size=(K + 1, V)))
+    p /= p.sum(axis=1, keepdims=True)
+    q = np.exp(rng.normal(size=(K, V)))
+    q /= q.sum(axis=1, keepdims=True)
+    B = 100_000
+    zp = torch.tensor(np.log(p), dtype=torch.float32, device="cuda").repeat(B, 1).contiguous()
+    zq = torch.tensor(np.log(q), dtype=torch.float32, device="cuda").repeat(B, 1).contiguous()
+    g = torch.Generator(device="cuda").manual_seed(3)
+    counts = [np.zeros(V) for _ in range(K + 1)]
+    for it in range(10):
+        x = synth.gumbel_max_tokens(zq, 1.0, g).view(B, K).contiguous()
+        u = torch.rand((B, K + 1), generator=g, device="cuda")
+        tok, n = sv.spec_verify_from_logits(zp, zq, x, u, 1.0)
+        tok, n = np_int(tok), np_int(n)
+        for j in range(K + 1):
+            sel = n >= j
+            counts[j] += np.bincount(tok[sel, j], minlength=V)
+    for j in range(K + 1):
+        exp = counts[j].sum() * p[j]
+        s = ((counts[j] - exp) ** 2 / exp).sum()
+        assert s <= stats.chi2.ppf(0.999, V - 1), (j, s)
+
+
+def test_determinism_bits():
+    B, K, V, T = 16, 4, 20000, 0.9
+    zp, zq, x, u = _from_logits_case(B, K, V, T, seed=9)
+    d1 = torch.zeros((B, K + 1, 6), device="cuda")
+    d2 = torch.zeros((B, K + 1, 6), device="cuda")
+    t1, n1 = sv.spec_verify_from_logits(zp, zq, x, u, T, out_debug=d1)
+    t1, n1 = t1.clone(), n1.clone()
+    t2, n2 = sv.spec_verify_from_logits(zp, zq, x, u, T, out_debug=d2)
+    torch.cuda.synchronize()
+    assert torch.equal(t1, t2) and torch.equal(n1, n2) and torch.equal(d1, d2)
+
+
+# ---------------------------------------------------------------- whole step, small
+@pytest.mark.parametrize("B,K,d,V,T", [(3, 3, 256, 5000, 0.8), (1, 5, 512, 32000, 1.0), (5, 0, 128, 1000, 1.0),
+                                       (12, 8, 384, 4099, 1.0)])
+def test_spec_verify_small(B, K, d, V, T):
+    w = synth.custom("small", B=B, K=K, d=d, V=V, temperature=T, seed=B + K + d + V)
+    inp, tok, n, logits, dbg = _run_head_case(w)
+    ref = oracle.spec_verify(np64(inp["hidden"]), np64(inp["W"]), np64(inp["draft_logits"]),
+                             np_int(inp["draft_tokens"]), np64(inp["uniforms"]), T, B, K)
+    err = logits_error(np64(logits), ref["target_logits"])
+    assert err["max_abs"] <= LOGIT_ATOL, err
+    st = compare_sampling(np_int(tok), np_int(n), ref, K)
+    compare_debug(np64(dbg), ref, np_int(n), K)
+    print(f"\nspec_verify small {B},{K},{d},{V},{T}: logits {err} {st}")
+
+
+@pytest.mark.parametrize("B,K,d,V", [(4, 4, 256, 3000), (40, 3, 512, 1001), (100, 4, 128, 20000)])
+def test_greedy_small(B, K, d, V):
+    w = synth.custom("greedy", B=B, K=K, d=d, V=V, temperature=0.0, noise=0.2, seed=B * K + V)
+    inp, tok, n, _, dbg = _run_head_case(w)
+    ref = oracle.spec_verify(np64(inp["hidden"]), np64(inp["W"]), None, np_int(inp["draft_tokens"]), None, 0.0, B, K)
+    st = compare_greedy(np_int(tok), np_int(n), ref)
+    assert st["ill_conditioned"] == 0, st
+    # greedy from logits on the oracle-independent GPU logits path gives the same
+    z = sv.spec_lm_head(inp["hidden"], inp["W"])
+    tok2, n2 = sv.spec_verify_from_logits(z, None, inp["draft_tokens"], None, 0.0)
+    torch.cuda.synchronize()
+    assert torch.equal(tok, tok2) and torch.equal(n, n2)
+    # debug: argmax ids and max logits
+    dbg = np64(dbg)
+    np.testing.assert_array_equal(dbg[:, :, 1].astype(np.int64), ref["argmax"])
+
+
+# ---------------------------------------------------------------- edge cases
+def test_invalid_draft_token_marks_the_sequence():
+    B, K, V, T = 4, 3, 1000, 1.0
+    zp, zq, x, u = _from_logits_case(B, K, V, T, seed=11)
+    x[2, 1] = V + 5
+    ws = torch.empty(sv.workspace_bytes(B, K, V, T, False), dtype=torch.uint8, device="cuda")
+    tok, n = sv.spec_verify_from_logits(zp, zq, x, u, T, workspace=ws)
+    word = sv.read_error(ws)
+    assert word & sv.DEVERR_TOKEN_RANGE
+    n = np_int(n)
+    tok = np_int(tok)
+    assert n[2] == -1 and (tok[2] == -1).all()
+    ref = oracle.verify_sampling(np64(zp).reshape(B, K + 1, V), np64(zq).reshape(B, K, V),
+                                 np.clip(np_int(x), 0, V - 1), np64(u), T)
+    keep = [0, 1, 3]
+    sub = {k: v[keep] for k, v in ref.items()}
+    compare_sampling(tok[keep], n[keep], sub, K)
+
+
+def test_nonfinite_logit_marks_the_sequence():
+    B, K, V, T = 3, 2, 5000, 1.0
+    zp, zq, x, u = _from_logits_case(B, K, V, T, seed=12)
+    zp[1 * (K + 1) + 2, 17] = float("nan")
+    ws = torch.empty(sv.workspace_bytes(B, K, V, T, False), dtype=torch.uint8, device="cuda")
+    tok, n = sv.spec_verify_from_logits(zp, zq, x, u, T, workspace=ws)
+    assert sv.read_error(ws) & sv.DEVERR_NONFINITE
+    assert np_int(n)[1] == -1 and np_int(n)[0] >= 0 and np_int(n)[2] >= 0
+    zp2 = zp.clone()
+    zp2[1 * (K + 1) + 2, 17] = float("inf")
+    t3, n3 = sv.spec_verify_from_logits(zp2, zq, x, u, 0.0, workspace=torch.empty(
+        sv.workspace_bytes(B, K, V, 0.0), dtype=torch.uint8, device="cuda"))
+    assert np_int(n3)[1] == -1
+
+
+def test_all_accept_and_first_reject_extremes():
+    """u = 0 accepts every draft with p(x) > 0 (then the bonus row is drawn);
+    u just below 1 rejects every draft whose a < 1."""
+    B, K, V, T = 32, 4, 3000, 1.0
+    zp, zq, x, u = _from_logits_case(B, K, V, T, seed=13)
+    for fill in (0.0, 0.99999994):
+        u2 = torch.full_like(u, fill)
+        u2[:, K] = u[:, K]
+        tok, n = sv.spec_verify_from_logits(zp, zq, x, u2, T)
+        torch.cuda.synchronize()
+        ref = oracle.verify_sampling(np64(zp).reshape(B, K + 1, V), np64(zq).reshape(B, K, V), np_int(x),
+                                     np64(u2), T)
+        compare_sampling(np_int(tok), np_int(n), ref, K)
+        if fill == 0.0:
+            assert (np_int(n) == K).all()
+
+
+def test_host_buffer_entry_point_matches_device_entry_point():
+    w = synth.custom("host", B=4, K=4, d=512, V=9000, temperature=0.8, seed=4)
+    inp = synth.make_inputs(w, device="cuda")
+    tok, n = sv.spec_verify(inp["hidden"], inp["W"], inp["draft_logits"], inp["draft_tokens"], inp["uniforms"], 0.8)
+    host = {k: v.cpu().pin_memory() for k, v in inp.items() if isinstance(v, torch.Tensor) and k != "W"}
+    tok_h, n_h = sv.spec_verify_host(host["hidden"], inp["W"], host["draft_logits"], host["draft_tokens"],
+                                     host["uniforms"], 0.8)
+    assert torch.equal(tok.cpu(), tok_h) and torch.equal(n.cpu(), n_h)
+
+
+# ---------------------------------------------------------------- full-size workloads
+def _sample_rows(B, K, seqs):
+    return np.concatenate([np.arange(b * (K + 1), (b + 1) * (K + 1)) for b in seqs])
+
+
+@pytest.mark.parametrize("name", ["head_B1_K5_V32000", "head_B8_K4_V128256"])
+def test_full_size_sampling_workload(name):
+    w = synth.WORKLOADS[name]
+    inp, tok, n, logits, dbg = _run_head_case(w)
+    ref = oracle.spec_verify(np64(inp["hidden"]), np64(inp["W"]), np64(inp["draft_logits"]),
+                             np_int(inp["draft_tokens"]), np64(inp["uniforms"]), w.temperature, w.B, w.K)
+    err = logits_error(np64(logits), ref["target_logits"])
+    st = compare_sampling(np_int(tok), np_int(n), ref, w.K)
+    print(f"\n{name}: logits {err}; decisions {st}; accepted {np_int(n).tolist()}")
+    assert err["max_abs"] <= LOGIT_ATOL, err
+    compare_debug(np64(dbg), ref, np_int(n), w.K)
+
+
+def test_full_size_70b_head_sampled_sequences():
+    w = synth.WORKLOADS["head_B64_K8_V152064"]
+    inp, tok, n, logits, dbg = _run_head_case(w)
+    seqs = [0, 9, 31, 63]
+    rows = _sample_rows(w.B, w.K, seqs)
+    h = np64(inp["hidden"])[rows]
+    ref_rows = oracle.lm_head(h, inp["W"].float().cpu().numpy())
+    err = logits_error(np64(logits)[rows], ref_rows)
+    assert err["max_abs"] <= LOGIT_ATOL, err
+    V, K = w.V, w.K
+    zq_rows = np.concatenate([np.arange(b * K, (b + 1) * K) for b in seqs])
+    ref = oracle.verify_sampling(ref_rows.reshape(len(seqs), K + 1, V),
+                                 np64(inp["draft_logits"])[zq_rows].reshape(len(seqs), K, V),
+                                 np_int(inp["draft_tokens"])[seqs], np64(inp["uniforms"])[seqs], w.temperature)
+    st = compare_sampling(np_int(tok)[seqs], np_int(n)[seqs], ref, K)
+    print(f"\n70B head: logits {err}; decisions {st}; accepted {np_int(n).tolist()}")
+    # properties that hold for every sequence
+    tok_all, n_all, x_all = np_int(tok), np_int(n), np_int(inp["draft_tokens"])
+    assert ((n_all >= 0) & (n_all <= K)).all()
+    for b in range(w.B):
+        assert (tok_all[b, :n_all[b]] == x_all[b, :n_all[b]]).all()
+        assert 0 <= tok_all[b, n_all[b]] < V and (tok_all[b, n_all[b] + 1:] == -1).all()
+
+
+def test_full_size_greedy_sampled_sequences():
+    w = synth.WORKLOADS["greedy_B256_K4_V128256"]
+    inp, tok, n, _, dbg = _run_head_case(w)
+    seqs = list(range(0, 256, 16))
+    rows = _sample_rows(w.B, w.K, seqs)
+    z = oracle.lm_head(np64(inp["hidden"])[rows], inp["W"].float().cpu().numpy())
+    ref = oracle.verify_greedy(z.reshape(len(seqs), w.K + 1, w.V), np_int(inp["draft_tokens"])[seqs])
+    st = compare_greedy(np_int(tok)[seqs], np_int(n)[seqs], ref)
+    print(f"\ngreedy full size: {st}; accepted mean {np_int(n).mean():.3f}")
+    assert st["ill_conditioned"] == 0, st
+    np.testing.assert_array_equal(np64(dbg)[seqs][:, :, 1].astype(np.int64), ref["argmax"])
