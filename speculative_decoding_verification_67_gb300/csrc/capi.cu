@@ -14,7 +14,7 @@ using sv::DeviceInfo;
 
 constexpr size_t kAlign = 256;
 constexpr int kAbiVersion = 1;
-constexpr int kMaxRows = 65535;  // grid.y of the per-row passes
+constexpr long long kMaxRows = 1ll << 24;  // rows of the per-row passes (grid.x)
 
 size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -26,14 +26,14 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 struct Layout {
   size_t ctrl_bytes = 0;
   size_t seq = 0, parts = 0, res = 0, logits = 0;  // sampling
-  size_t pmax = 0, pidx = 0, gscratch = 0;         // greedy
+  size_t pmax = 0, pidx = 0;                       // greedy
   int CA = 0, CB = 0, P = 0;
   size_t total = 0;
 };
 
-// int[0] error word, int[1] greedy ticket, int[2 .. 2+B) tickets of pass 1,
-// int[2+B .. 2+2B) tickets of pass 2.
-constexpr int kCtrlErr = 0, kCtrlGreedyTicket = 1, kCtrlTickets = 2;
+// int[0] error word, int[1 .. 1+B) tickets of pass 1, int[1+B .. 1+2B)
+// tickets of pass 2.
+constexpr int kCtrlErr = 0, kCtrlTickets = 1;
 
 Layout make_layout(int B, int K, int V, bool greedy, bool logits_in_ws, bool from_logits) {
   Layout L;
@@ -41,27 +41,25 @@ Layout make_layout(int B, int K, int V, bool greedy, bool logits_in_ws, bool fro
   size_t off = round_up(sizeof(int) * (kCtrlTickets + 2 * static_cast<size_t>(B)));
   L.ctrl_bytes = off;
   if (!greedy) {
-    L.CA = (V + sv::kRowChunk - 1) / sv::kRowChunk;
-    L.CB = (V + sv::kResChunk - 1) / sv::kResChunk;
+    L.CA = (V + sv::kChunk - 1) / sv::kChunk;
+    L.CB = L.CA;
     const size_t R = M + static_cast<size_t>(B) * K;
     L.seq = off;
     off += round_up(sizeof(sv::SeqState) * B);
     L.parts = off;
-    off += round_up(sizeof(sv::RowPart) * R * L.CA);
+    off += round_up(sizeof(sv::ChunkStat) * R * L.CA);
     L.res = off;
-    off += round_up(sizeof(double) * static_cast<size_t>(B) * L.CB);
+    off += round_up(sizeof(float2) * static_cast<size_t>(B) * L.CB);
     if (logits_in_ws) {
       L.logits = off;
       off += round_up(sizeof(float) * M * static_cast<size_t>(V));
     }
   } else {
-    L.P = from_logits ? (V + sv::kRowChunk - 1) / sv::kRowChunk : (V + sv::kHeadTileV - 1) / sv::kHeadTileV;
+    L.P = from_logits ? (V + sv::kChunk - 1) / sv::kChunk : (V + sv::kHeadTileV - 1) / sv::kHeadTileV;
     L.pmax = off;
     off += round_up(sizeof(float) * static_cast<size_t>(L.P) * M);
     L.pidx = off;
     off += round_up(sizeof(int) * static_cast<size_t>(L.P) * M);
-    L.gscratch = off;
-    off += round_up(sv::greedy_scratch_bytes(static_cast<int>(M)));
   }
   L.total = off;
   return L;
@@ -126,7 +124,7 @@ sv::VerifyArgs sampling_args(const Layout& L, const spec_dims& d, float T, const
   a.B = d.B;
   a.K = d.K;
   a.V = d.V;
-  a.T = T;
+  sv::exponent_constant(T, &a.c_hi, &a.c_lo);
   a.zp = zp;
   a.zq = zq;
   a.x = x;
@@ -138,9 +136,9 @@ sv::VerifyArgs sampling_args(const Layout& L, const spec_dims& d, float T, const
   a.err = ctrl + kCtrlErr;
   a.tickets_a = reinterpret_cast<unsigned*>(ctrl + kCtrlTickets);
   a.tickets_b = reinterpret_cast<unsigned*>(ctrl + kCtrlTickets + d.B);
-  a.parts = reinterpret_cast<sv::RowPart*>(ws + L.parts);
+  a.stats = reinterpret_cast<sv::ChunkStat*>(ws + L.parts);
   a.seq = reinterpret_cast<sv::SeqState*>(ws + L.seq);
-  a.res_sums = reinterpret_cast<double*>(ws + L.res);
+  a.res_sums = reinterpret_cast<float2*>(ws + L.res);
   a.CA = L.CA;
   a.CB = L.CB;
   return a;
@@ -223,7 +221,7 @@ spec_status spec_verify(const void* hidden, const void* W_lm, const float* draft
     if (enc_fail) return SPEC_ERR_CUDA;
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
     const sv::GreedyArgs g = greedy_args(L, dims, draft_tokens, out_tokens, out_num_accepted, out_debug, ws);
-    e = sv::launch_greedy_finish_ws(g, ws + L.gscratch, reinterpret_cast<unsigned*>(ws) + kCtrlGreedyTicket, s);
+    e = sv::launch_greedy_finish(g, s);
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
   }
   float* logits = out_target_logits ? out_target_logits : reinterpret_cast<float*>(ws + L.logits);
@@ -264,7 +262,7 @@ spec_status spec_verify_from_logits(const float* target_logits, const float* dra
                               reinterpret_cast<int*>(ws + L.pidx), s);
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
     const sv::GreedyArgs g = greedy_args(L, dims, draft_tokens, out_tokens, out_num_accepted, out_debug, ws);
-    e = sv::launch_greedy_finish_ws(g, ws + L.gscratch, reinterpret_cast<unsigned*>(ws) + kCtrlGreedyTicket, s);
+    e = sv::launch_greedy_finish(g, s);
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
   }
   const sv::VerifyArgs a = sampling_args(L, dims, temperature, target_logits, draft_logits, draft_tokens,

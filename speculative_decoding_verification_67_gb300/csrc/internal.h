@@ -27,13 +27,14 @@ constexpr int kErrTimeout = 0x4;
 // Output modes of the LM-head epilogue.
 enum class HeadOut : int {
   kLogits = 0,   // f32 logits [M][V]
-  kArgmax = 1,   // per (vocab tile, row) max and lowest argmax: [num_vt][M]
+  kArgmax = 1,   // per (row, vocab tile) max and lowest argmax: [M][num_vt]
 };
 
 constexpr int kHeadTileV = 128;   // vocabulary rows per tile (MMA M)
 constexpr int kHeadTileK = 64;    // hidden elements per pipeline stage (128-byte rows)
 
 struct HeadPlan {
+  bool precise = false; // per-hidden-block TMEM slots summed in registers (N = 32 or 64)
   int N = 0;            // positions per tile (MMA N), multiple of 16, <= 256
   int num_chunks = 0;   // position chunks, ceil(M / N)
   int num_vt = 0;       // vocabulary tiles, ceil(V / 128)
@@ -54,31 +55,31 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
                         const DeviceInfo& dev, cudaStream_t stream, bool* encode_failed);
 
 // ------------------------------------------------------------------ verify
-constexpr int kRowChunk = 8192;   // vocab elements per CTA of the row-statistics pass
-constexpr int kResChunk = 4096;   // vocab elements per CTA of the residual pass
+constexpr int kChunk = 4096;      // vocabulary tokens per CTA of the per-row passes
 constexpr int kMaxK = 32;
 
-// Per (row, chunk) partial of the softmax normaliser of z/T.
-struct RowPart {
-  float m;      // max of z/T over the chunk
+// Per (row, chunk) softmax normaliser of z/T: sum over the chunk of
+// 2^(z*log2(e)/T - k), k the chunk's integer reference, as a float pair.
+struct ChunkStat {
+  float k;      // integer-valued reference exponent (base 2)
   int bad;      // a non-finite logit was seen
-  double s;     // sum exp(z/T - m) over the chunk
+  float s_hi, s_lo;
 };
 
 // Per-sequence state handed from the decision to the residual pass.
 struct SeqState {
   int n;          // accepted drafts
   int bad;        // invalid input: skip
-  float m_p;      // max of z_p/T on row n
-  float m_q;      // max of z_q/T on row n (n < K)
-  double S_p;     // sum exp(z_p/T - m_p) on row n
-  double S_q;     // same for the draft row (n < K)
-  double kappa;   // S_p / S_q
+  float k_p;      // reference exponent of target row n
+  float k_q;      // reference exponent of draft row n (n < K)
+  float2 S_p;     // normaliser of target row n against k_p (float pair)
+  float2 S_q;     // same for the draft row (n < K)
+  float2 kappa;   // S_p / S_q (float pair)
 };
 
 struct VerifyArgs {
   int B, K, V;
-  float T;
+  float c_hi, c_lo;         // log2(e) / T as a float pair
   const float* zp;          // [B*(K+1)][V]
   const float* zq;          // [B*K][V]
   const int32_t* x;         // [B][K]
@@ -90,19 +91,22 @@ struct VerifyArgs {
   int* err;
   unsigned* tickets_a;      // [B]
   unsigned* tickets_b;      // [B]
-  RowPart* parts;           // [R][CA], R = B*(K+1) + B*K
+  ChunkStat* stats;         // [R][CA], R = B*(K+1) + B*K
   SeqState* seq;            // [B]
-  double* res_sums;         // [B][CB]
+  float2* res_sums;         // [B][CB]
   int CA, CB;
 };
+
+// log2(e) / T split into a float pair.
+void exponent_constant(float temperature, float* c_hi, float* c_lo);
 
 cudaError_t launch_verify_sampling(const VerifyArgs& a, cudaStream_t stream);
 
 struct GreedyArgs {
   int B, K, V;
   int P;                    // partitions of the vocabulary (partials per row)
-  const float* part_max;    // [P][M]
-  const int* part_idx;      // [P][M]  (-2 marks a non-finite logit)
+  const float* part_max;    // [M][P]
+  const int* part_idx;      // [M][P]  (-2 marks a non-finite logit)
   const int32_t* x;         // [B][K]
   int32_t* out_tokens;
   int32_t* out_n;
@@ -110,12 +114,9 @@ struct GreedyArgs {
   int* err;
 };
 
-// Scratch the greedy finish needs after the partition partials (bytes, for M rows),
-// and its launch; `ticket` must be zero before the launch.
-size_t greedy_scratch_bytes(int M);
-cudaError_t launch_greedy_finish_ws(const GreedyArgs& a, void* scratch, unsigned* ticket, cudaStream_t stream);
+cudaError_t launch_greedy_finish(const GreedyArgs& a, cudaStream_t stream);
 
-// Row argmax partials from given logits ([M][V] -> [P][M], P = ceil(V / kRowChunk)).
+// Row argmax partials from given logits ([M][V] -> [M][P], P = ceil(V / kChunk)).
 cudaError_t launch_row_argmax(const float* logits, int M, int V, float* part_max, int* part_idx,
                               cudaStream_t stream);
 

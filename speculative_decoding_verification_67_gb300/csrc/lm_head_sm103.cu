@@ -10,10 +10,8 @@
 // is organised around reading W exactly once at HBM speed:
 //
 //  * swap-AB: a tile is 128 vocabulary rows (the MMA's M = 128 operand, A)
-//    times N positions (the MMA's N operand, B, N = M rounded up to 16, at
-//    most 256 per position chunk); the f32 accumulator lives in TMEM,
-//    128 lanes x N columns, double-buffered so the epilogue of one tile
-//    overlaps the main loop of the next;
+//    times N positions (the MMA's N operand, B, N = M rounded up, at most
+//    256 per position chunk); the f32 accumulator lives in TMEM;
 //  * persistent CTAs, one per SM; each walks tiles tile = blockIdx.x +
 //    i*gridDim.x; position chunks of one vocabulary tile are adjacent in
 //    that order so that, when M needs several chunks, the CTAs reading the
@@ -23,6 +21,14 @@
 //    issues tcgen05.mma from one thread, warps 2-5 drain TMEM (tcgen05.ld)
 //    and write either the f32 logits or per-tile (max, lowest argmax)
 //    partials for the greedy path;
+//  * two accumulation schemes.  Standard (any N): one TMEM accumulator per
+//    tile over the whole hidden size, double-buffered so the epilogue of a
+//    tile overlaps the next tile's MMAs.  Precise (N <= 64, the small-batch
+//    regime): every 64-wide hidden block is accumulated into a fresh TMEM
+//    slot (4 slots rotate) and the epilogue adds the block results in f32
+//    registers with round-to-nearest, so the tensor core's own accumulation
+//    only ever spans 64 products; this cuts the logits' error against exact
+//    arithmetic several-fold at no cost to the weight stream;
 //  * every wait is bounded; a timeout sets the error word, drains the copies
 //    in flight and frees TMEM before returning.
 #include <cudaTypedefs.h>
@@ -39,11 +45,12 @@ namespace {
 constexpr int kThreads = 192;
 constexpr uint32_t kABytes = kHeadTileV * kHeadTileK * 2;  // 16 KB W tile per stage
 constexpr uint32_t kBarrierBytes = 512;
-constexpr uint32_t kReduceBytes = 3 * 4 * 256 * 4;         // argmax scratch
+constexpr uint32_t kReduceBytes = 2 * 4 * 256 * 4;         // argmax scratch
+constexpr int kSlotsPrecise = 4;
 
 struct HeadParams {
   int M, d, V;
-  int N, num_chunks, num_tiles, num_kb, stages;
+  int N, num_chunks, num_vt, num_tiles, num_kb, stages;
   uint32_t tmem_cols;
   int mode;
   float* logits;
@@ -59,21 +66,92 @@ __device__ __forceinline__ void report_timeout(int* err) {
   atomicOr(err ? err : &g_head_timeout_word, kErrTimeout);
 }
 
+// Output of 16 columns [c0, c0+16) of this thread's vocabulary row v.
+template <bool kArgmax>
+__device__ __forceinline__ void emit16(const HeadParams& p, const float (&val)[16], int c0, int m0, int v, int q,
+                                       int lane, float* red_val, int* red_idx) {
+  if (!kArgmax) {
+    if (v < p.V) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int m = m0 + c0 + i;
+        if (m < p.M) p.logits[static_cast<size_t>(m) * p.V + v] = val[i];
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float bv = val[i];
+      int bi = v;
+      const bool bad = (v < p.V) && !isfinite(bv);
+      if (v >= p.V || bad) {
+        bv = -INFINITY;
+        bi = 0x7fffffff;
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (ov > bv || (ov == bv && oi < bi)) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      const bool any_bad = __any_sync(0xffffffffu, bad);
+      if (lane == 0) {
+        red_val[q * 256 + c0 + i] = bv;
+        red_idx[q * 256 + c0 + i] = any_bad ? -2 : bi;
+      }
+    }
+  }
+}
+
+// Greedy partials of one tile: combine the four lane quadrants per column.
+__device__ __forceinline__ void argmax_finish(const HeadParams& p, int N, int vt, int m0, int et,
+                                              const float* red_val, const int* red_idx) {
+  for (int c = et; c < N; c += 128) {
+    const int m = m0 + c;
+    if (m >= p.M) continue;
+    float bv = red_val[c];
+    int bi = red_idx[c];
+    bool bad = bi == -2;
+#pragma unroll
+    for (int qq = 1; qq < 4; ++qq) {
+      const float ov = red_val[qq * 256 + c];
+      const int oi = red_idx[qq * 256 + c];
+      bad |= oi == -2;
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    p.part_max[static_cast<size_t>(m) * p.num_vt + vt] = bv;
+    p.part_idx[static_cast<size_t>(m) * p.num_vt + vt] = bad ? -2 : bi;
+  }
+}
+
+// kPrecN == 0: standard accumulation; kPrecN == 32 or 64: precise
+// accumulation with N == kPrecN.  kArgmax selects the greedy partials
+// epilogue instead of the logits one.
+template <int kPrecN, bool kArgmax>
 __global__ void __launch_bounds__(kThreads, 1)
     head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_h,
                 const HeadParams p) {
+  constexpr bool kPrecise = kPrecN > 0;
+  constexpr int kSlots = kPrecise ? kSlotsPrecise : 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
-  const uint32_t b_bytes = static_cast<uint32_t>(p.N) * 128u;
+  const int N = kPrecise ? kPrecN : p.N;
+  const uint32_t b_bytes = static_cast<uint32_t>(N) * 128u;
   const uint32_t stage_bytes = kABytes + b_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
-  uint64_t* full = bars;            // [S] TMA landed
-  uint64_t* empty = bars + S;       // [S] MMAs reading the stage are done
-  uint64_t* tfull = bars + 2 * S;   // [2] accumulator ready
-  uint64_t* tempty = tfull + 2;     // [2] accumulator drained
-  uint64_t* mma_done = tempty + 2;  // [1] teardown
+  uint64_t* full = bars;              // [S] TMA landed
+  uint64_t* empty = bars + S;         // [S] MMAs reading the stage are done
+  uint64_t* afull = bars + 2 * S;     // [4] accumulator (slot) ready
+  uint64_t* afree = afull + 4;        // [4] accumulator (slot) drained
+  uint64_t* mma_done = afree + 4;     // [1] teardown
   uint64_t* red_full = mma_done + 1;  // [1] argmax scratch written by the 4 epilogue warps
   uint64_t* red_free = red_full + 1;  // [1] argmax scratch consumed
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(red_free + 1);
@@ -88,9 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&afull[i], 1);
+      mbar_init(&afree[i], 4);
     }
     mbar_init(mma_done, 1);
     mbar_init(red_full, 4);
@@ -131,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* a_dst = smem + static_cast<size_t>(s) * stage_bytes;
           mbar_arrive_expect_tx(&full[s], stage_bytes);
           tma_load_2d(a_dst, &tmap_w, &full[s], kb * kHeadTileK, vt * kHeadTileV, pol_w);
-          tma_load_2d(a_dst + kABytes, &tmap_h, &full[s], kb * kHeadTileK, pc * p.N, pol_h);
+          tma_load_2d(a_dst + kABytes, &tmap_h, &full[s], kb * kHeadTileK, pc * N, pol_h);
           ++issued;
           if (++s == S) {
             s = 0;
@@ -157,44 +235,63 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kHeadTileV, static_cast<uint32_t>(p.N));
+      const uint32_t idesc = idesc_bf16_f32(kHeadTileV, static_cast<uint32_t>(N));
       int s = 0;
       uint32_t ph = 0;
-      int ab = 0;
-      uint32_t aph = 0;
+      int slot = 0;
+      uint32_t sph = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        if (!mbar_wait(&tempty[ab], aph ^ 1u)) {
-          report_timeout(p.err);
-          break;
+        if (!kPrecise) {
+          if (!mbar_wait(&afree[slot], sph ^ 1u)) {
+            report_timeout(p.err);
+            break;
+          }
+          tc_fence_after_sync();
         }
-        tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * p.N);
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(&full[s], ph)) {
             report_timeout(p.err);
             ok = false;
             break;
           }
+          if (kPrecise) {
+            if (!mbar_wait(&afree[slot], sph ^ 1u)) {
+              report_timeout(p.err);
+              ok = false;
+              break;
+            }
+          }
           tc_fence_after_sync();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(slot * N);
           const uint32_t a_addr = smem_u32(smem + static_cast<size_t>(s) * stage_bytes);
           const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
           for (int k = 0; k < kHeadTileK / 16; ++k) {
-            mma_bf16_ss(d_tmem, smem_desc_k_sw128(a_addr + k * 32), smem_desc_k_sw128(b_addr + k * 32),
-                        idesc, (kb | k) != 0 ? 1u : 0u);
+            const bool acc = kPrecise ? (k != 0) : ((kb | k) != 0);
+            mma_bf16_ss(d_tmem, smem_desc_k_sw128(a_addr + k * 32), smem_desc_k_sw128(b_addr + k * 32), idesc,
+                        acc ? 1u : 0u);
           }
           mma_commit(&empty[s]);
           if (++s == S) {
             s = 0;
             ph ^= 1u;
           }
+          if (kPrecise) {
+            mma_commit(&afull[slot]);
+            if (++slot == kSlots) {
+              slot = 0;
+              sph ^= 1u;
+            }
+          }
         }
         if (!ok) break;
-        mma_commit(&tfull[ab]);
-        if (++ab == 2) {
-          ab = 0;
-          aph ^= 1u;
+        if (!kPrecise) {
+          mma_commit(&afull[slot]);
+          if (++slot == kSlots) {
+            slot = 0;
+            sph ^= 1u;
+          }
         }
       }
       // Every MMA issued by this thread has retired once this arrives.
@@ -205,105 +302,85 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quadrant this warp may read
     const int et = threadIdx.x - 64;   // 0..127 among the epilogue threads
-    int ab = 0;
-    uint32_t aph = 0;
-    uint32_t rph = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    constexpr bool argmax = kArgmax;
+    int slot = 0;
+    uint32_t sph = 0, rph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
       const int vt = tile / p.num_chunks;
       const int pc = tile - vt * p.num_chunks;
-      if (!mbar_wait(&tfull[ab], aph)) {
+      const int v = vt * kHeadTileV + q * 32 + lane;
+      const int m0 = pc * N;
+      if (argmax && !mbar_wait(red_free, rph ^ 1u)) {  // previous tile's scratch consumed
         report_timeout(p.err);
         break;
       }
-      tc_fence_after_sync();
-      const int v = vt * kHeadTileV + q * 32 + lane;
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(ab * p.N);
-      const int m0 = pc * p.N;
-      if (p.mode == static_cast<int>(HeadOut::kLogits)) {
-        for (int c0 = 0; c0 < p.N; c0 += 16) {
-          float val[16];
-          tmem_load_16(t_row + c0, val);
-          if (v < p.V) {
+      if constexpr (kPrecise) {
+        float acc[kPrecN];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int m = m0 + c0 + i;
-              if (m < p.M) p.logits[static_cast<size_t>(m) * p.V + v] = val[i];
-            }
+        for (int i = 0; i < kPrecN; ++i) acc[i] = 0.f;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&afull[slot], sph)) {
+            report_timeout(p.err);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int c0 = 0; c0 < kPrecN; c0 += 32) {
+            float val[32];
+            tmem_load_32(t_lane + static_cast<uint32_t>(slot * kPrecN + c0), val);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[c0 + i] += val[i];
+          }
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&afree[slot]);
+          if (++slot == kSlots) {
+            slot = 0;
+            sph ^= 1u;
           }
         }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[ab]);
+        if (!ok) break;
+#pragma unroll
+        for (int c0 = 0; c0 < kPrecN; c0 += 16) {
+          float val[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) val[i] = acc[c0 + i];
+          emit16<kArgmax>(p, val, c0, m0, v, q, lane, red_val, red_idx);
+        }
       } else {
-        // the scratch of the previous tile must have been consumed
-        if (!mbar_wait(red_free, rph ^ 1u)) {
+        if (!mbar_wait(&afull[slot], sph)) {
           report_timeout(p.err);
           break;
         }
-        for (int c0 = 0; c0 < p.N; c0 += 16) {
+        tc_fence_after_sync();
+        const uint32_t t_row = t_lane + static_cast<uint32_t>(slot * N);
+        for (int c0 = 0; c0 < N; c0 += 16) {
           float val[16];
           tmem_load_16(t_row + c0, val);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float bv = val[i];
-            int bi = v;
-            const bool bad = (v < p.V) && !isfinite(bv);
-            if (v >= p.V || bad) {
-              bv = -INFINITY;
-              bi = 0x7fffffff;
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-              const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-              const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-              if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-              }
-            }
-            const bool any_bad = __any_sync(0xffffffffu, bad);
-            if (lane == 0) {
-              red_val[q * 256 + c0 + i] = bv;
-              red_idx[q * 256 + c0 + i] = any_bad ? -2 : bi;
-            }
-          }
+          emit16<kArgmax>(p, val, c0, m0, v, q, lane, red_val, red_idx);
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&tempty[ab]);
-          mbar_arrive(red_full);
+        if (lane == 0) mbar_arrive(&afree[slot]);
+        if (++slot == kSlots) {
+          slot = 0;
+          sph ^= 1u;
         }
+      }
+      if (argmax) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(red_full);
         if (!mbar_wait(red_full, rph)) {
           report_timeout(p.err);
           break;
         }
-        for (int c = et; c < p.N; c += 128) {
-          const int m = m0 + c;
-          if (m >= p.M) continue;
-          float bv = red_val[c];
-          int bi = red_idx[c];
-          bool bad = bi == -2;
-#pragma unroll
-          for (int qq = 1; qq < 4; ++qq) {
-            const float ov = red_val[qq * 256 + c];
-            const int oi = red_idx[qq * 256 + c];
-            bad |= oi == -2;
-            if (ov > bv || (ov == bv && oi < bi)) {
-              bv = ov;
-              bi = oi;
-            }
-          }
-          p.part_max[static_cast<size_t>(vt) * p.M + m] = bv;
-          p.part_idx[static_cast<size_t>(vt) * p.M + m] = bad ? -2 : bi;
-        }
+        argmax_finish(p, N, vt, m0, et, red_val, red_idx);
         __syncwarp();
         if (lane == 0) mbar_arrive(red_free);
         rph ^= 1u;
-      }
-      if (++ab == 2) {
-        ab = 0;
-        aph ^= 1u;
       }
     }
   }
@@ -342,20 +419,42 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t inner, uint64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int kPrecN, bool kArgmax>
+cudaError_t launch_variant(const CUtensorMap& map_w, const CUtensorMap& map_h, const HeadParams& p,
+                           const HeadPlan& h, const DeviceInfo& dev, cudaStream_t stream) {
+  static bool attr_done[64] = {false};
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev.device]) {
+    const cudaError_t e = cudaFuncSetAttribute(head_kernel<kPrecN, kArgmax>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin);
+    if (e != cudaSuccess) return e;
+    attr_done[dev.device] = true;
+  }
+  head_kernel<kPrecN, kArgmax><<<h.grid, kThreads, h.smem_bytes, stream>>>(map_w, map_h, p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 HeadPlan plan_head(int M, int d, int V, const DeviceInfo& dev) {
   HeadPlan h;
-  const int chunks = (M + 255) / 256;
-  const int per = (M + chunks - 1) / chunks;
-  h.N = std::max(16, (per + 15) / 16 * 16);
-  h.num_chunks = (M + h.N - 1) / h.N;
+  if (M <= 64) {
+    h.precise = true;
+    h.N = M <= 32 ? 32 : 64;
+    h.num_chunks = 1;
+    h.tmem_cols = static_cast<uint32_t>(kSlotsPrecise * h.N);
+  } else {
+    const int chunks = (M + 255) / 256;
+    const int per = (M + chunks - 1) / chunks;
+    h.N = std::max(16, (per + 15) / 16 * 16);
+    h.num_chunks = (M + h.N - 1) / h.N;
+    uint32_t cols = 32;
+    while (cols < static_cast<uint32_t>(2 * h.N)) cols <<= 1;
+    h.tmem_cols = cols;
+  }
   h.num_vt = (V + kHeadTileV - 1) / kHeadTileV;
   h.num_tiles = h.num_vt * h.num_chunks;
   h.num_kb = (d + kHeadTileK - 1) / kHeadTileK;
-  uint32_t cols = 32;
-  while (cols < static_cast<uint32_t>(2 * h.N)) cols <<= 1;
-  h.tmem_cols = cols;
   const size_t stage = kABytes + static_cast<size_t>(h.N) * 128;
   const size_t fixed = 1024 + kBarrierBytes + kReduceBytes;
   const size_t budget = static_cast<size_t>(dev.max_smem_optin);
@@ -379,19 +478,13 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
     *encode_failed = true;
     return cudaErrorInvalidValue;
   }
-  static bool attr_set[64] = {false};
-  if (dev.device >= 0 && dev.device < 64 && !attr_set[dev.device]) {
-    cudaError_t e = cudaFuncSetAttribute(head_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         dev.max_smem_optin);
-    if (e != cudaSuccess) return e;
-    attr_set[dev.device] = true;
-  }
   HeadParams p;
   p.M = M;
   p.d = d;
   p.V = V;
   p.N = h.N;
   p.num_chunks = h.num_chunks;
+  p.num_vt = h.num_vt;
   p.num_tiles = h.num_tiles;
   p.num_kb = h.num_kb;
   p.stages = h.stages;
@@ -401,8 +494,13 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
   p.part_max = part_max;
   p.part_idx = part_idx;
   p.err = err;
-  head_kernel<<<h.grid, kThreads, h.smem_bytes, stream>>>(map_w, map_h, p);
-  return cudaGetLastError();
+  const bool am = mode == HeadOut::kArgmax;
+  if (!h.precise) return am ? launch_variant<0, true>(map_w, map_h, p, h, dev, stream)
+                            : launch_variant<0, false>(map_w, map_h, p, h, dev, stream);
+  if (h.N == 32) return am ? launch_variant<32, true>(map_w, map_h, p, h, dev, stream)
+                           : launch_variant<32, false>(map_w, map_h, p, h, dev, stream);
+  return am ? launch_variant<64, true>(map_w, map_h, p, h, dev, stream)
+            : launch_variant<64, false>(map_w, map_h, p, h, dev, stream);
 }
 
 }  // namespace sv

@@ -10,7 +10,8 @@ Tolerances (fp32 kernels against the fp64 oracle):
     boundary of the drawn token's CDF step, measured relative to that step's
     width (counted); see DESIGN.md, "Readings", for why the band is relative;
   * greedy: bit-exact, except rows whose two largest oracle logits are closer
-    than GREEDY_GAP (reported; the argmax then may legitimately differ).
+    than twice the measured logit error (counted; only there may the f32
+    argmax legitimately differ).
 """
 from __future__ import annotations
 
@@ -23,7 +24,11 @@ LOGIT_ATOL = 1e-3
 PROB_RTOL = 1e-5
 ACCEPT_BAND = 1e-4
 DRAW_BAND = 1e-4
-GREEDY_GAP = 1e-5
+
+
+def t32(T: float) -> float:
+    """The temperature as the C ABI receives it (an f32), for the oracle."""
+    return float(np.float32(T))
 
 
 def np64(t) -> np.ndarray:
@@ -76,36 +81,51 @@ def compare_sampling(tok_gpu, n_gpu, ref, K, band_accept=ACCEPT_BAND, band_draw=
     return stats
 
 
-def compare_debug(dbg_gpu, ref, n_gpu, K, rtol=PROB_RTOL):
-    """Probabilities and log-normalisers reported by the GPU against the oracle."""
+def compare_debug(dbg_gpu, ref, n_gpu, K, T=1.0, logit_err=0.0, rtol=PROB_RTOL):
+    """Probabilities and log-normalisers reported by the GPU against the oracle.
+
+    With identical logits (logit_err = 0) the bound is rel 1e-5.  When the
+    target logits come from the GPU's own LM head they differ from the
+    oracle's by up to logit_err (measured, <= 1e-3), which moves log p by at
+    most 2*logit_err/T and log Z_p by at most logit_err/T; the bound widens
+    by exactly that.  Draft-side quantities (q, log Z_q) are inputs and keep
+    rel 1e-5."""
     dbg = np.asarray(dbg_gpu, dtype=np.float64)
     B = dbg.shape[0]
+    dp = 2.0 * logit_err / T
     if K > 0:
-        np.testing.assert_allclose(dbg[:, :K, 0], ref["p_x"], rtol=rtol, atol=0)
+        np.testing.assert_allclose(dbg[:, :K, 0], ref["p_x"], rtol=rtol + dp, atol=0)
         np.testing.assert_allclose(dbg[:, :K, 1], ref["q_x"], rtol=rtol, atol=0)
-        np.testing.assert_allclose(dbg[:, :K, 2], ref["accept_prob"], rtol=rtol, atol=0)
+        np.testing.assert_allclose(dbg[:, :K, 2], ref["accept_prob"], rtol=rtol + dp, atol=0)
         np.testing.assert_allclose(dbg[:, :K, 4], ref["logZ_q"], rtol=rtol, atol=1e-6)
-    np.testing.assert_allclose(dbg[:, :, 3], ref["logZ_p"], rtol=rtol, atol=1e-6)
+    np.testing.assert_allclose(dbg[:, :, 3], ref["logZ_p"], rtol=rtol, atol=1e-6 + logit_err / T)
     n = np.asarray(n_gpu)
     for b in range(B):
         if n[b] == ref["num_accepted"][b]:
-            np.testing.assert_allclose(dbg[b, n[b], 5], ref["residual_mass"][b], rtol=rtol, atol=1e-9)
+            np.testing.assert_allclose(dbg[b, n[b], 5], ref["residual_mass"][b], rtol=rtol, atol=1e-9 + dp)
 
 
-def compare_greedy(tok_gpu, n_gpu, ref, gap=GREEDY_GAP):
+def compare_greedy(tok_gpu, n_gpu, ref, logit_err=0.0):
+    """Greedy results must be identical.  The only admissible difference is a
+    row whose two largest oracle logits are within 2*logit_err (+1e-12) of
+    each other, where the GPU's f32 logits (off by at most logit_err) may
+    order them the other way; such sequences are counted."""
     tok_gpu = np.asarray(tok_gpu)
     n_gpu = np.asarray(n_gpu)
     B = len(n_gpu)
-    ill = 0
+    band = 2.0 * logit_err + 1e-12
+    near_rows, mismatched = 0, 0
     for b in range(B):
         n_o = int(ref["num_accepted"][b])
-        rows = ref["top2_gap"][b, :min(n_o, int(n_gpu[b])) + 1]
-        if (rows < gap).any():
-            ill += 1
-            continue
-        assert int(n_gpu[b]) == n_o, (b, int(n_gpu[b]), n_o)
-        np.testing.assert_array_equal(tok_gpu[b], ref["tokens"][b])
-    return dict(sequences=B, ill_conditioned=ill)
+        rows = ref["top2_gap"][b, :min(n_o, max(int(n_gpu[b]), 0)) + 1]
+        near = bool((rows <= band).any())
+        near_rows += int(near)
+        same = int(n_gpu[b]) == n_o and np.array_equal(tok_gpu[b], ref["tokens"][b])
+        if not same:
+            assert near, (f"sequence {b}: GPU {tok_gpu[b].tolist()} (n={int(n_gpu[b])}) vs oracle "
+                          f"{ref['tokens'][b].tolist()} (n={n_o}); top-2 gaps {rows}")
+            mismatched += 1
+    return dict(sequences=B, near_ties=near_rows, mismatched_near_ties=mismatched)
 
 
 def logits_error(z_gpu: np.ndarray, z_ref: np.ndarray) -> dict:

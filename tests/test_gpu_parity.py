@@ -16,7 +16,8 @@ import oracle
 import speculative_decoding_verification_67_gb300 as sv
 from speculative_decoding_verification_67_gb300 import synth
 
-from _helpers import (LOGIT_ATOL, compare_debug, compare_greedy, compare_sampling, logits_error, np64, np_int)
+from _helpers import (LOGIT_ATOL, compare_debug, compare_greedy, compare_sampling, logits_error, np64, np_int,
+                      t32)
 
 pytestmark = pytest.mark.gpu
 
@@ -96,10 +97,10 @@ def test_verify_from_logits_matches_oracle(B, K, V, T):
     dbg = torch.zeros((B, K + 1, sv.SPEC_DEBUG_FIELDS), device="cuda")
     tok, n = sv.spec_verify_from_logits(zp, zq, x, u, T, out_debug=dbg)
     torch.cuda.synchronize()
-    ref = oracle.verify_sampling(np64(zp).reshape(B, K + 1, V), np64(zq).reshape(B, K, V), np_int(x), np64(u), T)
+    ref = oracle.verify_sampling(np64(zp).reshape(B, K + 1, V), np64(zq).reshape(B, K, V), np_int(x), np64(u), t32(T))
     st = compare_sampling(np_int(tok), np_int(n), ref, K)
     print(f"\nfrom_logits B={B} K={K} V={V} T={T}: {st}")
-    compare_debug(np64(dbg), ref, np_int(n), K)
+    compare_debug(np64(dbg), ref, np_int(n), K, T)
 
 
 def test_tiny_logits_workload():
@@ -112,7 +113,7 @@ def test_tiny_logits_workload():
     torch.cuda.synchronize()
     ref = oracle.verify_sampling(np64(inp["target_logits"]).reshape(B, K + 1, V),
                                  np64(inp["draft_logits"]).reshape(B, K, V), np_int(inp["draft_tokens"]),
-                                 np64(inp["uniforms"]), T)
+                                 np64(inp["uniforms"]), t32(T))
     compare_sampling(np_int(tok), np_int(n), ref, K)
     compare_debug(np64(dbg), ref, np_int(n), K)
 
@@ -129,7 +130,7 @@ def test_many_draws_over_fixed_logits():
         u = us[i].contiguous()
         tok, n = sv.spec_verify_from_logits(zp, zq, x, u, T)
         torch.cuda.synchronize()
-        ref = oracle.verify_sampling(zp64, zq64, x64, np64(u), T)
+        ref = oracle.verify_sampling(zp64, zq64, x64, np64(u), t32(T))
         st = compare_sampling(np_int(tok), np_int(n), ref, K)
         for k in totals:
             totals[k] += st[k]
@@ -185,11 +186,11 @@ def test_spec_verify_small(B, K, d, V, T):
     w = synth.custom("small", B=B, K=K, d=d, V=V, temperature=T, seed=B + K + d + V)
     inp, tok, n, logits, dbg = _run_head_case(w)
     ref = oracle.spec_verify(np64(inp["hidden"]), np64(inp["W"]), np64(inp["draft_logits"]),
-                             np_int(inp["draft_tokens"]), np64(inp["uniforms"]), T, B, K)
+                             np_int(inp["draft_tokens"]), np64(inp["uniforms"]), t32(T), B, K)
     err = logits_error(np64(logits), ref["target_logits"])
     assert err["max_abs"] <= LOGIT_ATOL, err
     st = compare_sampling(np_int(tok), np_int(n), ref, K)
-    compare_debug(np64(dbg), ref, np_int(n), K)
+    compare_debug(np64(dbg), ref, np_int(n), K, T, err["max_abs"])
     print(f"\nspec_verify small {B},{K},{d},{V},{T}: logits {err} {st}")
 
 
@@ -198,15 +199,18 @@ def test_greedy_small(B, K, d, V):
     w = synth.custom("greedy", B=B, K=K, d=d, V=V, temperature=0.0, noise=0.2, seed=B * K + V)
     inp, tok, n, _, dbg = _run_head_case(w)
     ref = oracle.spec_verify(np64(inp["hidden"]), np64(inp["W"]), None, np_int(inp["draft_tokens"]), None, 0.0, B, K)
-    st = compare_greedy(np_int(tok), np_int(n), ref)
-    assert st["ill_conditioned"] == 0, st
-    # greedy from logits on the oracle-independent GPU logits path gives the same
     z = sv.spec_lm_head(inp["hidden"], inp["W"])
+    torch.cuda.synchronize()
+    err = logits_error(np64(z), ref["target_logits"])
+    st = compare_greedy(np_int(tok), np_int(n), ref, err["max_abs"])
+    assert st["mismatched_near_ties"] == 0, st
+    # greedy from the same GPU logits through the other entry point is identical
     tok2, n2 = sv.spec_verify_from_logits(z, None, inp["draft_tokens"], None, 0.0)
     torch.cuda.synchronize()
     assert torch.equal(tok, tok2) and torch.equal(n, n2)
-    # debug: argmax ids and max logits
+    # debug: the row max equals the max of the GPU logits; argmax ids match the oracle
     dbg = np64(dbg)
+    np.testing.assert_array_equal(dbg[:, :, 0].reshape(-1), np64(z).max(axis=1))
     np.testing.assert_array_equal(dbg[:, :, 1].astype(np.int64), ref["argmax"])
 
 
@@ -223,7 +227,7 @@ def test_invalid_draft_token_marks_the_sequence():
     tok = np_int(tok)
     assert n[2] == -1 and (tok[2] == -1).all()
     ref = oracle.verify_sampling(np64(zp).reshape(B, K + 1, V), np64(zq).reshape(B, K, V),
-                                 np.clip(np_int(x), 0, V - 1), np64(u), T)
+                                 np.clip(np_int(x), 0, V - 1), np64(u), t32(T))
     keep = [0, 1, 3]
     sub = {k: v[keep] for k, v in ref.items()}
     compare_sampling(tok[keep], n[keep], sub, K)
@@ -255,7 +259,7 @@ def test_all_accept_and_first_reject_extremes():
         tok, n = sv.spec_verify_from_logits(zp, zq, x, u2, T)
         torch.cuda.synchronize()
         ref = oracle.verify_sampling(np64(zp).reshape(B, K + 1, V), np64(zq).reshape(B, K, V), np_int(x),
-                                     np64(u2), T)
+                                     np64(u2), t32(T))
         compare_sampling(np_int(tok), np_int(n), ref, K)
         if fill == 0.0:
             assert (np_int(n) == K).all()
@@ -281,12 +285,40 @@ def test_full_size_sampling_workload(name):
     w = synth.WORKLOADS[name]
     inp, tok, n, logits, dbg = _run_head_case(w)
     ref = oracle.spec_verify(np64(inp["hidden"]), np64(inp["W"]), np64(inp["draft_logits"]),
-                             np_int(inp["draft_tokens"]), np64(inp["uniforms"]), w.temperature, w.B, w.K)
+                             np_int(inp["draft_tokens"]), np64(inp["uniforms"]), t32(w.temperature), w.B, w.K)
     err = logits_error(np64(logits), ref["target_logits"])
     st = compare_sampling(np_int(tok), np_int(n), ref, w.K)
     print(f"\n{name}: logits {err}; decisions {st}; accepted {np_int(n).tolist()}")
     assert err["max_abs"] <= LOGIT_ATOL, err
-    compare_debug(np64(dbg), ref, np_int(n), w.K)
+    compare_debug(np64(dbg), ref, np_int(n), w.K, w.temperature, err["max_abs"])
+
+
+def test_full_size_many_draws_b8_v128256():
+    """The headline workload with 64 fresh uniform sets over its fixed logits:
+    512 accept/draw decisions of the whole step (GPU LM head included) against
+    the oracle's fp64 logits.  Every mismatch must lie in a band; the band
+    cases stay under 0.1% of the draws."""
+    w = synth.WORKLOADS["head_B8_K4_V128256"]
+    inp = synth.make_inputs(w, device="cuda")
+    B, K, V, T = w.B, w.K, w.V, w.temperature
+    z_gpu = sv.spec_lm_head(inp["hidden"], inp["W"])
+    torch.cuda.synchronize()
+    z_ref = oracle.lm_head(np64(inp["hidden"]), inp["W"].float().cpu().numpy())
+    err = logits_error(np64(z_gpu), z_ref)
+    zq64 = np64(inp["draft_logits"]).reshape(B, K, V)
+    x64 = np_int(inp["draft_tokens"])
+    us = synth.fresh_uniforms(B, K, 64, device="cuda", seed=123)
+    totals = dict(draws=0, accept_exempt=0, draw_exempt=0, draw_mismatch_exempt=0, accept_mismatch_exempt=0)
+    for i in range(us.shape[0]):
+        u = us[i].contiguous()
+        tok, n = sv.spec_verify_from_logits(z_gpu, inp["draft_logits"], inp["draft_tokens"], u, T)
+        torch.cuda.synchronize()
+        ref = oracle.verify_sampling(z_ref.reshape(B, K + 1, V), zq64, x64, np64(u), t32(T))
+        st = compare_sampling(np_int(tok), np_int(n), ref, K)
+        for k in totals:
+            totals[k] += st[k]
+    print(f"\nfull-size many draws: logits {err}; {totals}")
+    assert totals["accept_exempt"] + totals["draw_exempt"] <= max(1, 0.001 * totals["draws"])
 
 
 def test_full_size_70b_head_sampled_sequences():
@@ -302,7 +334,7 @@ def test_full_size_70b_head_sampled_sequences():
     zq_rows = np.concatenate([np.arange(b * K, (b + 1) * K) for b in seqs])
     ref = oracle.verify_sampling(ref_rows.reshape(len(seqs), K + 1, V),
                                  np64(inp["draft_logits"])[zq_rows].reshape(len(seqs), K, V),
-                                 np_int(inp["draft_tokens"])[seqs], np64(inp["uniforms"])[seqs], w.temperature)
+                                 np_int(inp["draft_tokens"])[seqs], np64(inp["uniforms"])[seqs], t32(w.temperature))
     st = compare_sampling(np_int(tok)[seqs], np_int(n)[seqs], ref, K)
     print(f"\n70B head: logits {err}; decisions {st}; accepted {np_int(n).tolist()}")
     # properties that hold for every sequence
@@ -318,9 +350,15 @@ def test_full_size_greedy_sampled_sequences():
     inp, tok, n, _, dbg = _run_head_case(w)
     seqs = list(range(0, 256, 16))
     rows = _sample_rows(w.B, w.K, seqs)
-    z = oracle.lm_head(np64(inp["hidden"])[rows], inp["W"].float().cpu().numpy())
+    h_rows = inp["hidden"][torch.as_tensor(rows, device="cuda")].contiguous()
+    z = oracle.lm_head(np64(h_rows), inp["W"].float().cpu().numpy())
+    z_gpu = sv.spec_lm_head(h_rows, inp["W"])
+    torch.cuda.synchronize()
+    err = logits_error(np64(z_gpu), z)
     ref = oracle.verify_greedy(z.reshape(len(seqs), w.K + 1, w.V), np_int(inp["draft_tokens"])[seqs])
-    st = compare_greedy(np_int(tok)[seqs], np_int(n)[seqs], ref)
-    print(f"\ngreedy full size: {st}; accepted mean {np_int(n).mean():.3f}")
-    assert st["ill_conditioned"] == 0, st
+    st = compare_greedy(np_int(tok)[seqs], np_int(n)[seqs], ref, err["max_abs"])
+    print(f"\ngreedy full size: {st}; logits {err}; accepted mean {np_int(n).mean():.3f}")
+    assert st["mismatched_near_ties"] == 0, st
     np.testing.assert_array_equal(np64(dbg)[seqs][:, :, 1].astype(np.int64), ref["argmax"])
+    # the fused argmax epilogue saw exactly the values the plain LM head writes
+    np.testing.assert_array_equal(np64(dbg)[seqs][:, :, 0].reshape(-1), np64(z_gpu).max(axis=1))
