@@ -20,42 +20,42 @@ size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Workspace layout.  The control block (error word, tickets) is zeroed by a
-// memset at the start of every call; everything else is written before it
-// is read.
+// Workspace layout.  Nothing needs initialising by the caller: the first
+// kernel of a call clears the error word and the decision kernel clears the
+// tickets before the residual pass counts on them.
 struct Layout {
   size_t ctrl_bytes = 0;
-  size_t seq = 0, parts = 0, res = 0, logits = 0;  // sampling
-  size_t pmax = 0, pidx = 0;                       // greedy
-  int CA = 0, CB = 0, P = 0;
+  size_t seq = 0, tpart = 0, dpart = 0, res = 0, logits = 0;  // sampling
+  size_t pmax = 0, pidx = 0;                                   // greedy
+  int CA = 0, P = 0;
   size_t total = 0;
 };
 
-// int[0] error word, int[1 .. 1+B) tickets of pass 1, int[1+B .. 1+2B)
-// tickets of pass 2.
+// int[0] error word, int[1 .. 1+B) tickets of the residual pass.
 constexpr int kCtrlErr = 0, kCtrlTickets = 1;
 
 Layout make_layout(int B, int K, int V, bool greedy, bool logits_in_ws, bool from_logits) {
   Layout L;
   const size_t M = static_cast<size_t>(B) * (K + 1);
-  size_t off = round_up(sizeof(int) * (kCtrlTickets + 2 * static_cast<size_t>(B)));
+  const size_t num_vt = (static_cast<size_t>(V) + sv::kHeadTileV - 1) / sv::kHeadTileV;
+  size_t off = round_up(sizeof(int) * (kCtrlTickets + static_cast<size_t>(B)));
   L.ctrl_bytes = off;
+  L.CA = (V + sv::kChunk - 1) / sv::kChunk;
   if (!greedy) {
-    L.CA = (V + sv::kChunk - 1) / sv::kChunk;
-    L.CB = L.CA;
-    const size_t R = M + static_cast<size_t>(B) * K;
     L.seq = off;
     off += round_up(sizeof(sv::SeqState) * B);
-    L.parts = off;
-    off += round_up(sizeof(sv::ChunkStat) * R * L.CA);
+    L.tpart = off;  // per-tile partials are the most the LM head ever writes
+    off += round_up(sizeof(sv::StatPart) * M * (from_logits ? static_cast<size_t>(L.CA) : num_vt));
+    L.dpart = off;
+    off += round_up(sizeof(sv::StatPart) * static_cast<size_t>(B) * K * L.CA);
     L.res = off;
-    off += round_up(sizeof(float2) * static_cast<size_t>(B) * L.CB);
+    off += round_up(sizeof(float2) * static_cast<size_t>(B) * L.CA);
     if (logits_in_ws) {
       L.logits = off;
       off += round_up(sizeof(float) * M * static_cast<size_t>(V));
     }
   } else {
-    L.P = from_logits ? (V + sv::kChunk - 1) / sv::kChunk : (V + sv::kHeadTileV - 1) / sv::kHeadTileV;
+    L.P = from_logits ? L.CA : static_cast<int>(num_vt);
     L.pmax = off;
     off += round_up(sizeof(float) * static_cast<size_t>(L.P) * M);
     L.pidx = off;
@@ -119,7 +119,7 @@ spec_status check_sampling_inputs(const spec_dims& d, float T, const float* draf
 
 sv::VerifyArgs sampling_args(const Layout& L, const spec_dims& d, float T, const float* zp, const float* zq,
                              const int32_t* x, const float* u, int32_t* out_tokens, int32_t* out_n,
-                             float* out_debug, char* ws) {
+                             float* out_debug, char* ws, int Pt) {
   sv::VerifyArgs a;
   a.B = d.B;
   a.K = d.K;
@@ -134,13 +134,14 @@ sv::VerifyArgs sampling_args(const Layout& L, const spec_dims& d, float T, const
   a.out_debug = out_debug;
   int* ctrl = reinterpret_cast<int*>(ws);
   a.err = ctrl + kCtrlErr;
-  a.tickets_a = reinterpret_cast<unsigned*>(ctrl + kCtrlTickets);
-  a.tickets_b = reinterpret_cast<unsigned*>(ctrl + kCtrlTickets + d.B);
-  a.stats = reinterpret_cast<sv::ChunkStat*>(ws + L.parts);
+  a.tickets = reinterpret_cast<unsigned*>(ctrl + kCtrlTickets);
+  a.tpart = reinterpret_cast<const sv::StatPart*>(ws + L.tpart);
+  a.dpart = reinterpret_cast<const sv::StatPart*>(ws + L.dpart);
+  a.Pt = Pt;
+  a.Pd = L.CA;
   a.seq = reinterpret_cast<sv::SeqState*>(ws + L.seq);
   a.res_sums = reinterpret_cast<float2*>(ws + L.res);
-  a.CA = L.CA;
-  a.CB = L.CB;
+  a.CB = L.CA;
   return a;
 }
 
@@ -210,26 +211,45 @@ spec_status spec_verify(const void* hidden, const void* W_lm, const float* draft
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
   const int M = dims.B * (dims.K + 1);
-  if (cudaMemsetAsync(ws, 0, L.ctrl_bytes, s) != cudaSuccess) return SPEC_ERR_CUDA;
   int* err = reinterpret_cast<int*>(ws) + kCtrlErr;
   bool enc_fail = false;
   cudaError_t e;
   if (greedy) {
     e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kArgmax, nullptr,
-                        reinterpret_cast<float*>(ws + L.pmax), reinterpret_cast<int*>(ws + L.pidx), err, dev, s,
-                        &enc_fail);
-    if (enc_fail) return SPEC_ERR_CUDA;
-    if (e != cudaSuccess) return SPEC_ERR_CUDA;
+                        reinterpret_cast<float*>(ws + L.pmax), reinterpret_cast<int*>(ws + L.pidx), nullptr, err,
+                        true, dev, s, &enc_fail);
+    if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
     const sv::GreedyArgs g = greedy_args(L, dims, draft_tokens, out_tokens, out_num_accepted, out_debug, ws);
     e = sv::launch_greedy_finish(g, s);
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
   }
   float* logits = out_target_logits ? out_target_logits : reinterpret_cast<float*>(ws + L.logits);
-  e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kLogits, logits, nullptr, nullptr, err, dev,
-                      s, &enc_fail);
-  if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
+  const sv::HeadPlan plan = sv::plan_head(M, dims.d, dims.V, sv::HeadOut::kStats, dev);
+  sv::HeadStats hs;
+  sv::exponent_constant(temperature, &hs.c_hi, &hs.c_lo);
+  hs.tpart = reinterpret_cast<sv::StatPart*>(ws + L.tpart);
+  hs.zq = draft_logits;
+  hs.draft_rows = dims.B * dims.K;
+  hs.dpart = reinterpret_cast<sv::StatPart*>(ws + L.dpart);
+  int Pt;
+  if (plan.precise) {
+    // small batch: the LM head's epilogue and side warps produce the statistics
+    e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kStats, logits, nullptr, nullptr, &hs, err,
+                        true, dev, s, &enc_fail);
+    if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
+    Pt = plan.target_parts;
+  } else {
+    // large batch (compute-bound head): logits, then one statistics pass
+    e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kLogits, logits, nullptr, nullptr, nullptr,
+                        err, true, dev, s, &enc_fail);
+    if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
+    e = sv::launch_row_stats(logits, draft_logits, M, dims.B * dims.K, dims.V, hs.c_hi, hs.c_lo, hs.tpart, hs.dpart,
+                             err, s);
+    if (e != cudaSuccess) return SPEC_ERR_CUDA;
+    Pt = L.CA;
+  }
   const sv::VerifyArgs a = sampling_args(L, dims, temperature, logits, draft_logits, draft_tokens, uniforms,
-                                         out_tokens, out_num_accepted, out_debug, ws);
+                                         out_tokens, out_num_accepted, out_debug, ws, Pt);
   e = sv::launch_verify_sampling(a, s);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -254,19 +274,25 @@ spec_status spec_verify_from_logits(const float* target_logits, const float* dra
   if (st != SPEC_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
-  if (cudaMemsetAsync(ws, 0, L.ctrl_bytes, s) != cudaSuccess) return SPEC_ERR_CUDA;
+  int* err = reinterpret_cast<int*>(ws) + kCtrlErr;
+  const int M = dims.B * (dims.K + 1);
   cudaError_t e;
   if (greedy) {
-    const int M = dims.B * (dims.K + 1);
     e = sv::launch_row_argmax(target_logits, M, dims.V, reinterpret_cast<float*>(ws + L.pmax),
-                              reinterpret_cast<int*>(ws + L.pidx), s);
+                              reinterpret_cast<int*>(ws + L.pidx), err, s);
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
     const sv::GreedyArgs g = greedy_args(L, dims, draft_tokens, out_tokens, out_num_accepted, out_debug, ws);
     e = sv::launch_greedy_finish(g, s);
     return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
   }
-  const sv::VerifyArgs a = sampling_args(L, dims, temperature, target_logits, draft_logits, draft_tokens,
-                                         uniforms, out_tokens, out_num_accepted, out_debug, ws);
+  float c_hi, c_lo;
+  sv::exponent_constant(temperature, &c_hi, &c_lo);
+  e = sv::launch_row_stats(target_logits, draft_logits, M, dims.B * dims.K, dims.V, c_hi, c_lo,
+                           reinterpret_cast<sv::StatPart*>(ws + L.tpart), reinterpret_cast<sv::StatPart*>(ws + L.dpart),
+                           err, s);
+  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  const sv::VerifyArgs a = sampling_args(L, dims, temperature, target_logits, draft_logits, draft_tokens, uniforms,
+                                         out_tokens, out_num_accepted, out_debug, ws, L.CA);
   e = sv::launch_verify_sampling(a, s);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -281,7 +307,8 @@ spec_status spec_lm_head(const void* hidden, const void* W_lm, float* logits, in
   if (st != SPEC_OK) return st;
   bool enc_fail = false;
   const cudaError_t e = sv::launch_head(hidden, W_lm, M, d, V, sv::HeadOut::kLogits, logits, nullptr, nullptr,
-                                        nullptr, dev, reinterpret_cast<cudaStream_t>(stream), &enc_fail);
+                                        nullptr, nullptr, false, dev, reinterpret_cast<cudaStream_t>(stream),
+                                        &enc_fail);
   if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
 }

@@ -23,18 +23,33 @@ constexpr int kErrTokenRange = 0x1;
 constexpr int kErrNonFinite = 0x2;
 constexpr int kErrTimeout = 0x4;
 
+// ------------------------------------------------------------------ partials
+constexpr int kChunk = 4096;      // vocabulary tokens per unit of the per-row passes
+constexpr int kMaxK = 32;
+
+// Stored softmax-normaliser partial of one row over some of its tokens:
+// sum of 2^(z*log2(e)/T - k) as a float pair against the integer-valued
+// reference k (-inf when no token contributed).
+struct StatPart {
+  float k;
+  float s_hi, s_lo;
+  int bad;       // a non-finite logit was seen
+};
+
 // ------------------------------------------------------------------ LM head
 // Output modes of the LM-head epilogue.
 enum class HeadOut : int {
   kLogits = 0,   // f32 logits [M][V]
   kArgmax = 1,   // per (row, vocab tile) max and lowest argmax: [M][num_vt]
+  kStats = 2,    // logits, plus softmax partials of every target row and of
+                 // the draft rows (the sampling step's statistics)
 };
 
 constexpr int kHeadTileV = 128;   // vocabulary rows per tile (MMA M)
 constexpr int kHeadTileK = 64;    // hidden elements per pipeline stage (128-byte rows)
 
 struct HeadPlan {
-  bool precise = false; // per-hidden-block TMEM slots summed in registers (N = 32 or 64)
+  bool precise = false; // per-hidden-block TMEM slots summed in registers (N = 32, 48 or 64)
   int N = 0;            // positions per tile (MMA N), multiple of 16, <= 256
   int num_chunks = 0;   // position chunks, ceil(M / N)
   int num_vt = 0;       // vocabulary tiles, ceil(V / 128)
@@ -44,28 +59,30 @@ struct HeadPlan {
   uint32_t tmem_cols = 0;
   size_t smem_bytes = 0;
   int grid = 0;
+  // target-row partials: one per CTA (num_chunks == 1) or one per tile
+  bool per_cta_partials = false;
+  int target_parts = 0;  // partials per target row
 };
 
-HeadPlan plan_head(int M, int d, int V, const DeviceInfo& dev);
+HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev);
+
+// Sampling-step statistics the LM head produces alongside the logits.
+struct HeadStats {
+  float c_hi = 0.f, c_lo = 0.f;   // log2(e) / T as a float pair
+  StatPart* tpart = nullptr;      // [M][plan.target_parts]
+  const float* zq = nullptr;      // draft logits [draft_rows][V]
+  int draft_rows = 0;
+  StatPart* dpart = nullptr;      // [draft_rows][ceil(V / kChunk)]
+};
 
 // Enqueues the LM head.  Returns cudaSuccess or the first CUDA error;
-// *encode_failed is set when building a TMA descriptor failed.
+// *encode_failed is set when building a TMA descriptor failed.  When
+// zero_err is set, the kernel clears *err before anything can report.
 cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, HeadOut mode,
-                        float* logits, float* part_max, int* part_idx, int* err,
-                        const DeviceInfo& dev, cudaStream_t stream, bool* encode_failed);
+                        float* logits, float* part_max, int* part_idx, const HeadStats* stats, int* err,
+                        bool zero_err, const DeviceInfo& dev, cudaStream_t stream, bool* encode_failed);
 
 // ------------------------------------------------------------------ verify
-constexpr int kChunk = 4096;      // vocabulary tokens per CTA of the per-row passes
-constexpr int kMaxK = 32;
-
-// Per (row, chunk) softmax normaliser of z/T: sum over the chunk of
-// 2^(z*log2(e)/T - k), k the chunk's integer reference, as a float pair.
-struct ChunkStat {
-  float k;      // integer-valued reference exponent (base 2)
-  int bad;      // a non-finite logit was seen
-  float s_hi, s_lo;
-};
-
 // Per-sequence state handed from the decision to the residual pass.
 struct SeqState {
   int n;          // accepted drafts
@@ -89,17 +106,25 @@ struct VerifyArgs {
   float* out_debug;         // [B][K+1][6] or null
   // workspace
   int* err;
-  unsigned* tickets_a;      // [B]
-  unsigned* tickets_b;      // [B]
-  ChunkStat* stats;         // [R][CA], R = B*(K+1) + B*K
+  unsigned* tickets;        // [B] (zeroed by the decision kernel)
+  const StatPart* tpart;    // [B*(K+1)][Pt]
+  const StatPart* dpart;    // [B*K][Pd]
+  int Pt, Pd;
   SeqState* seq;            // [B]
   float2* res_sums;         // [B][CB]
-  int CA, CB;
+  int CB;
 };
 
 // log2(e) / T split into a float pair.
 void exponent_constant(float temperature, float* c_hi, float* c_lo);
 
+// Softmax partials of given target and draft logits (per row and 4096-token
+// chunk) for the from-logits entry point; clears *err first.
+cudaError_t launch_row_stats(const float* zp, const float* zq, int M, int draft_rows, int V, float c_hi, float c_lo,
+                             StatPart* tpart, StatPart* dpart, int* err, cudaStream_t stream);
+
+// Decision then residual draw (two launches, chained with programmatic
+// dependent launch).
 cudaError_t launch_verify_sampling(const VerifyArgs& a, cudaStream_t stream);
 
 struct GreedyArgs {
@@ -116,8 +141,28 @@ struct GreedyArgs {
 
 cudaError_t launch_greedy_finish(const GreedyArgs& a, cudaStream_t stream);
 
-// Row argmax partials from given logits ([M][V] -> [M][P], P = ceil(V / kChunk)).
-cudaError_t launch_row_argmax(const float* logits, int M, int V, float* part_max, int* part_idx,
+// Row argmax partials from given logits ([M][V] -> [M][P], P = ceil(V / kChunk));
+// clears *err first.
+cudaError_t launch_row_argmax(const float* logits, int M, int V, float* part_max, int* part_idx, int* err,
                               cudaStream_t stream);
+
+// Launch with programmatic stream serialization: the kernel may start
+// while its predecessor on the stream finishes and must begin with
+// griddep_wait() before touching the predecessor's outputs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 }  // namespace sv

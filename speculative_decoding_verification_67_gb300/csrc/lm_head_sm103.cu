@@ -19,8 +19,12 @@
 //  * warp roles: warp 0 issues TMA loads (W tile 128x64 with an evict-first
 //    L2 hint, hidden tile Nx64 with evict-last), warp 1 allocates TMEM and
 //    issues tcgen05.mma from one thread, warps 2-5 drain TMEM (tcgen05.ld)
-//    and write either the f32 logits or per-tile (max, lowest argmax)
-//    partials for the greedy path;
+//    and write the f32 logits, per-tile (max, lowest argmax) partials for
+//    the greedy path, or the logits plus the softmax(z/T) normaliser
+//    partials of every target row for the sampling path (the epilogue holds
+//    each logit in a register already, so the statistics cost no extra
+//    pass over the logits); in that mode warps 6-7 reduce the draft logits
+//    to the same partials meanwhile, hidden under the weight stream;
 //  * two accumulation schemes.  Standard (any N): one TMEM accumulator per
 //    tile over the whole hidden size, double-buffered so the epilogue of a
 //    tile overlaps the next tile's MMAs.  Precise (N <= 64, the small-batch
@@ -38,25 +42,39 @@
 
 #include "internal.h"
 #include "sm103_ptx.cuh"
+#include "verify_math.cuh"
 
 namespace sv {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 256;  // 8 warps: producer, MMA, 4 epilogue, 2 draft statistics
 constexpr uint32_t kABytes = kHeadTileV * kHeadTileK * 2;  // 16 KB W tile per stage
 constexpr uint32_t kBarrierBytes = 512;
-constexpr uint32_t kReduceBytes = 2 * 4 * 256 * 4;         // argmax scratch
+constexpr uint32_t kReduceBytes = 4 * 4 * 256 * 4;         // per-column scratch of the 4 epilogue warps
 constexpr int kSlotsPrecise = 4;
+
+constexpr int kModeLogits = static_cast<int>(HeadOut::kLogits);
+constexpr int kModeArgmax = static_cast<int>(HeadOut::kArgmax);
+constexpr int kModeStats = static_cast<int>(HeadOut::kStats);
 
 struct HeadParams {
   int M, d, V;
   int N, num_chunks, num_vt, num_tiles, num_kb, stages;
   uint32_t tmem_cols;
-  int mode;
   float* logits;
   float* part_max;
   int* part_idx;
   int* err;
+  int zero_err;
+  // sampling statistics
+  float c_hi, c_lo;
+  StatPart* tpart;
+  int tparts;          // partials per target row
+  int per_cta;         // one partial per CTA (else one per tile)
+  const float* zq;
+  int draft_rows;
+  StatPart* dpart;
+  int dparts;          // partials per draft row = ceil(V / kChunk)
 };
 
 // Timeouts of calls without a workspace (the bare LM head) latch here.
@@ -67,10 +85,12 @@ __device__ __forceinline__ void report_timeout(int* err) {
 }
 
 // Output of 16 columns [c0, c0+16) of this thread's vocabulary row v.
-template <bool kArgmax>
+// Scratch layout (per lane quadrant q and column): argmax uses [0] value,
+// [1] index; statistics use [0] reference k, [1] sum hi, [2] sum lo, [3] bad.
+template <int kMode>
 __device__ __forceinline__ void emit16(const HeadParams& p, const float (&val)[16], int c0, int m0, int v, int q,
-                                       int lane, float* red_val, int* red_idx) {
-  if (!kArgmax) {
+                                       int lane, float* scr) {
+  if (kMode != kModeArgmax) {
     if (v < p.V) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -78,7 +98,10 @@ __device__ __forceinline__ void emit16(const HeadParams& p, const float (&val)[1
         if (m < p.M) p.logits[static_cast<size_t>(m) * p.V + v] = val[i];
       }
     }
-  } else {
+  }
+  if (kMode == kModeArgmax) {
+    float* red_val = scr;
+    int* red_idx = reinterpret_cast<int*>(scr + 1024);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       float bv = val[i];
@@ -104,11 +127,141 @@ __device__ __forceinline__ void emit16(const HeadParams& p, const float (&val)[1
       }
     }
   }
+  if (kMode == kModeStats) {
+    const Expo c{p.c_hi, p.c_lo};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int col = c0 + i;
+      if (m0 + col >= p.M) break;  // uniform across the warp
+      const float z = val[i];
+      const bool in = v < p.V;
+      const float h = expo_hi(z, c);
+      const bool bad = in && !isfinite(h);
+      const float hv = (in && !bad) ? h : -INFINITY;
+      const float hm = warp_max_f(hv);
+      const float kw = (hm == -INFINITY) ? -INFINITY : ceilf(hm);
+      const float t = (hv != -INFINITY) ? exp2f((h - kw) + expo_lo(z, h, c)) : 0.f;
+      const ff sum = warp_sum_ff({t, 0.f});
+      const bool any_bad = __any_sync(0xffffffffu, bad);
+      if (lane == 0) {
+        scr[q * 256 + col] = kw;
+        scr[1024 + q * 256 + col] = sum.hi;
+        scr[2048 + q * 256 + col] = sum.lo;
+        reinterpret_cast<int*>(scr)[3072 + q * 256 + col] = any_bad ? 1 : 0;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void store_part(StatPart* dst, const Partial& a) {
+  StatPart sp;
+  sp.k = a.k;
+  sp.s_hi = a.s.hi;
+  sp.s_lo = a.s.lo;
+  sp.bad = a.bad;
+  *dst = sp;
+}
+
+// Softmax partials of one tile's columns: merge the four lane quadrants;
+// fold into the CTA's running partials (one per CTA) or store per tile.
+__device__ __forceinline__ void stats_finish(const HeadParams& p, int N, int vt, int m0, int et, const float* scr,
+                                             Partial (&run)[2]) {
+  int r = 0;
+  for (int c = et; c < N; c += 128, ++r) {
+    const int m = m0 + c;
+    if (m >= p.M) continue;
+    Partial acc = partial_empty();
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      Partial pq;
+      pq.k = scr[qq * 256 + c];
+      pq.s = {scr[1024 + qq * 256 + c], scr[2048 + qq * 256 + c]};
+      pq.bad = reinterpret_cast<const int*>(scr)[3072 + qq * 256 + c];
+      acc = partial_merge(acc, pq);
+    }
+    if (p.per_cta)
+      run[r] = partial_merge(run[r], acc);
+    else
+      store_part(&p.tpart[static_cast<size_t>(m) * p.tparts + vt], acc);
+  }
+}
+
+// Draft-row statistics by warps 6-7: units of (draft row, 4096-token chunk)
+// taken round-robin over CTAs; each lane streams 128 tokens of the unit in 4
+// blocks of 32, keeping a partial against an integer reference that only
+// moves up (exact rescaling), then the warp merges its lanes.
+__device__ void draft_stats(const HeadParams& p, int side_warp, int lane) {
+  const Expo c{p.c_hi, p.c_lo};
+  const long long units = static_cast<long long>(p.draft_rows) * p.dparts;
+  const bool vec = (p.V % 4) == 0;
+  for (long long i = side_warp;; i += 2) {
+    const long long u = blockIdx.x + i * gridDim.x;
+    if (u >= units) break;
+    const int row = static_cast<int>(u / p.dparts);
+    const int chunk = static_cast<int>(u - static_cast<long long>(row) * p.dparts);
+    const float* z = p.zq + static_cast<size_t>(row) * p.V;
+    Partial lp = partial_empty();
+#pragma unroll 1
+    for (int blk = 0; blk < kChunk / 1024; ++blk) {
+      float zv[32];
+      unsigned valid = 0;
+      const int base = chunk * kChunk + blk * 1024;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int e = base + (j * 32 + lane) * 4;
+        if (vec && e + 3 < p.V) {
+          const float4 f = __ldg(reinterpret_cast<const float4*>(z + e));
+          zv[4 * j] = f.x;
+          zv[4 * j + 1] = f.y;
+          zv[4 * j + 2] = f.z;
+          zv[4 * j + 3] = f.w;
+          valid |= 0xfu << (4 * j);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const bool in = e + t < p.V;
+            zv[4 * j + t] = in ? z[e + t] : 0.f;
+            valid |= in ? (1u << (4 * j + t)) : 0u;
+          }
+        }
+      }
+      float hm = -INFINITY;
+      int bad = 0;
+#pragma unroll
+      for (int t = 0; t < 32; ++t) {
+        if (!((valid >> t) & 1u)) continue;
+        const float h = expo_hi(zv[t], c);
+        if (!isfinite(h)) {
+          bad = 1;
+          valid &= ~(1u << t);
+        } else {
+          hm = fmaxf(hm, h);
+        }
+      }
+      lp.bad |= bad;
+      if (hm == -INFINITY) continue;
+      const float kn = ceilf(hm);
+      if (lp.k == -INFINITY) {
+        lp.k = kn;
+      } else if (kn > lp.k) {
+        lp.s = ff_scale2(lp.s, static_cast<int>(lp.k - kn));
+        lp.k = kn;
+      }
+      float sh = lp.s.hi, sl = lp.s.lo;
+#pragma unroll
+      for (int t = 0; t < 32; ++t)
+        if ((valid >> t) & 1u) ff_accumulate(sh, sl, pow2_rel(zv[t], c, lp.k));
+      lp.s = ff_norm(sh, sl);
+    }
+    const Partial wp = warp_merge(lp);
+    if (lane == 0) store_part(&p.dpart[u], wp);
+  }
 }
 
 // Greedy partials of one tile: combine the four lane quadrants per column.
-__device__ __forceinline__ void argmax_finish(const HeadParams& p, int N, int vt, int m0, int et,
-                                              const float* red_val, const int* red_idx) {
+__device__ __forceinline__ void argmax_finish(const HeadParams& p, int N, int vt, int m0, int et, const float* scr) {
+  const float* red_val = scr;
+  const int* red_idx = reinterpret_cast<const int*>(scr + 1024);
   for (int c = et; c < N; c += 128) {
     const int m = m0 + c;
     if (m >= p.M) continue;
@@ -131,9 +284,8 @@ __device__ __forceinline__ void argmax_finish(const HeadParams& p, int N, int vt
 }
 
 // kPrecN == 0: standard accumulation; kPrecN == 32 or 64: precise
-// accumulation with N == kPrecN.  kArgmax selects the greedy partials
-// epilogue instead of the logits one.
-template <int kPrecN, bool kArgmax>
+// accumulation with N == kPrecN.  kMode: HeadOut as int.
+template <int kPrecN, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_h,
                 const HeadParams p) {
@@ -155,12 +307,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* red_full = mma_done + 1;  // [1] argmax scratch written by the 4 epilogue warps
   uint64_t* red_free = red_full + 1;  // [1] argmax scratch consumed
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(red_free + 1);
-  float* red_val = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kBarrierBytes);
-  int* red_idx = reinterpret_cast<int*>(red_val + 4 * 256);
+  float* scr = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kBarrierBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  if (p.zero_err && blockIdx.x == 0 && threadIdx.x == 0) *p.err = 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -217,6 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      griddep_launch_dependents();
       // Let the last copies land before the CTA can exit (they complete the
       // `full` phase they were issued for; in a normal run that phase has
       // long completed and the waits return at once).
@@ -298,12 +451,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(mma_done);
       if (!mbar_wait(mma_done, 0)) report_timeout(p.err);
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;            // TMEM lane quadrant this warp may read
     const int et = threadIdx.x - 64;   // 0..127 among the epilogue threads
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    constexpr bool argmax = kArgmax;
+    // precise statistics keep per-thread running partials instead of
+    // reducing every tile across the quadrants
+    constexpr bool run_stats = kPrecise && kMode == kModeStats;
+    constexpr bool reduce = kMode != kModeLogits && !run_stats;  // cross-quadrant scratch per tile
+    constexpr int kRun = run_stats ? kPrecN : 1;
+    Partial run[2] = {partial_empty(), partial_empty()};
+    float rk[kRun], rs[kRun];
+    uint64_t badmask = 0;
+#pragma unroll
+    for (int i = 0; i < kRun; ++i) {
+      rk[i] = -INFINITY;
+      rs[i] = 0.f;
+    }
     int slot = 0;
     uint32_t sph = 0, rph = 0;
     bool ok = true;
@@ -312,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pc = tile - vt * p.num_chunks;
       const int v = vt * kHeadTileV + q * 32 + lane;
       const int m0 = pc * N;
-      if (argmax && !mbar_wait(red_free, rph ^ 1u)) {  // previous tile's scratch consumed
+      if (reduce && !mbar_wait(red_free, rph ^ 1u)) {  // previous tile's scratch consumed
         report_timeout(p.err);
         break;
       }
@@ -327,12 +492,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after_sync();
+          if constexpr (kPrecN == 48) {
+            float val[48];
+            tmem_load_48(t_lane + static_cast<uint32_t>(slot * kPrecN), val);
 #pragma unroll
-          for (int c0 = 0; c0 < kPrecN; c0 += 32) {
-            float val[32];
-            tmem_load_32(t_lane + static_cast<uint32_t>(slot * kPrecN + c0), val);
+            for (int i = 0; i < 48; ++i) acc[i] += val[i];
+          } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[c0 + i] += val[i];
+            for (int c0 = 0; c0 < kPrecN; c0 += 32) {
+              float val[32];
+              tmem_load_32(t_lane + static_cast<uint32_t>(slot * kPrecN + c0), val);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) acc[c0 + i] += val[i];
+            }
           }
           tc_fence_before_sync();
           __syncwarp();
@@ -343,12 +515,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
+        if constexpr (run_stats) {
+          // logits out, and fold this row's value of every column into the
+          // thread's running partial of that column (exact rescaling)
+          const Expo c{p.c_hi, p.c_lo};
+          if (v < p.V) {
 #pragma unroll
-        for (int c0 = 0; c0 < kPrecN; c0 += 16) {
-          float val[16];
+            for (int i = 0; i < kPrecN; ++i) {
+              if (i >= p.M) break;
+              const float z = acc[i];
+              p.logits[static_cast<size_t>(i) * p.V + v] = z;
+              const float h = expo_hi(z, c);
+              if (!isfinite(h)) {
+                badmask |= 1ull << i;
+                continue;
+              }
+              const float kn = fmaxf(rk[i], ceilf(h));
+              rs[i] = ldexpf(rs[i], static_cast<int>(fmaxf(rk[i] - kn, -200.f)));
+              rk[i] = kn;
+              rs[i] += exp2f((h - kn) + expo_lo(z, h, c));
+            }
+          }
+        } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) val[i] = acc[c0 + i];
-          emit16<kArgmax>(p, val, c0, m0, v, q, lane, red_val, red_idx);
+          for (int c0 = 0; c0 < kPrecN; c0 += 16) {
+            float val[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) val[i] = acc[c0 + i];
+            emit16<kMode>(p, val, c0, m0, v, q, lane, scr);
+          }
         }
       } else {
         if (!mbar_wait(&afull[slot], sph)) {
@@ -360,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c0 = 0; c0 < N; c0 += 16) {
           float val[16];
           tmem_load_16(t_row + c0, val);
-          emit16<kArgmax>(p, val, c0, m0, v, q, lane, red_val, red_idx);
+          emit16<kMode>(p, val, c0, m0, v, q, lane, scr);
         }
         tc_fence_before_sync();
         __syncwarp();
@@ -370,19 +565,65 @@ __global__ void __launch_bounds__(kThreads, 1)
           sph ^= 1u;
         }
       }
-      if (argmax) {
+      if (reduce) {
         __syncwarp();
         if (lane == 0) mbar_arrive(red_full);
         if (!mbar_wait(red_full, rph)) {
           report_timeout(p.err);
           break;
         }
-        argmax_finish(p, N, vt, m0, et, red_val, red_idx);
+        if (kMode == kModeArgmax) argmax_finish(p, N, vt, m0, et, scr);
+        if (kMode == kModeStats) stats_finish(p, N, vt, m0, et, scr, run);
         __syncwarp();
         if (lane == 0) mbar_arrive(red_free);
         rph ^= 1u;
       }
     }
+    if constexpr (run_stats) {
+      // Merge the 128 threads' running partials per column through shared
+      // memory (the pipeline stages are idle now: every load has been
+      // consumed), several threads per column, then one partial per CTA.
+      float2* tr = reinterpret_cast<float2*>(smem);            // [kPrecN][128]
+      uint64_t* bm = reinterpret_cast<uint64_t*>(tr + kPrecN * 128);
+#pragma unroll
+      for (int i = 0; i < kPrecN; ++i) tr[i * 128 + et] = make_float2(rk[i], rs[i]);
+      bm[et] = badmask;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(red_full);
+      if (!mbar_wait(red_full, 0)) {
+        report_timeout(p.err);
+      } else {
+        constexpr int kTpc = kPrecN == 32 ? 4 : 2;             // threads per column
+        constexpr int kSpan = 128 / kTpc;                      // partials each merges
+        const int col = et / kTpc, part = et % kTpc;
+        Partial acc = partial_empty();
+        for (int t = part * kSpan; col < kPrecN && t < (part + 1) * kSpan; ++t) {
+          const float2 w = tr[col * 128 + t];
+          Partial pt;
+          pt.k = w.x;
+          pt.s = {w.y, 0.f};
+          pt.bad = static_cast<int>((bm[t] >> col) & 1ull);
+          acc = partial_merge(acc, pt);
+        }
+#pragma unroll
+        for (int off = 1; off < kTpc; off <<= 1) {
+          Partial o;
+          o.k = __shfl_xor_sync(0xffffffffu, acc.k, off);
+          o.s = shfl_xor_ff(acc.s, off);
+          o.bad = __shfl_xor_sync(0xffffffffu, acc.bad, off);
+          acc = partial_merge(acc, o);
+        }
+        if (part == 0 && col < kPrecN && col < p.M)
+          store_part(&p.tpart[static_cast<size_t>(col) * p.tparts + blockIdx.x], acc);
+      }
+    } else if (kMode == kModeStats && p.per_cta) {
+      int r = 0;
+      for (int c = et; c < N; c += 128, ++r)
+        if (c < p.M) store_part(&p.tpart[static_cast<size_t>(c) * p.tparts + blockIdx.x], run[r]);
+    }
+  } else if (kMode == kModeStats) {
+    // ------------------------------------------------------------ draft statistics
+    draft_stats(p, warp - 6, lane);
   }
 
   tc_fence_before_sync();
@@ -419,30 +660,44 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, uint64_t inner, uint64
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int kPrecN, bool kArgmax>
+template <int kPrecN, int kMode>
 cudaError_t launch_variant(const CUtensorMap& map_w, const CUtensorMap& map_h, const HeadParams& p,
                            const HeadPlan& h, const DeviceInfo& dev, cudaStream_t stream) {
   static bool attr_done[64] = {false};
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev.device]) {
-    const cudaError_t e = cudaFuncSetAttribute(head_kernel<kPrecN, kArgmax>,
+    const cudaError_t e = cudaFuncSetAttribute(head_kernel<kPrecN, kMode>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin);
     if (e != cudaSuccess) return e;
     attr_done[dev.device] = true;
   }
-  head_kernel<kPrecN, kArgmax><<<h.grid, kThreads, h.smem_bytes, stream>>>(map_w, map_h, p);
+  head_kernel<kPrecN, kMode><<<h.grid, kThreads, h.smem_bytes, stream>>>(map_w, map_h, p);
   return cudaGetLastError();
+}
+
+template <int kPrecN>
+cudaError_t launch_mode(HeadOut mode, const CUtensorMap& map_w, const CUtensorMap& map_h, const HeadParams& p,
+                        const HeadPlan& h, const DeviceInfo& dev, cudaStream_t stream) {
+  switch (mode) {
+    case HeadOut::kLogits: return launch_variant<kPrecN, kModeLogits>(map_w, map_h, p, h, dev, stream);
+    case HeadOut::kArgmax: return launch_variant<kPrecN, kModeArgmax>(map_w, map_h, p, h, dev, stream);
+    case HeadOut::kStats: return launch_variant<kPrecN, kModeStats>(map_w, map_h, p, h, dev, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-HeadPlan plan_head(int M, int d, int V, const DeviceInfo& dev) {
+HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev) {
   HeadPlan h;
   if (M <= 64) {
     h.precise = true;
-    h.N = M <= 32 ? 32 : 64;
+    h.N = M <= 32 ? 32 : (M <= 48 ? 48 : 64);
     h.num_chunks = 1;
-    h.tmem_cols = static_cast<uint32_t>(kSlotsPrecise * h.N);
+    // tcgen05.alloc takes a power of two >= 32 columns
+    uint32_t cols = 32;
+    while (cols < static_cast<uint32_t>(kSlotsPrecise * h.N)) cols <<= 1;
+    h.tmem_cols = cols;
   } else {
     const int chunks = (M + 255) / 256;
     const int per = (M + chunks - 1) / chunks;
@@ -456,21 +711,26 @@ HeadPlan plan_head(int M, int d, int V, const DeviceInfo& dev) {
   h.num_tiles = h.num_vt * h.num_chunks;
   h.num_kb = (d + kHeadTileK - 1) / kHeadTileK;
   const size_t stage = kABytes + static_cast<size_t>(h.N) * 128;
-  const size_t fixed = 1024 + kBarrierBytes + kReduceBytes;
+  // the cross-quadrant scratch is used by the greedy epilogue and by the
+  // per-tile statistics of the standard scheme only
+  const bool scratch = mode == HeadOut::kArgmax || (!h.precise && mode == HeadOut::kStats);
+  const size_t fixed = 1024 + kBarrierBytes + (scratch ? kReduceBytes : 0);
   const size_t budget = static_cast<size_t>(dev.max_smem_optin);
   int stages = static_cast<int>((budget - fixed) / stage);
   stages = std::min(12, std::max(2, stages));
   h.stages = stages;
   h.smem_bytes = fixed + static_cast<size_t>(stages) * stage;
   h.grid = std::min(h.num_tiles, dev.sm_count);
+  h.per_cta_partials = h.num_chunks == 1;
+  h.target_parts = h.per_cta_partials ? h.grid : h.num_vt;
   return h;
 }
 
 cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, HeadOut mode, float* logits,
-                        float* part_max, int* part_idx, int* err, const DeviceInfo& dev, cudaStream_t stream,
-                        bool* encode_failed) {
+                        float* part_max, int* part_idx, const HeadStats* stats, int* err, bool zero_err,
+                        const DeviceInfo& dev, cudaStream_t stream, bool* encode_failed) {
   *encode_failed = false;
-  const HeadPlan h = plan_head(M, d, V, dev);
+  const HeadPlan h = plan_head(M, d, V, mode, dev);
   CUtensorMap map_w, map_h;
   if (!encode_bf16_rows(&map_w, W, static_cast<uint64_t>(d), static_cast<uint64_t>(V), kHeadTileV) ||
       !encode_bf16_rows(&map_h, hidden, static_cast<uint64_t>(d), static_cast<uint64_t>(M),
@@ -478,7 +738,7 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
     *encode_failed = true;
     return cudaErrorInvalidValue;
   }
-  HeadParams p;
+  HeadParams p = {};
   p.M = M;
   p.d = d;
   p.V = V;
@@ -489,18 +749,27 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
   p.num_kb = h.num_kb;
   p.stages = h.stages;
   p.tmem_cols = h.tmem_cols;
-  p.mode = static_cast<int>(mode);
   p.logits = logits;
   p.part_max = part_max;
   p.part_idx = part_idx;
   p.err = err;
-  const bool am = mode == HeadOut::kArgmax;
-  if (!h.precise) return am ? launch_variant<0, true>(map_w, map_h, p, h, dev, stream)
-                            : launch_variant<0, false>(map_w, map_h, p, h, dev, stream);
-  if (h.N == 32) return am ? launch_variant<32, true>(map_w, map_h, p, h, dev, stream)
-                           : launch_variant<32, false>(map_w, map_h, p, h, dev, stream);
-  return am ? launch_variant<64, true>(map_w, map_h, p, h, dev, stream)
-            : launch_variant<64, false>(map_w, map_h, p, h, dev, stream);
+  p.zero_err = (zero_err && err) ? 1 : 0;
+  if (mode == HeadOut::kStats) {
+    if (!stats) return cudaErrorInvalidValue;
+    p.c_hi = stats->c_hi;
+    p.c_lo = stats->c_lo;
+    p.tpart = stats->tpart;
+    p.tparts = h.target_parts;
+    p.per_cta = h.per_cta_partials ? 1 : 0;
+    p.zq = stats->zq;
+    p.draft_rows = stats->draft_rows;
+    p.dpart = stats->dpart;
+    p.dparts = (V + kChunk - 1) / kChunk;
+  }
+  if (!h.precise) return launch_mode<0>(mode, map_w, map_h, p, h, dev, stream);
+  if (h.N == 32) return launch_mode<32>(mode, map_w, map_h, p, h, dev, stream);
+  if (h.N == 48) return launch_mode<48>(mode, map_w, map_h, p, h, dev, stream);
+  return launch_mode<64>(mode, map_w, map_h, p, h, dev, stream);
 }
 
 }  // namespace sv

@@ -1,36 +1,30 @@
 // Vocabulary-parallel verify-and-accept kernels (sm_103a, CUDA cores).
 //
-// Sampling path (T > 0), two launches after the LM head:
+// Sampling path (T > 0).  The softmax(z/T) normaliser partials of every
+// target row and draft row come from the LM-head kernel (its epilogue and
+// two side warps) or, on given logits, from row_stats_kernel.  Then two
+// launches chained with programmatic dependent launch:
 //
-//  1. stats_kernel, grid (rows) x (chunks of 4096 tokens): every target row
-//     z_p[b,j] (j = 0..K) and draft row z_q[b,j] (j < K) is read once with
-//     128-bit loads and reduced to its softmax(z/T) normaliser (page
-//     "quochung.cyou" A.I article, section "Forward pass": the scores form a
-//     distribution summing to 100%).  The last CTA of each sequence (atomic
-//     ticket; no CTA ever waits for another) combines the chunks, gathers
-//     p_j(x_j) and q_j(x_j), runs the accept test u_j < min(1, p_j(x_j) /
-//     q_j(x_j)) (section "Modified rejection sampling / Giải pháp"), takes
-//     the accepted prefix with one warp ballot (section "Áp dụng thuật
-//     toán": left to right, stop at the first rejection) and writes the
-//     accepted tokens.
+//  1. decide_kernel, one CTA per sequence: merges the partials of the
+//     sequence's 2K+1 rows into their normalisers (page "quochung.cyou"
+//     A.I article, section "Forward pass": the scores form a distribution
+//     summing to 100%), gathers p_j(x_j) and q_j(x_j), runs the accept test
+//     u_j < min(1, p_j(x_j) / q_j(x_j)) (section "Modified rejection
+//     sampling / Giải pháp"), takes the accepted prefix with one warp ballot
+//     (section "Áp dụng thuật toán": left to right, stop at the first
+//     rejection) and writes the accepted tokens.
 //  2. residual_kernel, grid (sequences) x (chunks of 4096 tokens): the row
 //     pair at the first rejection n_b is read once more and reduced to the
 //     mass of max(0, p - q) per chunk (section "Khi reject thì lấy token từ
 //     đâu?"), or of p_K for the bonus token when n_b = K.  The last CTA of
-//     the sequence finds the chunk holding u*S and rescans it with a
-//     block-wide prefix scan for the smallest token whose cumulative mass
-//     exceeds u*S (inverse CDF, ascending token id).
+//     the sequence (atomic ticket; no CTA ever waits for another) finds the
+//     chunk holding u*S and rescans it with a block-wide prefix scan for the
+//     smallest token whose cumulative mass exceeds u*S (inverse CDF,
+//     ascending token id).
 //
-// Arithmetic.  exp(z/T) is evaluated as 2^(z*c) with c = log2(e)/T carried
-// as a pair of floats, so z*c is exact to ~1e-14 and no rounded temperature
-// or log2(e) scales every exponent the same way.  Each chunk sums
-// 2^(z*c - k_c) against an integer reference k_c (the ceiling of its largest
-// exponent): rescaling chunks to a common reference is then an exact power
-// of two.  Sums are compensated (float-float), so the normalisers, their
-// ratio kappa = S_p / S_q and the residual's prefix sums carry no
-// systematic error larger than ~1e-12; the only per-token error left is the
-// f32 rounding of one exponent and one exp2f, which is random across tokens.
-// Nothing here uses f64 (slow on this part).
+// Arithmetic: see verify_math.cuh (exact power-of-two rescaling of
+// partials, float-float sums, exponent map z * log2(e)/T as a float pair);
+// nothing here uses f64 (slow on this part).
 //
 // Greedy path (T = 0): the LM head writes per-(row, vocabulary tile)
 // (max, lowest argmax) partials; greedy_finish_kernel reduces them and
@@ -40,6 +34,8 @@
 #include <climits>
 
 #include "internal.h"
+#include "sm103_ptx.cuh"
+#include "verify_math.cuh"
 
 namespace sv {
 namespace {
@@ -49,86 +45,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kPer = kChunk / kThreads;  // 16 tokens per thread
 static_assert(kPer == 16, "load16 handles 16 tokens per thread");
 
-// ------------------------------------------------------------ float-float
-struct ff {
-  float hi, lo;
-};
-
-// a + b exactly as hi + lo (Knuth's TwoSum).
-__device__ __forceinline__ ff two_sum(float a, float b) {
-  const float s = a + b;
-  const float bb = s - a;
-  const float e = (a - (s - bb)) + (b - bb);
-  return {s, e};
-}
-
-__device__ __forceinline__ ff ff_norm(float hi, float lo) {
-  const float s = hi + lo;
-  return {s, lo - (s - hi)};
-}
-
-__device__ __forceinline__ ff ff_add(ff a, ff b) {
-  const ff s = two_sum(a.hi, b.hi);
-  return ff_norm(s.hi, s.lo + a.lo + b.lo);
-}
-
-__device__ __forceinline__ ff ff_add_f(ff a, float b) {
-  const ff s = two_sum(a.hi, b);
-  return ff_norm(s.hi, s.lo + a.lo);
-}
-
-// a > b for normalised pairs.
-__device__ __forceinline__ bool ff_gt(ff a, ff b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
-
-__device__ __forceinline__ ff ff_scale2(ff a, int e) { return {ldexpf(a.hi, e), ldexpf(a.lo, e)}; }
-
-__device__ __forceinline__ ff ff_mul_f(ff a, float b) {
-  const float p = a.hi * b;
-  const float e = fmaf(a.hi, b, -p);
-  return ff_norm(p, e + a.lo * b);
-}
-
-// a / b to ~1e-14 (one correction step of the f32 quotient).
-__device__ __forceinline__ ff ff_div(ff a, ff b) {
-  const float q1 = a.hi / b.hi;
-  const ff qb = ff_mul_f(b, q1);
-  const ff r = ff_add(a, {-qb.hi, -qb.lo});
-  const float q2 = r.hi / b.hi;
-  return ff_norm(q1, q2);
-}
-
-__device__ __forceinline__ ff shfl_xor_ff(ff v, int off) {
-  return {__shfl_xor_sync(0xffffffffu, v.hi, off), __shfl_xor_sync(0xffffffffu, v.lo, off)};
-}
-
-__device__ __forceinline__ ff warp_sum_ff(ff v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = ff_add(v, shfl_xor_ff(v, off));
-  return v;
-}
-
-// ------------------------------------------------------------ exponent map
-// z * c as a float pair, c = log2(e) / T given as (ch, cl).
-struct Expo {
-  float ch, cl;
-};
-
-__device__ __forceinline__ ff expo(float z, Expo c) {
-  const float h = z * c.ch;
-  const float l = fmaf(z, c.ch, -h) + z * c.cl;
-  return ff_norm(h, l);
-}
-
-// 2^(y - k) for an integer-valued float k.
-__device__ __forceinline__ float pow2_rel(ff y, float k) { return exp2f((y.hi - k) + y.lo); }
-
 // ------------------------------------------------------------ block helpers
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-  return v;
-}
-
 __device__ __forceinline__ int warp_max_i(int v) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, off));
@@ -208,40 +125,94 @@ __device__ __forceinline__ void load16(const float* __restrict__ row, int e0, in
   }
 }
 
+// ---------------------------------------------------------------- statistics
+// Softmax partial of one (row, chunk) of given logits; thread partials are
+// merged across the block (exact rescaling), no barrier before the merge.
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) row_stats_kernel(const float* __restrict__ zp,
+                                                             const float* __restrict__ zq, int M, int V, Expo c,
+                                                             StatPart* tpart, StatPart* dpart, int P, int* err) {
+  __shared__ Partial sm[kWarps];
+  const int row = blockIdx.x, chunk = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (row == 0 && chunk == 0 && threadIdx.x == 0) *err = 0;
+  const bool target = row < M;
+  const float* z = target ? zp + static_cast<size_t>(row) * V : zq + static_cast<size_t>(row - M) * V;
+  float v[kPer];
+  unsigned valid;
+  load16<kVec>(z, chunk * kChunk + threadIdx.x * kPer, V, v, valid);
+  Partial tp = partial_empty();
+  float hm = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    if (!((valid >> i) & 1u)) continue;
+    const float h = expo_hi(v[i], c);
+    if (!isfinite(h)) {
+      tp.bad = 1;
+      valid &= ~(1u << i);
+    } else {
+      hm = fmaxf(hm, h);
+    }
+  }
+  if (hm != -INFINITY) {
+    tp.k = ceilf(hm);
+    float sh = 0.f, sl = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i)
+      if ((valid >> i) & 1u) ff_accumulate(sh, sl, pow2_rel(v[i], c, tp.k));
+    tp.s = ff_norm(sh, sl);
+  }
+  tp = warp_merge(tp);
+  if (lane == 0) sm[warp] = tp;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Partial acc = sm[0];
+    for (int w = 1; w < kWarps; ++w) acc = partial_merge(acc, sm[w]);
+    StatPart out;
+    out.k = acc.k;
+    out.s_hi = acc.s.hi;
+    out.s_lo = acc.s.lo;
+    out.bad = acc.bad;
+    if (target)
+      tpart[static_cast<size_t>(row) * P + chunk] = out;
+    else
+      dpart[static_cast<size_t>(row - M) * P + chunk] = out;
+  }
+}
+
 // ---------------------------------------------------------------- decision
-// Run by the whole block of the last statistics CTA of sequence b.
-__device__ void decide_sequence(const VerifyArgs& a, int b) {
+// One CTA per sequence: merge the partials of its 2K+1 rows, run the accept
+// tests, take the accepted prefix, write the accepted tokens and hand the
+// row pair at the first rejection (or the bonus row) to the residual pass.
+__global__ void __launch_bounds__(kThreads) decide_kernel(const VerifyArgs a) {
   __shared__ float rk[2 * kMaxK + 1];
   __shared__ ff rS[2 * kMaxK + 1];
   __shared__ int rbad[2 * kMaxK + 1];
+  griddep_wait();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.x;
   const int K = a.K;
-  const int M = a.B * (K + 1);
   const int nrows = 2 * K + 1;
+  if (threadIdx.x == 0) a.tickets[b] = 0u;
 
-  // combine the chunk partials of every row of the sequence, one warp per row
   for (int r = warp; r < nrows; r += kWarps) {
-    const int grow = r <= K ? b * (K + 1) + r : M + b * K + (r - K - 1);
-    const ChunkStat* pp = a.stats + static_cast<size_t>(grow) * a.CA;
-    float kmax = -INFINITY;
-    int bad = 0;
-    for (int c = lane; c < a.CA; c += 32) {
-      kmax = fmaxf(kmax, __ldcg(&pp[c].k));
-      bad |= __ldcg(&pp[c].bad);
+    const StatPart* pp = r <= K ? a.tpart + static_cast<size_t>(b * (K + 1) + r) * a.Pt
+                                : a.dpart + static_cast<size_t>(b * K + (r - K - 1)) * a.Pd;
+    const int np = r <= K ? a.Pt : a.Pd;
+    Partial acc = partial_empty();
+    for (int i = lane; i < np; i += 32) {
+      const float4 w = __ldcg(reinterpret_cast<const float4*>(pp + i));
+      Partial pi;
+      pi.k = w.x;
+      pi.s = {w.y, w.z};
+      pi.bad = __float_as_int(w.w);
+      acc = partial_merge(acc, pi);
     }
-    kmax = warp_max(kmax);
-    ff s{0.f, 0.f};
-    for (int c = lane; c < a.CA; c += 32) {
-      const float kc = __ldcg(&pp[c].k);
-      const ff sc{__ldcg(&pp[c].s_hi), __ldcg(&pp[c].s_lo)};
-      if (sc.hi > 0.f) s = ff_add(s, ff_scale2(sc, static_cast<int>(kc - kmax)));
-    }
-    s = warp_sum_ff(s);
-    bad = __any_sync(0xffffffffu, bad != 0) ? 1 : 0;
+    acc = warp_merge(acc);
     if (lane == 0) {
-      rk[r] = kmax;
-      rS[r] = s;
-      rbad[r] = bad || !(s.hi > 0.f) || !isfinite(s.hi) || !isfinite(kmax);
+      rk[r] = acc.k;
+      rS[r] = acc.s;
+      rbad[r] = acc.bad || !(acc.s.hi > 0.f) || !isfinite(acc.s.hi) || !isfinite(acc.k);
     }
   }
   __syncthreads();
@@ -257,9 +228,9 @@ __device__ void decide_sequence(const VerifyArgs& a, int b) {
     if (tok_ok) {
       const float zp = a.zp[static_cast<size_t>(b * (K + 1) + lane) * a.V + xj];
       const float zq = a.zq[static_cast<size_t>(b * K + lane) * a.V + xj];
-      const ff yp = expo(zp, c), yq = expo(zq, c);
-      const float lp = (yp.hi - rk[lane]) + yp.lo;          // log2 of S_p * p(x)
-      const float lq = (yq.hi - rk[K + 1 + lane]) + yq.lo;  // log2 of S_q * q(x)
+      const float hp = expo_hi(zp, c), hq = expo_hi(zq, c);
+      const float lp = (hp - rk[lane]) + expo_lo(zp, hp, c);          // log2 of S_p * p(x)
+      const float lq = (hq - rk[K + 1 + lane]) + expo_lo(zq, hq, c);  // log2 of S_q * q(x)
       const float Sp = rS[lane].hi, Sq = rS[K + 1 + lane].hi;
       pj = exp2f(lp) / Sp;
       qj = exp2f(lq) / Sq;
@@ -313,63 +284,6 @@ __device__ void decide_sequence(const VerifyArgs& a, int b) {
   }
 }
 
-// ---------------------------------------------------------------- pass 1
-template <bool kVec>
-__global__ void __launch_bounds__(kThreads) stats_kernel(const VerifyArgs a) {
-  __shared__ float sm_f[kWarps];
-  __shared__ ff sm_ff[kWarps];
-  __shared__ int sm_i[1];
-  const int row = blockIdx.x, chunk = blockIdx.y;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int M = a.B * (a.K + 1);
-  const bool target = row < M;
-  const float* z = target ? a.zp + static_cast<size_t>(row) * a.V : a.zq + static_cast<size_t>(row - M) * a.V;
-  const int b = target ? row / (a.K + 1) : (row - M) / a.K;
-  const Expo c{a.c_hi, a.c_lo};
-
-  float v[kPer];
-  unsigned valid;
-  load16<kVec>(z, chunk * kChunk + threadIdx.x * kPer, a.V, v, valid);
-  ff y[kPer];
-  float ymax = -INFINITY;
-  int bad = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    const bool in = (valid >> i) & 1u;
-    bad |= in && !isfinite(v[i]);
-    y[i] = expo(v[i], c);
-    if (in) ymax = fmaxf(ymax, y[i].hi);
-  }
-  ymax = warp_max(ymax);
-  if (lane == 0) sm_f[warp] = ymax;
-  __syncthreads();
-  float kc = sm_f[0];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) kc = fmaxf(kc, sm_f[w]);
-  kc = ceilf(kc);
-  ff s{0.f, 0.f};
-#pragma unroll
-  for (int i = 0; i < kPer; ++i)
-    if ((valid >> i) & 1u) s = ff_add_f(s, pow2_rel(y[i], kc));
-  s = warp_sum_ff(s);
-  const int any_bad = __syncthreads_or(bad);
-  if (lane == 0) sm_ff[warp] = s;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    ff t = sm_ff[0];
-    for (int w = 1; w < kWarps; ++w) t = ff_add(t, sm_ff[w]);
-    ChunkStat cs;
-    cs.k = kc;
-    cs.bad = any_bad;
-    cs.s_hi = t.hi;
-    cs.s_lo = t.lo;
-    a.stats[static_cast<size_t>(row) * a.CA + chunk] = cs;
-  }
-  const unsigned expected = static_cast<unsigned>((2 * a.K + 1) * a.CA);
-  if (!last_block_ticket(&a.tickets_a[b], expected, sm_i)) return;
-  decide_sequence(a, b);
-}
-
 // ---------------------------------------------------------------- pass 2
 struct ResRow {
   const float* zp;
@@ -383,9 +297,9 @@ struct ResRow {
 // S_p * max(0, p - q) = max(0, e_p - kappa * e_q) for one token, kappa =
 // S_p / S_q as a float pair; for the bonus row (no rejection) S_p * p = e_p.
 __device__ __forceinline__ float residual_term(float zp, float zq, const ResRow& R) {
-  const float ep = pow2_rel(expo(zp, R.c), R.k_p);
+  const float ep = pow2_rel(zp, R.c, R.k_p);
   if (!R.rej) return ep;
-  const float eq = pow2_rel(expo(zq, R.c), R.k_q);
+  const float eq = pow2_rel(zq, R.c, R.k_q);
   return fmaxf(0.f, ep - fmaf(R.kh, eq, R.kl * eq));
 }
 
@@ -457,6 +371,7 @@ __global__ void __launch_bounds__(kThreads) residual_kernel(const VerifyArgs a) 
   __shared__ int s_chunk;
   const int b = blockIdx.x, chunk = blockIdx.y;
   const int lane = threadIdx.x & 31;
+  griddep_wait();
   if (threadIdx.x == 0) {
     const SeqState* g = &a.seq[b];
     st.n = __ldcg(&g->n);
@@ -489,7 +404,7 @@ __global__ void __launch_bounds__(kThreads) residual_kernel(const VerifyArgs a) 
     block_excl_scan_ff({segment_total(r), 0.f}, excl, total, sm_ff);
     if (threadIdx.x == 0) a.res_sums[static_cast<size_t>(b) * a.CB + chunk] = make_float2(total.hi, total.lo);
   }
-  if (!last_block_ticket(&a.tickets_b[b], static_cast<unsigned>(a.CB), sm_i)) return;
+  if (!last_block_ticket(&a.tickets[b], static_cast<unsigned>(a.CB), sm_i)) return;
 
   const float2* sums = a.res_sums + static_cast<size_t>(b) * a.CB;
   const float u = a.u[b * (K + 1) + K];
@@ -595,6 +510,7 @@ __global__ void __launch_bounds__(kThreads) greedy_finish_kernel(const GreedyArg
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.x;
   const int K = a.K;
+  griddep_wait();
   for (int j = 0; j <= K; ++j) {
     const size_t row = static_cast<size_t>(b) * (K + 1) + j;
     const float* pv = a.part_max + row * a.P;
@@ -680,12 +596,13 @@ __global__ void __launch_bounds__(kThreads) greedy_finish_kernel(const GreedyArg
 // Per (row, chunk) max and lowest argmax of given logits: [M][P] partials.
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) row_argmax_kernel(const float* __restrict__ logits, int M, int V, int P,
-                                                             float* part_max, int* part_idx) {
+                                                             float* part_max, int* part_idx, int* err) {
   __shared__ float sv[kWarps];
   __shared__ int si[kWarps];
   __shared__ int sb[kWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int row = blockIdx.x, chunk = blockIdx.y;
+  if (row == 0 && chunk == 0 && threadIdx.x == 0) *err = 0;
   const int e0 = chunk * kChunk + threadIdx.x * kPer;
   float z[kPer];
   unsigned valid;
@@ -743,38 +660,41 @@ void exponent_constant(float temperature, float* c_hi, float* c_lo) {
   *c_lo = static_cast<float>(c - static_cast<double>(*c_hi));
 }
 
-cudaError_t launch_verify_sampling(const VerifyArgs& a, cudaStream_t stream) {
-  const int M = a.B * (a.K + 1);
-  const int R = M + a.B * a.K;
-  const bool vec = (a.V % 4) == 0;
-  const dim3 g1(R, a.CA);
-  if (vec)
-    stats_kernel<true><<<g1, kThreads, 0, stream>>>(a);
+cudaError_t launch_row_stats(const float* zp, const float* zq, int M, int draft_rows, int V, float c_hi, float c_lo,
+                             StatPart* tpart, StatPart* dpart, int* err, cudaStream_t stream) {
+  const int P = (V + kChunk - 1) / kChunk;
+  const dim3 g(M + draft_rows, P);
+  const Expo c{c_hi, c_lo};
+  if (V % 4 == 0)
+    row_stats_kernel<true><<<g, kThreads, 0, stream>>>(zp, zq, M, V, c, tpart, dpart, P, err);
   else
-    stats_kernel<false><<<g1, kThreads, 0, stream>>>(a);
-  cudaError_t e = cudaGetLastError();
+    row_stats_kernel<false><<<g, kThreads, 0, stream>>>(zp, zq, M, V, c, tpart, dpart, P, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_verify_sampling(const VerifyArgs& a, cudaStream_t stream) {
+  cudaError_t e = launch_dependent(decide_kernel, dim3(a.B), dim3(kThreads), stream, a);
   if (e != cudaSuccess) return e;
   const dim3 g2(a.B, a.CB);
-  if (vec)
-    residual_kernel<true><<<g2, kThreads, 0, stream>>>(a);
+  if (a.V % 4 == 0)
+    e = launch_dependent(residual_kernel<true>, g2, dim3(kThreads), stream, a);
   else
-    residual_kernel<false><<<g2, kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+    e = launch_dependent(residual_kernel<false>, g2, dim3(kThreads), stream, a);
+  return e;
 }
 
 cudaError_t launch_greedy_finish(const GreedyArgs& a, cudaStream_t stream) {
-  greedy_finish_kernel<<<a.B, kThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(greedy_finish_kernel, dim3(a.B), dim3(kThreads), stream, a);
 }
 
-cudaError_t launch_row_argmax(const float* logits, int M, int V, float* part_max, int* part_idx,
+cudaError_t launch_row_argmax(const float* logits, int M, int V, float* part_max, int* part_idx, int* err,
                               cudaStream_t stream) {
   const int P = (V + kChunk - 1) / kChunk;
   const dim3 g(M, P);
   if (V % 4 == 0)
-    row_argmax_kernel<true><<<g, kThreads, 0, stream>>>(logits, M, V, P, part_max, part_idx);
+    row_argmax_kernel<true><<<g, kThreads, 0, stream>>>(logits, M, V, P, part_max, part_idx, err);
   else
-    row_argmax_kernel<false><<<g, kThreads, 0, stream>>>(logits, M, V, P, part_max, part_idx);
+    row_argmax_kernel<false><<<g, kThreads, 0, stream>>>(logits, M, V, P, part_max, part_idx, err);
   return cudaGetLastError();
 }
 
