@@ -150,6 +150,21 @@ SPEC_API spec_status spec_verify(const void *hidden, const void *W_lm, const flo
                         float *out_debug, spec_stream_t stream);
 
 /*
+ * spec_verify with per-stage timing: identical arguments and work, plus
+ * `stage_events`, an array of 3 cudaEvent_t handles (created by the caller)
+ * recorded on `stream` before the LM-head kernel, between the LM head (with
+ * its fused softmax statistics, or the head and the statistics pass for
+ * large batches) and the finishing kernel, and after it.  The events sit
+ * between the launches, so the finishing kernel no longer overlaps the
+ * head's tail; use it to attribute time, not to measure the step.
+ */
+SPEC_API spec_status spec_verify_timed(const void *hidden, const void *W_lm, const float *draft_logits,
+                                       const int32_t *draft_tokens, const float *uniforms, float temperature,
+                                       int32_t *out_tokens, int32_t *out_num_accepted, spec_dims dims,
+                                       void *workspace, size_t workspace_bytes, float *out_target_logits,
+                                       float *out_debug, spec_stream_t stream, void *const *stage_events);
+
+/*
  * The verify-and-accept part alone, on given target logits
  * (device f32 [B*(K+1)][V]); same arguments and rules as spec_verify
  * otherwise.  dims.d is ignored.  Workspace: spec_verify_workspace_bytes(dims, T, 0).

@@ -50,6 +50,8 @@ _SIGS = {
     "spec_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "spec_verify_workspace_bytes": (_SZ, [SpecDims, _F32, _I32]),
     "spec_verify": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _SZ, _VP, _VP, _VP]),
+    "spec_verify_timed": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _SZ, _VP, _VP, _VP,
+                                         ctypes.POINTER(_VP)]),
     "spec_verify_from_logits": (ctypes.c_int, [_VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _SZ, _VP, _VP]),
     "spec_lm_head": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, _VP]),
     "spec_verify_host_workspace_bytes": (_SZ, [SpecDims, _F32]),
@@ -133,7 +135,7 @@ def _outputs(B, K, device, out_tokens, out_num_accepted):
 
 def spec_verify(hidden, W_lm, draft_logits, draft_tokens, uniforms, temperature: float, *,
                 out_tokens=None, out_num_accepted=None, workspace=None, out_target_logits=None,
-                out_debug=None, stream=None):
+                out_debug=None, stream=None, stage_events=None):
     """LM head + verify-and-accept.  hidden bf16 [B*(K+1), d], W_lm bf16 [V, d],
     draft_logits f32 [B*K, V] (None when temperature == 0), draft_tokens int32
     [B, K], uniforms f32 [B, K+1] (None when temperature == 0).
@@ -155,10 +157,16 @@ def spec_verify(hidden, W_lm, draft_logits, draft_tokens, uniforms, temperature:
     need = library().spec_verify_workspace_bytes(SpecDims(B, K, d, V), T, int(out_target_logits is None))
     if workspace is None:
         workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=hidden.device)
-    _check(library().spec_verify(
-        _ptr(hidden), _ptr(W_lm), _ptr(draft_logits if T > 0 else None), _ptr(draft_tokens if K > 0 else None),
-        _ptr(uniforms if T > 0 else None), T, _ptr(out_tokens), _ptr(out_num_accepted), SpecDims(B, K, d, V),
-        _ptr(workspace), workspace.numel(), _ptr(out_target_logits), _ptr(out_debug), _stream(stream)))
+    args = (_ptr(hidden), _ptr(W_lm), _ptr(draft_logits if T > 0 else None), _ptr(draft_tokens if K > 0 else None),
+            _ptr(uniforms if T > 0 else None), T, _ptr(out_tokens), _ptr(out_num_accepted), SpecDims(B, K, d, V),
+            _ptr(workspace), workspace.numel(), _ptr(out_target_logits), _ptr(out_debug), _stream(stream))
+    if stage_events is None:
+        _check(library().spec_verify(*args))
+    else:
+        # three torch.cuda.Event(enable_timing=True): before the LM head,
+        # between the head and the finishing kernel, after it
+        handles = (_VP * 3)(*[ctypes.c_void_p(ev.cuda_event) for ev in stage_events])
+        _check(library().spec_verify_timed(*args, handles))
     return out_tokens, out_num_accepted
 
 
@@ -253,8 +261,9 @@ class Verifier:
         self.out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=device)
         self.out_num_accepted = torch.empty((B,), dtype=torch.int32, device=device)
 
-    def __call__(self, hidden, W_lm, draft_logits, draft_tokens, uniforms, out_debug=None, stream=None):
+    def __call__(self, hidden, W_lm, draft_logits, draft_tokens, uniforms, out_debug=None, stream=None,
+                 stage_events=None):
         return spec_verify(hidden, W_lm, draft_logits, draft_tokens, uniforms, self.T,
                            out_tokens=self.out_tokens, out_num_accepted=self.out_num_accepted,
                            workspace=self.workspace, out_target_logits=self.target_logits,
-                           out_debug=out_debug, stream=stream)
+                           out_debug=out_debug, stream=stream, stage_events=stage_events)

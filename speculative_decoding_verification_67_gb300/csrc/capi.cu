@@ -21,11 +21,11 @@ size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Workspace layout.  Nothing needs initialising by the caller: the first
-// kernel of a call clears the error word and the decision kernel clears the
-// tickets before the residual pass counts on them.
+// kernel of a call clears the error word, and the kernel producing the
+// softmax statistics clears the tickets the finishing kernel counts on.
 struct Layout {
   size_t ctrl_bytes = 0;
-  size_t seq = 0, tpart = 0, dpart = 0, res = 0, logits = 0;  // sampling
+  size_t tpart = 0, dpart = 0, res = 0, logits = 0;  // sampling
   size_t pmax = 0, pidx = 0;                                   // greedy
   int CA = 0, P = 0;
   size_t total = 0;
@@ -42,8 +42,6 @@ Layout make_layout(int B, int K, int V, bool greedy, bool logits_in_ws, bool fro
   L.ctrl_bytes = off;
   L.CA = (V + sv::kChunk - 1) / sv::kChunk;
   if (!greedy) {
-    L.seq = off;
-    off += round_up(sizeof(sv::SeqState) * B);
     L.tpart = off;  // per-tile partials are the most the LM head ever writes
     off += round_up(sizeof(sv::StatPart) * M * (from_logits ? static_cast<size_t>(L.CA) : num_vt));
     L.dpart = off;
@@ -139,7 +137,6 @@ sv::VerifyArgs sampling_args(const Layout& L, const spec_dims& d, float T, const
   a.dpart = reinterpret_cast<const sv::StatPart*>(ws + L.dpart);
   a.Pt = Pt;
   a.Pd = L.CA;
-  a.seq = reinterpret_cast<sv::SeqState*>(ws + L.seq);
   a.res_sums = reinterpret_cast<float2*>(ws + L.res);
   a.CB = L.CA;
   return a;
@@ -187,11 +184,15 @@ size_t spec_verify_workspace_bytes(spec_dims dims, float temperature, int32_t lo
   return make_layout(dims.B, dims.K, dims.V, temperature == 0.f, logits_in_workspace != 0, false).total;
 }
 
-spec_status spec_verify(const void* hidden, const void* W_lm, const float* draft_logits,
+}  // extern "C"
+
+namespace {
+
+spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft_logits,
                         const int32_t* draft_tokens, const float* uniforms, float temperature,
                         int32_t* out_tokens, int32_t* out_num_accepted, spec_dims dims, void* workspace,
                         size_t workspace_bytes, float* out_target_logits, float* out_debug,
-                        spec_stream_t stream) {
+                        spec_stream_t stream, void* const* ev) {
   if (!dims_ok(dims, true)) return SPEC_ERR_DIMS;
   if (!hidden || !W_lm) return SPEC_ERR_ARG;
   if (!aligned(hidden, 16) || !aligned(W_lm, 16)) return SPEC_ERR_ALIGN;
@@ -214,14 +215,18 @@ spec_status spec_verify(const void* hidden, const void* W_lm, const float* draft
   int* err = reinterpret_cast<int*>(ws) + kCtrlErr;
   bool enc_fail = false;
   cudaError_t e;
+  auto mark = [&](int i) -> bool {
+    return !ev || cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev[i]), s) == cudaSuccess;
+  };
+  if (!mark(0)) return SPEC_ERR_CUDA;
   if (greedy) {
     e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kArgmax, nullptr,
                         reinterpret_cast<float*>(ws + L.pmax), reinterpret_cast<int*>(ws + L.pidx), nullptr, err,
                         true, dev, s, &enc_fail);
-    if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
+    if (enc_fail || e != cudaSuccess || !mark(1)) return SPEC_ERR_CUDA;
     const sv::GreedyArgs g = greedy_args(L, dims, draft_tokens, out_tokens, out_num_accepted, out_debug, ws);
     e = sv::launch_greedy_finish(g, s);
-    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+    return (e == cudaSuccess && mark(2)) ? SPEC_OK : SPEC_ERR_CUDA;
   }
   float* logits = out_target_logits ? out_target_logits : reinterpret_cast<float*>(ws + L.logits);
   const sv::HeadPlan plan = sv::plan_head(M, dims.d, dims.V, sv::HeadOut::kStats, dev);
@@ -231,6 +236,8 @@ spec_status spec_verify(const void* hidden, const void* W_lm, const float* draft
   hs.zq = draft_logits;
   hs.draft_rows = dims.B * dims.K;
   hs.dpart = reinterpret_cast<sv::StatPart*>(ws + L.dpart);
+  hs.tickets = reinterpret_cast<unsigned*>(reinterpret_cast<int*>(ws) + kCtrlTickets);
+  hs.n_tickets = dims.B;
   int Pt;
   if (plan.precise) {
     // small batch: the LM head's epilogue and side warps produce the statistics
@@ -244,14 +251,40 @@ spec_status spec_verify(const void* hidden, const void* W_lm, const float* draft
                         err, true, dev, s, &enc_fail);
     if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
     e = sv::launch_row_stats(logits, draft_logits, M, dims.B * dims.K, dims.V, hs.c_hi, hs.c_lo, hs.tpart, hs.dpart,
-                             err, s);
+                             nullptr, hs.tickets, hs.n_tickets, s);
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
     Pt = L.CA;
   }
+  if (!mark(1)) return SPEC_ERR_CUDA;
   const sv::VerifyArgs a = sampling_args(L, dims, temperature, logits, draft_logits, draft_tokens, uniforms,
                                          out_tokens, out_num_accepted, out_debug, ws, Pt);
   e = sv::launch_verify_sampling(a, s);
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  return (e == cudaSuccess && mark(2)) ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+spec_status spec_verify(const void* hidden, const void* W_lm, const float* draft_logits,
+                        const int32_t* draft_tokens, const float* uniforms, float temperature,
+                        int32_t* out_tokens, int32_t* out_num_accepted, spec_dims dims, void* workspace,
+                        size_t workspace_bytes, float* out_target_logits, float* out_debug,
+                        spec_stream_t stream) {
+  return verify_impl(hidden, W_lm, draft_logits, draft_tokens, uniforms, temperature, out_tokens,
+                     out_num_accepted, dims, workspace, workspace_bytes, out_target_logits, out_debug, stream,
+                     nullptr);
+}
+
+spec_status spec_verify_timed(const void* hidden, const void* W_lm, const float* draft_logits,
+                              const int32_t* draft_tokens, const float* uniforms, float temperature,
+                              int32_t* out_tokens, int32_t* out_num_accepted, spec_dims dims, void* workspace,
+                              size_t workspace_bytes, float* out_target_logits, float* out_debug,
+                              spec_stream_t stream, void* const* stage_events) {
+  if (!stage_events || !stage_events[0] || !stage_events[1] || !stage_events[2]) return SPEC_ERR_ARG;
+  return verify_impl(hidden, W_lm, draft_logits, draft_tokens, uniforms, temperature, out_tokens,
+                     out_num_accepted, dims, workspace, workspace_bytes, out_target_logits, out_debug, stream,
+                     stage_events);
 }
 
 spec_status spec_verify_from_logits(const float* target_logits, const float* draft_logits,
@@ -289,7 +322,7 @@ spec_status spec_verify_from_logits(const float* target_logits, const float* dra
   sv::exponent_constant(temperature, &c_hi, &c_lo);
   e = sv::launch_row_stats(target_logits, draft_logits, M, dims.B * dims.K, dims.V, c_hi, c_lo,
                            reinterpret_cast<sv::StatPart*>(ws + L.tpart), reinterpret_cast<sv::StatPart*>(ws + L.dpart),
-                           err, s);
+                           err, reinterpret_cast<unsigned*>(reinterpret_cast<int*>(ws) + kCtrlTickets), dims.B, s);
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   const sv::VerifyArgs a = sampling_args(L, dims, temperature, target_logits, draft_logits, draft_tokens, uniforms,
                                          out_tokens, out_num_accepted, out_debug, ws, L.CA);

@@ -73,6 +73,8 @@ struct HeadStats {
   const float* zq = nullptr;      // draft logits [draft_rows][V]
   int draft_rows = 0;
   StatPart* dpart = nullptr;      // [draft_rows][ceil(V / kChunk)]
+  unsigned* tickets = nullptr;    // [n_tickets] zeroed by the kernel
+  int n_tickets = 0;
 };
 
 // Enqueues the LM head.  Returns cudaSuccess or the first CUDA error;
@@ -83,17 +85,6 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
                         bool zero_err, const DeviceInfo& dev, cudaStream_t stream, bool* encode_failed);
 
 // ------------------------------------------------------------------ verify
-// Per-sequence state handed from the decision to the residual pass.
-struct SeqState {
-  int n;          // accepted drafts
-  int bad;        // invalid input: skip
-  float k_p;      // reference exponent of target row n
-  float k_q;      // reference exponent of draft row n (n < K)
-  float2 S_p;     // normaliser of target row n against k_p (float pair)
-  float2 S_q;     // same for the draft row (n < K)
-  float2 kappa;   // S_p / S_q (float pair)
-};
-
 struct VerifyArgs {
   int B, K, V;
   float c_hi, c_lo;         // log2(e) / T as a float pair
@@ -106,11 +97,10 @@ struct VerifyArgs {
   float* out_debug;         // [B][K+1][6] or null
   // workspace
   int* err;
-  unsigned* tickets;        // [B] (zeroed by the decision kernel)
+  unsigned* tickets;        // [B] (zeroed by the kernel producing the statistics)
   const StatPart* tpart;    // [B*(K+1)][Pt]
   const StatPart* dpart;    // [B*K][Pd]
   int Pt, Pd;
-  SeqState* seq;            // [B]
   float2* res_sums;         // [B][CB]
   int CB;
 };
@@ -119,12 +109,13 @@ struct VerifyArgs {
 void exponent_constant(float temperature, float* c_hi, float* c_lo);
 
 // Softmax partials of given target and draft logits (per row and 4096-token
-// chunk) for the from-logits entry point; clears *err first.
+// chunk); clears *err first when err is given, and the n_tickets tickets.
 cudaError_t launch_row_stats(const float* zp, const float* zq, int M, int draft_rows, int V, float c_hi, float c_lo,
-                             StatPart* tpart, StatPart* dpart, int* err, cudaStream_t stream);
+                             StatPart* tpart, StatPart* dpart, int* err, unsigned* tickets, int n_tickets,
+                             cudaStream_t stream);
 
-// Decision then residual draw (two launches, chained with programmatic
-// dependent launch).
+// Decision and residual draw (one launch, chained with programmatic
+// dependent launch after the statistics).
 cudaError_t launch_verify_sampling(const VerifyArgs& a, cudaStream_t stream);
 
 struct GreedyArgs {

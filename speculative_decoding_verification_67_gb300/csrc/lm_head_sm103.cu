@@ -28,11 +28,11 @@
 //  * two accumulation schemes.  Standard (any N): one TMEM accumulator per
 //    tile over the whole hidden size, double-buffered so the epilogue of a
 //    tile overlaps the next tile's MMAs.  Precise (N <= 64, the small-batch
-//    regime): every 64-wide hidden block is accumulated into a fresh TMEM
-//    slot (4 slots rotate) and the epilogue adds the block results in f32
-//    registers with round-to-nearest, so the tensor core's own accumulation
-//    only ever spans 64 products; this cuts the logits' error against exact
-//    arithmetic several-fold at no cost to the weight stream;
+//    regime): every four 64-wide hidden blocks are accumulated into a fresh
+//    TMEM slot (4 slots rotate) and the epilogue adds the slot results in
+//    f32 registers with round-to-nearest, so the tensor core's own
+//    accumulation only ever spans 256 products; this cuts the logits' error
+//    against exact arithmetic several-fold at no cost to the weight stream;
 //  * every wait is bounded; a timeout sets the error word, drains the copies
 //    in flight and frees TMEM before returning.
 #include <cudaTypedefs.h>
@@ -52,6 +52,7 @@ constexpr uint32_t kABytes = kHeadTileV * kHeadTileK * 2;  // 16 KB W tile per s
 constexpr uint32_t kBarrierBytes = 512;
 constexpr uint32_t kReduceBytes = 4 * 4 * 256 * 4;         // per-column scratch of the 4 epilogue warps
 constexpr int kSlotsPrecise = 4;
+constexpr int kGroupPrecise = 4;  // hidden blocks accumulated per TMEM slot (precise scheme)
 
 constexpr int kModeLogits = static_cast<int>(HeadOut::kLogits);
 constexpr int kModeArgmax = static_cast<int>(HeadOut::kArgmax);
@@ -75,6 +76,8 @@ struct HeadParams {
   int draft_rows;
   StatPart* dpart;
   int dparts;          // partials per draft row = ceil(V / kChunk)
+  unsigned* tickets;   // zeroed here for the kernel that follows
+  int n_tickets;
 };
 
 // Timeouts of calls without a workspace (the bare LM head) latch here.
@@ -312,7 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  if (p.zero_err && blockIdx.x == 0 && threadIdx.x == 0) *p.err = 0;
+  if (blockIdx.x == 0) {
+    if (p.zero_err && threadIdx.x == 0) *p.err = 0;
+    for (int i = threadIdx.x; i < p.n_tickets; i += kThreads) p.tickets[i] = 0u;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -408,7 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          if (kPrecise) {
+          const bool group_first = !kPrecise || (kb % kGroupPrecise) == 0;
+          const bool group_last = kPrecise && ((kb + 1) % kGroupPrecise == 0 || kb + 1 == p.num_kb);
+          if (kPrecise && group_first) {
             if (!mbar_wait(&afree[slot], sph ^ 1u)) {
               report_timeout(p.err);
               ok = false;
@@ -421,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
           for (int k = 0; k < kHeadTileK / 16; ++k) {
-            const bool acc = kPrecise ? (k != 0) : ((kb | k) != 0);
+            const bool acc = kPrecise ? !(group_first && k == 0) : ((kb | k) != 0);
             mma_bf16_ss(d_tmem, smem_desc_k_sw128(a_addr + k * 32), smem_desc_k_sw128(b_addr + k * 32), idesc,
                         acc ? 1u : 0u);
           }
@@ -430,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             s = 0;
             ph ^= 1u;
           }
-          if (kPrecise) {
+          if (group_last) {
             mma_commit(&afull[slot]);
             if (++slot == kSlots) {
               slot = 0;
@@ -485,7 +493,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float acc[kPrecN];
 #pragma unroll
         for (int i = 0; i < kPrecN; ++i) acc[i] = 0.f;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int groups = (p.num_kb + kGroupPrecise - 1) / kGroupPrecise;
+        for (int g = 0; g < groups; ++g) {
           if (!mbar_wait(&afull[slot], sph)) {
             report_timeout(p.err);
             ok = false;
@@ -530,10 +539,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 badmask |= 1ull << i;
                 continue;
               }
-              const float kn = fmaxf(rk[i], ceilf(h));
-              rs[i] = ldexpf(rs[i], static_cast<int>(fmaxf(rk[i] - kn, -200.f)));
-              rk[i] = kn;
-              rs[i] += exp2f((h - kn) + expo_lo(z, h, c));
+              const float kn = ceilf(h);
+              if (kn > rk[i]) {  // the reference rises (rarely after the first tile)
+                rs[i] *= pow2_int(rk[i] - kn);
+                rk[i] = kn;
+              }
+              rs[i] += exp2f((h - rk[i]) + expo_lo(z, h, c));
             }
           }
         } else {
@@ -583,10 +594,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Merge the 128 threads' running partials per column through shared
       // memory (the pipeline stages are idle now: every load has been
       // consumed), several threads per column, then one partial per CTA.
-      float2* tr = reinterpret_cast<float2*>(smem);            // [kPrecN][128]
-      uint64_t* bm = reinterpret_cast<uint64_t*>(tr + kPrecN * 128);
+      // [thread][column] with an odd pitch: thread et's writes and the
+      // column readers' loads both land in distinct banks
+      constexpr int kPitch = kPrecN + 1;
+      float* trk = reinterpret_cast<float*>(smem);             // references
+      float* trs = trk + 128 * kPitch;                         // sums
+      uint64_t* bm = reinterpret_cast<uint64_t*>(trs + 128 * kPitch + 2);
 #pragma unroll
-      for (int i = 0; i < kPrecN; ++i) tr[i * 128 + et] = make_float2(rk[i], rs[i]);
+      for (int i = 0; i < kPrecN; ++i) {
+        trk[et * kPitch + i] = rk[i];
+        trs[et * kPitch + i] = rs[i];
+      }
       bm[et] = badmask;
       __syncwarp();
       if (lane == 0) mbar_arrive(red_full);
@@ -594,25 +612,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         report_timeout(p.err);
       } else {
         constexpr int kTpc = kPrecN == 32 ? 4 : 2;             // threads per column
-        constexpr int kSpan = 128 / kTpc;                      // partials each merges
+        constexpr int kSpan = 128 / kTpc;                      // partials each thread reads
         const int col = et / kTpc, part = et % kTpc;
-        Partial acc = partial_empty();
-        for (int t = part * kSpan; col < kPrecN && t < (part + 1) * kSpan; ++t) {
-          const float2 w = tr[col * 128 + t];
-          Partial pt;
-          pt.k = w.x;
-          pt.s = {w.y, 0.f};
-          pt.bad = static_cast<int>((bm[t] >> col) & 1ull);
-          acc = partial_merge(acc, pt);
+        const bool active = col < kPrecN;
+        const int ccol = active ? col : 0;
+        const int t0 = part * kSpan;
+        // pass 1: the column's reference = the largest of the 128 references
+        float kmax = -INFINITY;
+        int bad = 0;
+#pragma unroll 8
+        for (int t = 0; t < kSpan; ++t) {
+          kmax = fmaxf(kmax, trk[(t0 + t) * kPitch + ccol]);
+          bad |= static_cast<int>((bm[t0 + t] >> ccol) & 1ull);
         }
 #pragma unroll
         for (int off = 1; off < kTpc; off <<= 1) {
-          Partial o;
-          o.k = __shfl_xor_sync(0xffffffffu, acc.k, off);
-          o.s = shfl_xor_ff(acc.s, off);
-          o.bad = __shfl_xor_sync(0xffffffffu, acc.bad, off);
-          acc = partial_merge(acc, o);
+          kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
+          bad |= __shfl_xor_sync(0xffffffffu, bad, off);
         }
+        // pass 2: exact power-of-two scaling to that reference, compensated
+        // sum in four independent chains
+        float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+        if (kmax != -INFINITY) {
+#pragma unroll 4
+          for (int t = 0; t < kSpan; ++t) {
+            const int idx = (t0 + t) * kPitch + ccol;
+            ff_accumulate(sh[t & 3], sl[t & 3], trs[idx] * pow2_int(trk[idx] - kmax));
+          }
+        }
+        ff sum = ff_norm(sh[0], sl[0]);
+#pragma unroll
+        for (int i = 1; i < 4; ++i) sum = ff_add(sum, ff_norm(sh[i], sl[i]));
+#pragma unroll
+        for (int off = 1; off < kTpc; off <<= 1) sum = ff_add(sum, shfl_xor_ff(sum, off));
+        Partial acc;
+        acc.k = kmax;
+        acc.s = sum;
+        acc.bad = bad;
         if (part == 0 && col < kPrecN && col < p.M)
           store_part(&p.tpart[static_cast<size_t>(col) * p.tparts + blockIdx.x], acc);
       }
@@ -765,6 +801,8 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
     p.draft_rows = stats->draft_rows;
     p.dpart = stats->dpart;
     p.dparts = (V + kChunk - 1) / kChunk;
+    p.tickets = stats->tickets;
+    p.n_tickets = stats->n_tickets;
   }
   if (!h.precise) return launch_mode<0>(mode, map_w, map_h, p, h, dev, stream);
   if (h.N == 32) return launch_mode<32>(mode, map_w, map_h, p, h, dev, stream);

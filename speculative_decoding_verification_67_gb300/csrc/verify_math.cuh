@@ -55,6 +55,12 @@ __device__ __forceinline__ void ff_accumulate(float& hi, float& lo, float b) {
 // a > b for normalised pairs.
 __device__ __forceinline__ bool ff_gt(ff a, ff b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
 
+// 2^e for an integer-valued float e <= 0 (exact; 0 below the normal range,
+// and for e = -inf).
+__device__ __forceinline__ float pow2_int(float e) {
+  return e >= -126.f ? __int_as_float((static_cast<int>(e) + 127) << 23) : 0.f;
+}
+
 // a * 2^e, exact (barring underflow).
 __device__ __forceinline__ ff ff_scale2(ff a, int e) { return {ldexpf(a.hi, e), ldexpf(a.lo, e)}; }
 

@@ -2,22 +2,22 @@
 //
 // Sampling path (T > 0).  The softmax(z/T) normaliser partials of every
 // target row and draft row come from the LM-head kernel (its epilogue and
-// two side warps) or, on given logits, from row_stats_kernel.  Then two
-// launches chained with programmatic dependent launch:
+// two side warps) or, on given logits, from row_stats_kernel.  Then one
+// launch, chained with programmatic dependent launch: finish_kernel, grid
+// (sequences) x (chunks of 4096 tokens).  Every CTA of a sequence
 //
-//  1. decide_kernel, one CTA per sequence: merges the partials of the
-//     sequence's 2K+1 rows into their normalisers (page "quochung.cyou"
-//     A.I article, section "Forward pass": the scores form a distribution
-//     summing to 100%), gathers p_j(x_j) and q_j(x_j), runs the accept test
-//     u_j < min(1, p_j(x_j) / q_j(x_j)) (section "Modified rejection
-//     sampling / Giải pháp"), takes the accepted prefix with one warp ballot
-//     (section "Áp dụng thuật toán": left to right, stop at the first
-//     rejection) and writes the accepted tokens.
-//  2. residual_kernel, grid (sequences) x (chunks of 4096 tokens): the row
-//     pair at the first rejection n_b is read once more and reduced to the
-//     mass of max(0, p - q) per chunk (section "Khi reject thì lấy token từ
-//     đâu?"), or of p_K for the bonus token when n_b = K.  The last CTA of
-//     the sequence (atomic ticket; no CTA ever waits for another) finds the
+//  1. merges the partials of the sequence's 2K+1 rows into their
+//     normalisers (page "quochung.cyou" A.I article, section "Forward pass":
+//     the scores form a distribution summing to 100%), gathers p_j(x_j) and
+//     q_j(x_j), runs the accept test u_j < min(1, p_j(x_j) / q_j(x_j))
+//     (section "Modified rejection sampling / Giải pháp") and takes the
+//     accepted prefix with one warp ballot (section "Áp dụng thuật toán":
+//     left to right, stop at the first rejection) -- the same arithmetic in
+//     every CTA, so the same decision, with no exchange between CTAs;
+//  2. reduces its chunk of the row pair at the first rejection n_b to the
+//     mass of max(0, p - q) (section "Khi reject thì lấy token từ đâu?"), or
+//     of p_K for the bonus token when n_b = K.  The last CTA of the
+//     sequence (atomic ticket; no CTA ever waits for another) finds the
 //     chunk holding u*S and rescans it with a block-wide prefix scan for the
 //     smallest token whose cumulative mass exceeds u*S (inverse CDF,
 //     ascending token id).
@@ -131,11 +131,15 @@ __device__ __forceinline__ void load16(const float* __restrict__ row, int e0, in
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) row_stats_kernel(const float* __restrict__ zp,
                                                              const float* __restrict__ zq, int M, int V, Expo c,
-                                                             StatPart* tpart, StatPart* dpart, int P, int* err) {
+                                                             StatPart* tpart, StatPart* dpart, int P, int* err,
+                                                             unsigned* tickets, int n_tickets) {
   __shared__ Partial sm[kWarps];
   const int row = blockIdx.x, chunk = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (row == 0 && chunk == 0 && threadIdx.x == 0) *err = 0;
+  if (row == 0 && chunk == 0) {
+    if (err && threadIdx.x == 0) *err = 0;
+    for (int i = threadIdx.x; i < n_tickets; i += kThreads) tickets[i] = 0u;
+  }
   const bool target = row < M;
   const float* z = target ? zp + static_cast<size_t>(row) * V : zq + static_cast<size_t>(row - M) * V;
   float v[kPer];
@@ -181,110 +185,189 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(const float* __rest
 }
 
 // ---------------------------------------------------------------- decision
-// One CTA per sequence: merge the partials of its 2K+1 rows, run the accept
-// tests, take the accepted prefix, write the accepted tokens and hand the
-// row pair at the first rejection (or the bonus row) to the residual pass.
-__global__ void __launch_bounds__(kThreads) decide_kernel(const VerifyArgs a) {
-  __shared__ float rk[2 * kMaxK + 1];
-  __shared__ ff rS[2 * kMaxK + 1];
-  __shared__ int rbad[2 * kMaxK + 1];
-  griddep_wait();
+// The decision of one sequence, computed by every CTA of that sequence with
+// identical arithmetic (so identically): merge the softmax partials of its
+// 2K+1 rows, run the accept tests left to right, take the accepted prefix.
+struct Decision {
+  int n, bad, badtok, rowbad;
+  float k_p, k_q;
+  ff S_p, S_q, kappa;
+};
+
+struct DecideSmem {
+  float rk[2 * kMaxK + 1];
+  ff rS[2 * kMaxK + 1];
+  int rbad[2 * kMaxK + 1];
+  int xj[kMaxK];
+  float zqx[kMaxK];
+  float zpx[kMaxK];
+  float uj[kMaxK + 1];
+  float pj[kMaxK], qj[kMaxK], aj[kMaxK];
+  Decision d;
+};
+
+// Loads the sequence's inputs that no preceding kernel writes (drafts,
+// uniforms, draft logits at the drafts); may run before griddep_wait.
+__device__ void load_inputs(const VerifyArgs& a, int b, DecideSmem& ds) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x >= 32) return;
+  const int K = a.K;
+  if (lane < K) {
+    const int x = a.x[b * K + lane];
+    const bool ok = x >= 0 && x < a.V;
+    ds.xj[lane] = x;
+    ds.zqx[lane] = ok ? a.zq[static_cast<size_t>(b * K + lane) * a.V + x] : 0.f;
+  }
+  for (int j = lane; j <= K; j += 32) ds.uj[j] = a.u[b * (K + 1) + j];
+}
+
+// Merge the partials of every row of sequence b (one warp per row, two
+// passes: the row's largest reference, then the exact-scaled compensated
+// sum), then warp 0 decides.  Ends with a __syncthreads.
+__device__ void decide(const VerifyArgs& a, int b, DecideSmem& ds) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int b = blockIdx.x;
   const int K = a.K;
   const int nrows = 2 * K + 1;
-  if (threadIdx.x == 0) a.tickets[b] = 0u;
-
+  // the target logit at each draft, issued now so its latency overlaps the merge
+  float zpx = 0.f;
+  if (warp == kWarps - 1 && lane < K) {
+    const int xj = ds.xj[lane];
+    if (xj >= 0 && xj < a.V) zpx = __ldcg(&a.zp[static_cast<size_t>(b * (K + 1) + lane) * a.V + xj]);
+  }
   for (int r = warp; r < nrows; r += kWarps) {
     const StatPart* pp = r <= K ? a.tpart + static_cast<size_t>(b * (K + 1) + r) * a.Pt
                                 : a.dpart + static_cast<size_t>(b * K + (r - K - 1)) * a.Pd;
     const int np = r <= K ? a.Pt : a.Pd;
-    Partial acc = partial_empty();
-    for (int i = lane; i < np; i += 32) {
-      const float4 w = __ldcg(reinterpret_cast<const float4*>(pp + i));
-      Partial pi;
-      pi.k = w.x;
-      pi.s = {w.y, w.z};
-      pi.bad = __float_as_int(w.w);
-      acc = partial_merge(acc, pi);
+    // batches of kBatch partials per lane, all loads issued before use; a
+    // row of up to 32*kBatch partials stays in registers for both passes
+    constexpr int kBatch = 8;
+    float4 w[kBatch];
+    float kmax = -INFINITY;
+    int bad = 0;
+    for (int i0 = 0; i0 < np; i0 += 32 * kBatch) {
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int i = i0 + j * 32 + lane;
+        w[j] = i < np ? __ldcg(reinterpret_cast<const float4*>(pp + i)) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (w[j].y != 0.f || w[j].z != 0.f) kmax = fmaxf(kmax, w[j].x);
+        bad |= __float_as_int(w[j].w);
+      }
     }
-    acc = warp_merge(acc);
+    kmax = warp_max_f(kmax);
+    bad = __any_sync(0xffffffffu, bad != 0) ? 1 : 0;
+    float sh = 0.f, sl = 0.f;
+    if (kmax != -INFINITY) {
+      for (int i0 = 0; i0 < np; i0 += 32 * kBatch) {
+        if (np > 32 * kBatch) {  // more than one batch: reload (L2-resident)
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) {
+            const int i = i0 + j * 32 + lane;
+            w[j] = i < np ? __ldcg(reinterpret_cast<const float4*>(pp + i)) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          if (w[j].y != 0.f || w[j].z != 0.f) {
+            const float sc = pow2_int(w[j].x - kmax);
+            ff_accumulate(sh, sl, w[j].y * sc);
+            ff_accumulate(sh, sl, w[j].z * sc);
+          }
+        }
+      }
+    }
+    const ff s = warp_sum_ff(ff_norm(sh, sl));
     if (lane == 0) {
-      rk[r] = acc.k;
-      rS[r] = acc.s;
-      rbad[r] = acc.bad || !(acc.s.hi > 0.f) || !isfinite(acc.s.hi) || !isfinite(acc.k);
+      ds.rk[r] = kmax;
+      ds.rS[r] = s;
+      ds.rbad[r] = bad || !(s.hi > 0.f) || !isfinite(s.hi) || !isfinite(kmax);
+    }
+  }
+  if (warp == kWarps - 1 && lane < K) ds.zpx[lane] = zpx;
+  __syncthreads();
+  if (warp == 0) {
+    const Expo c{a.c_hi, a.c_lo};
+    bool tok_ok = true, acc = false;
+    float pj = 0.f, qj = 0.f, aj = 0.f;
+    if (lane < K) {
+      const int xj = ds.xj[lane];
+      tok_ok = xj >= 0 && xj < a.V;
+      if (tok_ok) {
+        const float zp = ds.zpx[lane];
+        const float zq = ds.zqx[lane];
+        const float hp = expo_hi(zp, c), hq = expo_hi(zq, c);
+        const float lp = (hp - ds.rk[lane]) + expo_lo(zp, hp, c);          // log2 of S_p * p(x)
+        const float lq = (hq - ds.rk[K + 1 + lane]) + expo_lo(zq, hq, c);  // log2 of S_q * q(x)
+        const float Sp = ds.rS[lane].hi, Sq = ds.rS[K + 1 + lane].hi;
+        pj = exp2f(lp) / Sp;
+        qj = exp2f(lq) / Sq;
+        aj = fminf(1.f, exp2f(lp - lq) * (Sq / Sp));
+        acc = ds.uj[lane] < aj;
+      }
+      ds.pj[lane] = pj;
+      ds.qj[lane] = qj;
+      ds.aj[lane] = aj;
+    }
+    const unsigned acc_mask = __ballot_sync(0xffffffffu, acc);
+    const unsigned badtok = __ballot_sync(0xffffffffu, lane < K && !tok_ok);
+    int rowbad = 0;
+    for (int r = lane; r < nrows; r += 32) rowbad |= ds.rbad[r];
+    rowbad = __any_sync(0xffffffffu, rowbad != 0) ? 1 : 0;
+    int n = (acc_mask == 0xffffffffu) ? 32 : (__ffs(~acc_mask) - 1);
+    n = min(n, K);
+    if (lane == 0) {
+      Decision d;
+      d.n = n;
+      d.badtok = badtok != 0u;
+      d.rowbad = rowbad;
+      d.bad = d.badtok || d.rowbad;
+      d.k_p = ds.rk[n];
+      d.S_p = ds.rS[n];
+      if (n < K) {
+        d.k_q = ds.rk[K + 1 + n];
+        d.S_q = ds.rS[K + 1 + n];
+        d.kappa = ff_div(ds.rS[n], ds.rS[K + 1 + n]);
+      } else {
+        d.k_q = 0.f;
+        d.S_q = {0.f, 0.f};
+        d.kappa = {0.f, 0.f};
+      }
+      ds.d = d;
     }
   }
   __syncthreads();
+}
 
-  if (warp != 0) return;
-  const Expo c{a.c_hi, a.c_lo};
-  bool tok_ok = true, acc = false;
-  int xj = -1;
-  float pj = 0.f, qj = 0.f, aj = 0.f;
-  if (lane < K) {
-    xj = a.x[b * K + lane];
-    tok_ok = xj >= 0 && xj < a.V;
-    if (tok_ok) {
-      const float zp = a.zp[static_cast<size_t>(b * (K + 1) + lane) * a.V + xj];
-      const float zq = a.zq[static_cast<size_t>(b * K + lane) * a.V + xj];
-      const float hp = expo_hi(zp, c), hq = expo_hi(zq, c);
-      const float lp = (hp - rk[lane]) + expo_lo(zp, hp, c);          // log2 of S_p * p(x)
-      const float lq = (hq - rk[K + 1 + lane]) + expo_lo(zq, hq, c);  // log2 of S_q * q(x)
-      const float Sp = rS[lane].hi, Sq = rS[K + 1 + lane].hi;
-      pj = exp2f(lp) / Sp;
-      qj = exp2f(lq) / Sq;
-      aj = fminf(1.f, exp2f(lp - lq) * (Sq / Sp));
-      acc = a.u[b * (K + 1) + lane] < aj;
-    }
-  }
-  const unsigned acc_mask = __ballot_sync(0xffffffffu, acc);
-  const unsigned badtok = __ballot_sync(0xffffffffu, lane < K && !tok_ok);
-  int rowbad = 0;
-  for (int r = lane; r < nrows; r += 32) rowbad |= rbad[r];
-  rowbad = __any_sync(0xffffffffu, rowbad != 0) ? 1 : 0;
-  const bool bad = badtok != 0u || rowbad != 0;
-  int n = (acc_mask == 0xffffffffu) ? 32 : (__ffs(~acc_mask) - 1);
-  n = min(n, K);
-
-  // positions 0..K (K + 1 <= 33 may exceed the warp: a second pass covers j = 32)
+// The accepted prefix, the -1 padding, the accept count and the debug
+// fields 0-4 (written once per sequence).
+__device__ void write_prefix(const VerifyArgs& a, int b, const DecideSmem& ds) {
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x >= 32) return;
+  const int K = a.K;
+  const Decision& d = ds.d;
   for (int j = lane; j <= K; j += 32) {
-    const bool slot = j < K;  // j == lane whenever slot is true
-    a.out_tokens[b * (K + 1) + j] = (!bad && j < n) ? xj : -1;
+    const bool slot = j < K;
+    a.out_tokens[b * (K + 1) + j] = (!d.bad && j < d.n) ? ds.xj[j] : -1;
     if (a.out_debug) {
       float* dbg = a.out_debug + static_cast<size_t>(b * (K + 1) + j) * 6;
-      dbg[0] = slot ? pj : 0.f;
-      dbg[1] = slot ? qj : 0.f;
-      dbg[2] = slot ? aj : 0.f;
+      dbg[0] = slot ? ds.pj[j] : 0.f;
+      dbg[1] = slot ? ds.qj[j] : 0.f;
+      dbg[2] = slot ? ds.aj[j] : 0.f;
       // log sum_v exp(z_v / T) = ln 2 * (k + log2 S)
-      dbg[3] = 0.6931471805599453f * (rk[j] + log2f(rS[j].hi));
-      dbg[4] = slot ? 0.6931471805599453f * (rk[K + 1 + j] + log2f(rS[K + 1 + j].hi)) : 0.f;
+      dbg[3] = 0.6931471805599453f * (ds.rk[j] + log2f(ds.rS[j].hi));
+      dbg[4] = slot ? 0.6931471805599453f * (ds.rk[K + 1 + j] + log2f(ds.rS[K + 1 + j].hi)) : 0.f;
       dbg[5] = 0.f;
     }
   }
   if (lane == 0) {
-    a.out_n[b] = bad ? -1 : n;
-    if (bad) atomicOr(a.err, (badtok ? kErrTokenRange : 0) | (rowbad ? kErrNonFinite : 0));
-    SeqState st;
-    st.n = n;
-    st.bad = bad ? 1 : 0;
-    st.k_p = rk[n];
-    st.S_p = make_float2(rS[n].hi, rS[n].lo);
-    if (n < K) {
-      st.k_q = rk[K + 1 + n];
-      st.S_q = make_float2(rS[K + 1 + n].hi, rS[K + 1 + n].lo);
-      const ff kap = ff_div(rS[n], rS[K + 1 + n]);
-      st.kappa = make_float2(kap.hi, kap.lo);
-    } else {
-      st.k_q = 0.f;
-      st.S_q = make_float2(0.f, 0.f);
-      st.kappa = make_float2(0.f, 0.f);
-    }
-    a.seq[b] = st;
+    a.out_n[b] = d.bad ? -1 : d.n;
+    if (d.bad) atomicOr(a.err, (d.badtok ? kErrTokenRange : 0) | (d.rowbad ? kErrNonFinite : 0));
   }
 }
 
-// ---------------------------------------------------------------- pass 2
+// ---------------------------------------------------------------- residual
 struct ResRow {
   const float* zp;
   const float* zq;
@@ -362,64 +445,72 @@ __device__ void locate_in_chunk(const ResRow& R, int chunk, ff base, ff t, int& 
   __syncthreads();
 }
 
+// grid (sequences) x (chunks of 4096 tokens): the decision (redundantly per
+// CTA), the residual mass of the row pair at the first rejection (or of
+// the bonus row) per chunk, and, in the last CTA of the sequence, the
+// inverse-CDF draw.
 template <bool kVec>
-__global__ void __launch_bounds__(kThreads) residual_kernel(const VerifyArgs a) {
+__global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyArgs a) {
+  __shared__ DecideSmem ds;
   __shared__ ff sm_ff[kWarps];
   __shared__ int sm_i[2 * kWarps];
-  __shared__ SeqState st;
   __shared__ ff s_base, s_t, s_S;
   __shared__ int s_chunk;
   const int b = blockIdx.x, chunk = blockIdx.y;
   const int lane = threadIdx.x & 31;
+  load_inputs(a, b, ds);
   griddep_wait();
-  if (threadIdx.x == 0) {
-    const SeqState* g = &a.seq[b];
-    st.n = __ldcg(&g->n);
-    st.bad = __ldcg(&g->bad);
-    st.k_p = __ldcg(&g->k_p);
-    st.k_q = __ldcg(&g->k_q);
-    st.S_p = __ldcg(&g->S_p);
-    st.S_q = __ldcg(&g->S_q);
-    st.kappa = __ldcg(&g->kappa);
-  }
-  __syncthreads();
-  if (st.bad) return;
+  decide(a, b, ds);
+  if (chunk == 0) write_prefix(a, b, ds);
+  const Decision& d = ds.d;
+  if (d.bad) return;
   const int K = a.K;
-  const int n = st.n;
+  const int n = d.n;
   ResRow R;
   R.rej = n < K;
   R.zp = a.zp + static_cast<size_t>(b * (K + 1) + n) * a.V;
   R.zq = R.rej ? a.zq + static_cast<size_t>(b * K + n) * a.V : nullptr;
   R.c = {a.c_hi, a.c_lo};
-  R.k_p = st.k_p;
-  R.k_q = st.k_q;
-  R.kh = st.kappa.x;
-  R.kl = st.kappa.y;
+  R.k_p = d.k_p;
+  R.k_q = d.k_q;
+  R.kh = d.kappa.hi;
+  R.kl = d.kappa.lo;
   R.V = a.V;
 
   {
     float r[kPer];
     residual_segment<kVec>(R, chunk * kChunk + threadIdx.x * kPer, r);
-    ff excl, total;
-    block_excl_scan_ff({segment_total(r), 0.f}, excl, total, sm_ff);
-    if (threadIdx.x == 0) a.res_sums[static_cast<size_t>(b) * a.CB + chunk] = make_float2(total.hi, total.lo);
+    const ff ws = warp_sum_ff({segment_total(r), 0.f});
+    if (lane == 0) sm_ff[threadIdx.x >> 5] = ws;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      ff total = sm_ff[0];
+      for (int w = 1; w < kWarps; ++w) total = ff_add(total, sm_ff[w]);
+      a.res_sums[static_cast<size_t>(b) * a.CB + chunk] = make_float2(total.hi, total.lo);
+    }
   }
   if (!last_block_ticket(&a.tickets[b], static_cast<unsigned>(a.CB), sm_i)) return;
 
   const float2* sums = a.res_sums + static_cast<size_t>(b) * a.CB;
-  const float u = a.u[b * (K + 1) + K];
-  // total residual mass (warp 0, lanes over chunks)
+  const float u = ds.uj[K];
+  // total residual mass (warp 0, lanes over chunks); the first 64 chunk sums
+  // stay in registers for the search below
+  ff cached[2] = {{0.f, 0.f}, {0.f, 0.f}};
   if (threadIdx.x < 32) {
     ff s{0.f, 0.f};
     for (int i = lane; i < a.CB; i += 32) {
       const float2 v = __ldcg(&sums[i]);
-      s = ff_add(s, {v.x, v.y});
+      const ff fv{v.x, v.y};
+      if (i < 64) cached[i >> 5] = fv;
+      s = ff_add(s, fv);
     }
     s = warp_sum_ff(s);
     if (lane == 0) s_S = s;
   }
   __syncthreads();
+  bool refilled = false;
   if (!(s_S.hi > 0.f) && R.rej) {
+    refilled = true;
     // A rejection whose residual has no mass in f32 (impossible in exact
     // arithmetic): draw from p at that position instead.
     R.rej = false;
@@ -447,8 +538,12 @@ __global__ void __launch_bounds__(kThreads) residual_kernel(const VerifyArgs a) 
       const int i = i0 + lane;
       ff v{0.f, 0.f};
       if (i < a.CB) {
-        const float2 w = __ldcg(&sums[i]);
-        v = {w.x, w.y};
+        if (i0 < 64 && !refilled) {
+          v = cached[i0 >> 5];
+        } else {
+          const float2 w = __ldcg(&sums[i]);
+          v = {w.x, w.y};
+        }
       }
       ff incl = v;
 #pragma unroll
@@ -491,7 +586,7 @@ __global__ void __launch_bounds__(kThreads) residual_kernel(const VerifyArgs a) 
     if (y == INT_MAX) y = last_pos >= 0 ? last_pos : 0;
     a.out_tokens[b * (K + 1) + n] = y;
     if (a.out_debug) {
-      const ff mass = R.rej ? ff_div(s_S, {st.S_p.x, st.S_p.y}) : ff{1.f, 0.f};
+      const ff mass = R.rej ? ff_div(s_S, d.S_p) : ff{1.f, 0.f};
       a.out_debug[static_cast<size_t>(b * (K + 1) + n) * 6 + 5] = mass.hi;
     }
   }
@@ -518,14 +613,24 @@ __global__ void __launch_bounds__(kThreads) greedy_finish_kernel(const GreedyArg
     float bv = -INFINITY;
     int bi = INT_MAX;
     int bad = 0;
-    for (int p = threadIdx.x; p < a.P; p += kThreads) {
-      const float v = __ldcg(&pv[p]);
-      const int i = __ldcg(&pi[p]);
-      if (i == -2) {
-        bad = 1;
-      } else if (v > bv || (v == bv && i < bi)) {
-        bv = v;
-        bi = i;
+    constexpr int kBatch = 4;
+    for (int p0 = 0; p0 < a.P; p0 += kThreads * kBatch) {
+      float v[kBatch];
+      int ix[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const int p = p0 + j * kThreads + threadIdx.x;
+        v[j] = p < a.P ? __ldcg(&pv[p]) : -INFINITY;
+        ix[j] = p < a.P ? __ldcg(&pi[p]) : INT_MAX;
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (ix[j] == -2) {
+          bad = 1;
+        } else if (v[j] > bv || (v[j] == bv && ix[j] < bi)) {
+          bv = v[j];
+          bi = ix[j];
+        }
       }
     }
 #pragma unroll
@@ -661,26 +766,22 @@ void exponent_constant(float temperature, float* c_hi, float* c_lo) {
 }
 
 cudaError_t launch_row_stats(const float* zp, const float* zq, int M, int draft_rows, int V, float c_hi, float c_lo,
-                             StatPart* tpart, StatPart* dpart, int* err, cudaStream_t stream) {
+                             StatPart* tpart, StatPart* dpart, int* err, unsigned* tickets, int n_tickets,
+                             cudaStream_t stream) {
   const int P = (V + kChunk - 1) / kChunk;
   const dim3 g(M + draft_rows, P);
   const Expo c{c_hi, c_lo};
   if (V % 4 == 0)
-    row_stats_kernel<true><<<g, kThreads, 0, stream>>>(zp, zq, M, V, c, tpart, dpart, P, err);
+    row_stats_kernel<true><<<g, kThreads, 0, stream>>>(zp, zq, M, V, c, tpart, dpart, P, err, tickets, n_tickets);
   else
-    row_stats_kernel<false><<<g, kThreads, 0, stream>>>(zp, zq, M, V, c, tpart, dpart, P, err);
+    row_stats_kernel<false><<<g, kThreads, 0, stream>>>(zp, zq, M, V, c, tpart, dpart, P, err, tickets, n_tickets);
   return cudaGetLastError();
 }
 
 cudaError_t launch_verify_sampling(const VerifyArgs& a, cudaStream_t stream) {
-  cudaError_t e = launch_dependent(decide_kernel, dim3(a.B), dim3(kThreads), stream, a);
-  if (e != cudaSuccess) return e;
-  const dim3 g2(a.B, a.CB);
-  if (a.V % 4 == 0)
-    e = launch_dependent(residual_kernel<true>, g2, dim3(kThreads), stream, a);
-  else
-    e = launch_dependent(residual_kernel<false>, g2, dim3(kThreads), stream, a);
-  return e;
+  const dim3 g(a.B, a.CB);
+  if (a.V % 4 == 0) return launch_dependent(finish_kernel<true>, g, dim3(kThreads), stream, a);
+  return launch_dependent(finish_kernel<false>, g, dim3(kThreads), stream, a);
 }
 
 cudaError_t launch_greedy_finish(const GreedyArgs& a, cudaStream_t stream) {
