@@ -340,8 +340,9 @@ __device__ void decide(const VerifyArgs& a, int b, DecideSmem& ds) {
   __syncthreads();
 }
 
-// The accepted prefix, the -1 padding, the accept count and the debug
-// fields 0-4 (written once per sequence).
+// The accepted prefix, the -1 padding after the drawn token, the accept
+// count and the debug fields 0-4 (written once per sequence, by the CTA of
+// chunk 0).
 __device__ void write_prefix(const VerifyArgs& a, int b, const DecideSmem& ds) {
   const int lane = threadIdx.x & 31;
   if (threadIdx.x >= 32) return;
@@ -349,7 +350,9 @@ __device__ void write_prefix(const VerifyArgs& a, int b, const DecideSmem& ds) {
   const Decision& d = ds.d;
   for (int j = lane; j <= K; j += 32) {
     const bool slot = j < K;
-    a.out_tokens[b * (K + 1) + j] = (!d.bad && j < d.n) ? ds.xj[j] : -1;
+    // position n belongs to the drawn token, written by the sequence's last
+    // CTA (only an invalid sequence gets -1 there)
+    if (d.bad || j != d.n) a.out_tokens[b * (K + 1) + j] = (!d.bad && j < d.n) ? ds.xj[j] : -1;
     if (a.out_debug) {
       float* dbg = a.out_debug + static_cast<size_t>(b * (K + 1) + j) * 6;
       dbg[0] = slot ? ds.pj[j] : 0.f;
@@ -358,7 +361,7 @@ __device__ void write_prefix(const VerifyArgs& a, int b, const DecideSmem& ds) {
       // log sum_v exp(z_v / T) = ln 2 * (k + log2 S)
       dbg[3] = 0.6931471805599453f * (ds.rk[j] + log2f(ds.rS[j].hi));
       dbg[4] = slot ? 0.6931471805599453f * (ds.rk[K + 1 + j] + log2f(ds.rS[K + 1 + j].hi)) : 0.f;
-      dbg[5] = 0.f;
+      if (d.bad || j != d.n) dbg[5] = 0.f;  // field 5 at n: the last CTA's residual mass
     }
   }
   if (lane == 0) {
@@ -459,6 +462,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyArgs a) {
   const int b = blockIdx.x, chunk = blockIdx.y;
   const int lane = threadIdx.x & 31;
   load_inputs(a, b, ds);
+  __syncthreads();  // the drafts in shared memory are read by other warps below
   griddep_wait();
   decide(a, b, ds);
   if (chunk == 0) write_prefix(a, b, ds);
