@@ -85,7 +85,8 @@ typedef enum {
   SPEC_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than required */
   SPEC_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
   SPEC_ERR_ARCH = 6,         /* current device is not sm_103 (GB300) */
-  SPEC_ERR_DEVICE_INPUT = 7  /* returned by spec_verify_read_error only */
+  SPEC_ERR_DEVICE_INPUT = 7, /* returned by spec_verify_read_error only */
+  SPEC_ERR_SCRATCH_LIMIT = 8 /* request larger than the fixed scratch of the no-allocation entry point */
 } spec_status;
 
 /* Bits of the device error word (spec_verify_read_error). */
@@ -175,6 +176,47 @@ SPEC_API spec_status spec_verify_from_logits(const float *target_logits, const f
                                     int32_t *out_num_accepted, spec_dims dims, void *workspace,
                                     size_t workspace_bytes, float *out_debug,
                                     spec_stream_t stream);
+
+/*
+ * spec_verify_from_logits for callers that cannot allocate device memory.
+ * (No counterpart on the pages: this is a deployment variant of the same step.)
+ *
+ * Some callers have no room to allocate at all while they decode: a serving
+ * process that reserved the whole GPU at start-up for its weights and its
+ * key-value cache has nothing left for a cudaMalloc, and one that does find
+ * memory would stall every stream of the device on the call's implicit
+ * synchronisation in the middle of a decoding step.  This entry point takes
+ * the same inputs and outputs as spec_verify_from_logits but no workspace:
+ * its scratch is a fixed array of SPEC_NOALLOC_SCRATCH_BYTES bytes of device
+ * memory inside the library, which every GPU that loads the library holds
+ * until the process exits.
+ *
+ *  - Requests whose workspace, spec_verify_workspace_bytes(dims, T, 0), would
+ *    exceed SPEC_NOALLOC_SCRATCH_BYTES are refused with
+ *    SPEC_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *  - The first call on a device looks up the array's device address (a
+ *    runtime query, once per device, with that device current); make that
+ *    first call before capturing any stream on the device.
+ *  - Every call on a device shares the one array.  Calls whose work overlaps
+ *    on the GPU (different streams, different host threads without ordering)
+ *    race on it and corrupt each other's results; order them.  Each call
+ *    clears what it needs cleared itself, so stale contents of the last call
+ *    do no harm.
+ *  - Nothing is allocated: no cudaMalloc, no cudaFree, no allocating library
+ *    routine.  Error reporting as in spec_verify_from_logits; the device
+ *    error word lives in the shared array and is read with
+ *    spec_verify_noalloc_read_error.
+ */
+#define SPEC_NOALLOC_SCRATCH_BYTES (1u << 20)
+SPEC_API spec_status spec_verify_from_logits_noalloc(const float *target_logits, const float *draft_logits,
+                                                     const int32_t *draft_tokens, const float *uniforms,
+                                                     float temperature, int32_t *out_tokens,
+                                                     int32_t *out_num_accepted, spec_dims dims, float *out_debug,
+                                                     spec_stream_t stream);
+
+/* Device error word of the no-allocation entry point's last call on the
+ * current device (synchronises `stream` first); as spec_verify_read_error. */
+SPEC_API spec_status spec_verify_noalloc_read_error(int32_t *error_word, spec_stream_t stream);
 
 /*
  * LM head alone (page "quochung.cyou" section "Hidden state": the final hidden

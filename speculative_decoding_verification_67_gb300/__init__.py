@@ -24,7 +24,7 @@ import torch
 __all__ = [
     "SPEC_DEBUG_FIELDS", "SpecError", "library", "workspace_bytes", "host_workspace_bytes",
     "spec_verify", "spec_verify_from_logits", "spec_lm_head", "spec_verify_host", "read_error",
-    "Verifier",
+    "spec_verify_from_logits_noalloc", "noalloc_read_error", "Verifier",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspec_verify.so")
@@ -57,7 +57,10 @@ _SIGS = {
     "spec_verify_host_workspace_bytes": (_SZ, [SpecDims, _F32]),
     "spec_verify_host": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _SZ, _VP]),
     "spec_verify_read_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32), _VP]),
+    "spec_verify_from_logits_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _VP]),
+    "spec_verify_noalloc_read_error": (ctypes.c_int, [ctypes.POINTER(_I32), _VP]),
 }
+NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 def library() -> ctypes.CDLL:
@@ -193,6 +196,40 @@ def spec_verify_from_logits(target_logits, draft_logits, draft_tokens, uniforms,
         _ptr(uniforms if T > 0 else None), T, _ptr(out_tokens), _ptr(out_num_accepted), SpecDims(B, K, 0, V),
         _ptr(workspace), workspace.numel(), _ptr(out_debug), _stream(stream)))
     return out_tokens, out_num_accepted
+
+
+def spec_verify_from_logits_noalloc(target_logits, draft_logits, draft_tokens, uniforms, temperature: float, *,
+                                    out_tokens, out_num_accepted, out_debug=None, stream=None):
+    """spec_verify_from_logits without a workspace, for callers that cannot
+    allocate device memory while they decode (the library's fixed
+    NOALLOC_SCRATCH_BYTES array serves as scratch; calls on one device must
+    not overlap).  The outputs must be given: nothing is allocated here."""
+    B, K = draft_tokens.shape
+    V = target_logits.shape[1]
+    T = float(temperature)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, K), "cuda")
+    _need(target_logits, "target_logits", torch.float32, (B * (K + 1), V), "cuda")
+    if T > 0:
+        _need(draft_logits, "draft_logits", torch.float32, (B * K, V), "cuda")
+        _need(uniforms, "uniforms", torch.float32, (B, K + 1), "cuda")
+    _need(out_tokens, "out_tokens", torch.int32, (B, K + 1), "cuda")
+    _need(out_num_accepted, "out_num_accepted", torch.int32, (B,), "cuda")
+    if out_debug is not None:
+        _need(out_debug, "out_debug", torch.float32, (B, K + 1, SPEC_DEBUG_FIELDS), "cuda")
+    _check(library().spec_verify_from_logits_noalloc(
+        _ptr(target_logits), _ptr(draft_logits if T > 0 else None), _ptr(draft_tokens if K > 0 else None),
+        _ptr(uniforms if T > 0 else None), T, _ptr(out_tokens), _ptr(out_num_accepted), SpecDims(B, K, 0, V),
+        _ptr(out_debug), _stream(stream)))
+    return out_tokens, out_num_accepted
+
+
+def noalloc_read_error(stream=None) -> int:
+    """Device error word of the no-allocation entry point's last call."""
+    word = ctypes.c_int32(0)
+    st = library().spec_verify_noalloc_read_error(ctypes.byref(word), _stream(stream))
+    if st not in (0, 7):
+        _check(st)
+    return int(word.value)
 
 
 def spec_lm_head(hidden, W_lm, logits=None, stream=None):

@@ -175,6 +175,8 @@ const char* spec_status_string(spec_status s) {
     case SPEC_ERR_CUDA: return "SPEC_ERR_CUDA: CUDA call failed";
     case SPEC_ERR_ARCH: return "SPEC_ERR_ARCH: current device is not sm_103 (GB300)";
     case SPEC_ERR_DEVICE_INPUT: return "SPEC_ERR_DEVICE_INPUT: invalid input found on the device";
+    case SPEC_ERR_SCRATCH_LIMIT:
+      return "SPEC_ERR_SCRATCH_LIMIT: request larger than the no-allocation entry point's fixed scratch";
   }
   return "SPEC_ERR_UNKNOWN";
 }
@@ -328,6 +330,64 @@ spec_status spec_verify_from_logits(const float* target_logits, const float* dra
                                          out_tokens, out_num_accepted, out_debug, ws, L.CA);
   e = sv::launch_verify_sampling(a, s);
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- no allocation
+// Scratch of spec_verify_from_logits_noalloc: one fixed array per device,
+// shared by every call on that device (see the header).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the scratch array on the current device; looked up once
+// per device (host code cannot use the symbol's name as an address).
+spec_status noalloc_scratch(const DeviceInfo& dev, char** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev.device]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return SPEC_ERR_CUDA;
+    g_noalloc_ptr[dev.device] = ptr;
+  }
+  *out = static_cast<char*>(g_noalloc_ptr[dev.device]);
+  return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+spec_status spec_verify_from_logits_noalloc(const float* target_logits, const float* draft_logits,
+                                            const int32_t* draft_tokens, const float* uniforms, float temperature,
+                                            int32_t* out_tokens, int32_t* out_num_accepted, spec_dims dims,
+                                            float* out_debug, spec_stream_t stream) {
+  if (!dims_ok(dims, false)) return SPEC_ERR_DIMS;
+  if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SPEC_ERR_ARG;
+  const size_t need = make_layout(dims.B, dims.K, dims.V, temperature == 0.f, false, true).total;
+  if (need > SPEC_NOALLOC_SCRATCH_BYTES) return SPEC_ERR_SCRATCH_LIMIT;
+  DeviceInfo dev;
+  spec_status st = current_device(dev);
+  if (st != SPEC_OK) return st;
+  char* scratch = nullptr;
+  st = noalloc_scratch(dev, &scratch);
+  if (st != SPEC_OK) return st;
+  return spec_verify_from_logits(target_logits, draft_logits, draft_tokens, uniforms, temperature, out_tokens,
+                                 out_num_accepted, dims, scratch, SPEC_NOALLOC_SCRATCH_BYTES, out_debug, stream);
+}
+
+spec_status spec_verify_noalloc_read_error(int32_t* error_word, spec_stream_t stream) {
+  if (!error_word) return SPEC_ERR_ARG;
+  DeviceInfo dev;
+  spec_status st = current_device(dev);
+  if (st != SPEC_OK) return st;
+  char* scratch = nullptr;
+  st = noalloc_scratch(dev, &scratch);
+  if (st != SPEC_OK) return st;
+  return spec_verify_read_error(scratch, error_word, stream);
 }
 
 spec_status spec_lm_head(const void* hidden, const void* W_lm, float* logits, int32_t M, int32_t d, int32_t V,
