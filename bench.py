@@ -105,15 +105,19 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def dist_setup(n_gpus: int):
+def dist_setup(n_gpus: int, backend: str = "nccl"):
+    """One process per GPU under torchrun (RANK / WORLD_SIZE / LOCAL_RANK /
+    MASTER_* from the environment); single process otherwise."""
     if n_gpus > 1 or int(os.environ.get("WORLD_SIZE", "1")) > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl")
+        dist.init_process_group(backend)
         rank, world = dist.get_rank(), dist.get_world_size()
         local = int(os.environ.get("LOCAL_RANK", rank))
-        torch.cuda.set_device(local)
+        if backend == "nccl":
+            torch.cuda.set_device(local)
         return rank, world, local
-    torch.cuda.set_device(0)
+    if torch.cuda.is_available():
+        torch.cuda.set_device(0)
     return 0, 1, 0
 
 
@@ -124,12 +128,21 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's time: the whole job is done only when it is."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(local_ms: float, world: int, units_per_step_per_rank: int, steps: int) -> tuple:
+    """(value, max_ms): whole-job units per second over the max-over-ranks
+    time; every rank processes its own units (weak scaling)."""
+    ms = max_over_ranks(local_ms, world)
+    return world * units_per_step_per_rank * steps / (ms / 1e3), ms
 
 
 def host_arrays(inp) -> dict:
@@ -292,12 +305,11 @@ def main():
     barrier(world)
     ms = e0.elapsed_time(e1)
     clk = clocks.stop()
-    ms = max_over_ranks(ms, world)
+    value, ms = job_throughput(ms, world, M, args.steps)
     ms_per_step = ms / args.steps
     # a contraction timed inside a loop of a second or more runs at the
     # sustained (power-capped) tensor rate, a short one at the burst rate
     peak_tf = peak_tf_sustained if ms >= 1000.0 else peak_tf_burst
-    value = world * M * args.steps / (ms / 1e3)
 
     # dominant kernel: the LM head as the step runs it (fused softmax statistics
     # for small batches), timed per step with CUDA events recorded between the
