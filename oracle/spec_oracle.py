@@ -19,7 +19,7 @@ Everything is plain numpy in float64.  The steps follow the pages:
         and the acceptance / residual / exactness equations under
         "Приёмка и почему распределение НЕ портится".
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   - temperature: p = softmax(z / T) for target and draft alike; T = 0 is the
     greedy limit (argmax, ties to the lowest token id);
   - accept iff u < a (strict; [QH] prints u <= a, [MLC] prints random() < a;

@@ -8,12 +8,15 @@ Tolerances (fp32 kernels against the fp64 oracle):
     (the decision is within rounding of its threshold; counted);
   * the drawn token: identical, except where u lies within DRAW_BAND of a
     boundary of the drawn token's CDF step, measured relative to that step's
-    width (counted); see DESIGN.md, "Readings", for why the band is relative;
+    width (counted); the band is relative because an f32 CDF step is only
+    resolved to a fraction of its own width, however small the step;
   * greedy: bit-exact, except rows whose two largest oracle logits are closer
     than twice the measured logit error (counted; only there may the f32
     argmax legitimately differ).
 """
 from __future__ import annotations
+
+import os
 
 import numpy as np
 import torch
@@ -135,3 +138,19 @@ def logits_error(z_gpu: np.ndarray, z_ref: np.ndarray) -> dict:
 
 def cuda_inputs(inputs: dict) -> dict:
     return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inputs.items()}
+
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def load_golden(name):
+    """A fixture under tests/golden/: lines "key value value ...", '#' comments."""
+    out = {}
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *vals = line.split()
+            out[key] = np.array([float(v) for v in vals])
+    return out

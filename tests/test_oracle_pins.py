@@ -18,20 +18,7 @@ import oracle
 from oracle import spec_oracle
 from speculative_decoding_verification_67_gb300 import synth
 
-GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
-
-
-def load_golden(name):
-    out = {}
-    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
-        for line in f:
-            line = line.split("#", 1)[0].strip()
-            if not line:
-                continue
-            key, *vals = line.split()
-            out[key] = np.array([float(v) for v in vals])
-    return out
-
+from _helpers import load_golden
 
 def draw_drafts(q_rows, n, seed):
     """n independent draft tokens per row of q (Gumbel-max, seeded)."""
