@@ -1,6 +1,7 @@
 """Benchmark of the verify-and-accept step on GB300.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+               [--row verify|kv_commit]
 
 A step is one call of the whole step (LM head, softmax statistics, accept
 test, accepted prefix, residual / bonus draw) on one batch of the workload,
@@ -13,6 +14,11 @@ inputs resident in HBM.  Prints ONE JSON line on rank 0.
   e2e        the same metric through spec_verify_host: pinned host inputs
              copied in and the tokens copied out inside the timed region
   cpu_baseline  the fp64 CPU oracle on a bounded sample of the same workload
+
+--row kv_commit measures the KV-cache commit that follows the step instead
+(one spec_kv_commit call per step -- a plan kernel and a copy kernel -- on a
+paged cache, KV workloads of synth.KV_WORKLOADS; value = kept entry bytes
+read and written per second).
 
 With N > 1 (torchrun) every rank runs its own copy of the workload (the
 sequences of different ranks are independent problems): weak scaling, no
@@ -261,6 +267,143 @@ def dataclasses_replace(w, **kw):
     return dataclasses.replace(w, **kw)
 
 
+# ------------------------------------------------------------------ KV commit
+KV_METRIC = "KV-cache commit: kept entry bytes copied (read + written) per second"
+
+
+def kv_bytes(w, n) -> int:
+    """Algorithmic bytes of one commit: every kept entry read from the staging
+    plane and written to its slot, plus the per-sequence integers."""
+    keep = [0 if int(x) < 0 else min(int(x) + 1, w.S) for x in n]
+    return 2 * sum(keep) * w.layers * w.entry_bytes + 4 * w.B * 3 + 4 * sum((k + w.page_size - 1) // w.page_size + 1
+                                                                              for k in keep)
+
+
+def run_kv_commit(args):
+    import speculative_decoding_verification_67_gb300 as sv
+
+    w = synth.KV_WORKLOADS[args.kv_workload]
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    inp = synth.make_kv_inputs(w, device=dev, seed=w.seed + rank)
+    stream = torch.cuda.current_stream(dev)
+    ws = sv.kv_workspace(inp["pool"], w.B, w.S, w.max_pages)
+    seq0 = inp["seq_len"].clone()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (129 MB)
+    flush_rd = torch.ones(64 << 20, dtype=torch.float32, device=dev)  # 256 MB
+    nbytes = kv_bytes(w, inp["num_accepted"].cpu().tolist())
+    fused = w.B <= 4096   # the library's one-kernel path (plan + copy above that)
+
+    def commit():
+        sv.spec_kv_commit(inp["num_accepted"], inp["seq_len"], inp["block_table"], inp["pool"], inp["staged"],
+                          workspace=ws, stream=stream)
+
+    peak_gbs, _, _, peak_kind = load_peaks()
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        inp["seq_len"].copy_(seq0)
+        commit()
+    torch.cuda.synchronize()
+    barrier(world)
+    # each launch timed alone between events; the lengths are reset and L2 is
+    # flushed between launches, outside the event pairs: a 256 MB write, then a
+    # 256 MB read so that the write-back of the dirty lines is not charged to
+    # the commit (a decode step reaches the commit with L2 full of the LM
+    # head's clean weight lines, not of dirty ones)
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for e0, e1 in pairs:
+        inp["seq_len"].copy_(seq0)
+        flush.fill_(1)
+        flush_rd.sum()
+        e0.record(stream)
+        commit()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    launch_ms = [a.elapsed_time(b) for a, b in pairs]
+    mean_ms = max_over_ranks(statistics.mean(launch_ms), world)
+    err = sv.kv_commit_read_error(ws, stream=stream)  # of the last timed call
+    gbs = nbytes / (mean_ms * 1e-3) / 1e9
+    value = world * nbytes / (mean_ms * 1e-3) / 1e9
+
+    # end to end: num_accepted copied in from pinned host memory, the commit,
+    # the new lengths copied back, host wall clock
+    n_host = inp["num_accepted"].cpu().pin_memory()
+    len_host = torch.empty_like(n_host).pin_memory()
+    n_dev = torch.empty_like(inp["num_accepted"])
+    e2e_steps = max(10, min(args.steps, 200))
+    e2e_s = 0.0
+    for _ in range(e2e_steps):
+        inp["seq_len"].copy_(seq0)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        n_dev.copy_(n_host, non_blocking=True)
+        sv.spec_kv_commit(n_dev, inp["seq_len"], inp["block_table"], inp["pool"], inp["staged"], workspace=ws,
+                          stream=stream)
+        len_host.copy_(inp["seq_len"], non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_s += time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, world)
+    e2e = {"value": world * nbytes * e2e_steps / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": 4 * w.B,
+           "d2h_bytes_per_step": 4 * w.B, "steps": e2e_steps, "ms_per_step": 1e3 * e2e_s / e2e_steps,
+           "timer": "host wall clock: H2D num_accepted, spec_kv_commit, D2H seq_len, synchronise"}
+    line = {
+        "metric": KV_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "K": w.K, "S": w.S, "layers": w.layers, "entry_bytes": w.entry_bytes,
+                   "page_size": w.page_size, "bytes_per_commit": nbytes,
+                   "kept_entries": int(sum(0 if int(x) < 0 else min(int(x) + 1, w.S)
+                                           for x in inp["num_accepted"].cpu().tolist())),
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "flushed between launches (256 MB write + 256 MB read, outside the event pairs)"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs,
+                     "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "kv_commit_fused_kernel" if fused else "kv_plan_kernel + kv_copy_kernel",
+                     "bytes_per_launch": nbytes, "launch_ms": mean_ms,
+                     "launch_ms_min": min(launch_ms)},
+        "e2e": e2e, "gpu_launches": (1 if fused else 2) * args.steps, "clocks": clk, "device_error_word": err,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = kv_cpu_baseline(w, inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def kv_cpu_baseline(w, inp, reps: int = 3) -> dict:
+    """The oracle's commit on the host cores, whole workload, a few repeats."""
+    from oracle import kv_commit as kv_oracle
+    host = {k: v.cpu().numpy() for k, v in inp.items()}
+    n = host["num_accepted"]
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        pool = host["pool"]
+        kv_oracle.commit(n, host["seq_len"], host["block_table"], pool, host["staged"], w.page_size)
+    dt = (time.perf_counter() - t0) / reps
+    nbytes = kv_bytes(w, n.tolist())
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"whole workload {w.name}, {reps} commits, numpy on one host thread"}
+
+
+def run_kv_reference(args):
+    """--impl reference for the KV row: the oracle on the host, rank 0 only."""
+    w = synth.KV_WORKLOADS[args.kv_workload]
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    inp = synth.make_kv_inputs(w, device="cpu")
+    base = kv_cpu_baseline(w, inp, reps=max(1, min(args.steps, 50)))
+    line = {"impl": "reference", "metric": KV_METRIC, "value": base["value"], "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "u8", "data": "synthetic", "config": {"workload": w.name}, "cpu_baseline": base,
+            "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -269,8 +412,15 @@ def main():
     ap.add_argument("--workload", default="head_B8_K4_V128256", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--row", default="verify", choices=["verify", "kv_commit"])
+    ap.add_argument("--kv-workload", default="kv_B64_K8_L80_E4096", choices=sorted(synth.KV_WORKLOADS))
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.row == "kv_commit":
+        if args.impl == "reference":
+            return run_kv_reference(args)
+        args.steps = min(args.steps, 500)
+        return run_kv_commit(args)
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

@@ -12,7 +12,9 @@ Names follow the C ABI:
 * :func:`spec_verify_from_logits` -- verify-and-accept on given logits;
 * :func:`spec_lm_head` -- the LM-head contraction alone;
 * :func:`spec_verify_host` -- :func:`spec_verify` with host (CPU) tensors;
-* :func:`read_error` -- the device error word of a workspace.
+* :func:`read_error` -- the device error word of a workspace;
+* :func:`spec_kv_commit` -- commit the kept cache entries of a round
+  (``include/spec_kv_commit.h``).
 """
 from __future__ import annotations
 
@@ -25,6 +27,7 @@ __all__ = [
     "SPEC_DEBUG_FIELDS", "SpecError", "library", "workspace_bytes", "host_workspace_bytes",
     "spec_verify", "spec_verify_from_logits", "spec_lm_head", "spec_verify_host", "read_error",
     "spec_verify_from_logits_noalloc", "noalloc_read_error", "Verifier",
+    "kv_workspace", "spec_kv_commit", "kv_commit_read_error",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspec_verify.so")
@@ -34,6 +37,12 @@ DEVERR_TOKEN_RANGE, DEVERR_NONFINITE, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 
 class SpecDims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("K", ctypes.c_int32), ("d", ctypes.c_int32), ("V", ctypes.c_int32)]
+
+
+class SpecKvDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("S", ctypes.c_int32), ("layers", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("max_pages", ctypes.c_int32),
+                ("entry_bytes", ctypes.c_int64)]
 
 
 class SpecError(RuntimeError):
@@ -59,6 +68,9 @@ _SIGS = {
     "spec_verify_read_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32), _VP]),
     "spec_verify_from_logits_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _VP]),
     "spec_verify_noalloc_read_error": (ctypes.c_int, [ctypes.POINTER(_I32), _VP]),
+    "spec_kv_commit_workspace_bytes": (_SZ, [SpecKvDims]),
+    "spec_kv_commit": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, SpecKvDims, _VP, _SZ, _VP]),
+    "spec_kv_commit_read_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32), _VP]),
 }
 NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -304,3 +316,67 @@ class Verifier:
                            out_tokens=self.out_tokens, out_num_accepted=self.out_num_accepted,
                            workspace=self.workspace, out_target_logits=self.target_logits,
                            out_debug=out_debug, stream=stream, stage_events=stage_events)
+
+
+# ---------------------------------------------------------------- KV commit
+KV_DEVERR_CAPACITY, KV_DEVERR_PAGE, KV_DEVERR_LENGTH = 1, 2, 4
+
+
+def _kv_dims(num_accepted, block_table, pool, staged, S):
+    if pool is None or pool.dim() != 4 or not pool.is_cuda or not pool.is_contiguous():
+        raise ValueError("pool must be a contiguous CUDA tensor [layers][num_pages][page_size][E]")
+    layers, num_pages, page_size, E = pool.shape
+    B = num_accepted.shape[0]
+    if staged is not None:
+        if staged.dtype != pool.dtype:
+            raise ValueError("staged and pool must share a dtype")
+        S = staged.shape[2]
+        _need(staged, "staged", pool.dtype, (layers, B, S, E), "cuda")
+    elif S is None:
+        raise ValueError("S is required in in-place mode")
+    if block_table.dim() != 2:
+        raise ValueError("block_table must be [B][max_pages]")
+    return SpecKvDims(B, int(S), layers, page_size, num_pages, block_table.shape[1], E * pool.element_size())
+
+
+def kv_workspace(pool, B: int, S: int, max_pages: int = 1, device=None) -> torch.Tensor:
+    """A zeroed workspace for :func:`spec_kv_commit` on caches shaped like
+    ``pool`` with ``B`` sequences of ``S`` staged entries (reusable across
+    calls; each call leaves it ready for the next)."""
+    layers, num_pages, page_size, E = pool.shape
+    dims = SpecKvDims(B, S, layers, page_size, num_pages, max_pages, E * pool.element_size())
+    n = library().spec_kv_commit_workspace_bytes(dims)
+    if n == 0:
+        raise ValueError("invalid sizes")
+    return torch.zeros(int(n), dtype=torch.uint8, device=pool.device if device is None else device)
+
+
+def spec_kv_commit(num_accepted, seq_len, block_table, pool, staged=None, *, S: int = None, workspace=None,
+                   stream=None):
+    """Commit one round's kept cache entries.
+
+    ``pool`` [layers][num_pages][page_size][E] and ``staged``
+    [layers][B][S][E] (same dtype; E elements make one entry) or None for
+    in-place mode, where ``S`` must be given.  ``num_accepted`` and
+    ``seq_len`` int32 [B] (``seq_len`` is advanced in place), ``block_table``
+    int32 [B][max_pages].  Returns the workspace (its error word is read by
+    :func:`kv_commit_read_error`)."""
+    dims = _kv_dims(num_accepted, block_table, pool, staged, S)
+    _need(num_accepted, "num_accepted", torch.int32, (dims.B,), "cuda")
+    _need(seq_len, "seq_len", torch.int32, (dims.B,), "cuda")
+    _need(block_table, "block_table", torch.int32, (dims.B, dims.max_pages), "cuda")
+    if workspace is None:
+        workspace = kv_workspace(pool, dims.B, dims.S, dims.max_pages)
+    if workspace.dtype != torch.uint8 or not workspace.is_cuda:
+        raise ValueError("workspace must be a CUDA uint8 tensor")
+    _check(library().spec_kv_commit(_ptr(num_accepted), _ptr(seq_len), _ptr(block_table), _ptr(staged),
+                                    _ptr(pool), dims, _ptr(workspace), workspace.numel(), _stream(stream)))
+    return workspace
+
+
+def kv_commit_read_error(workspace, stream=None) -> int:
+    """Synchronises the stream and returns the error word of the latest commit
+    on ``workspace`` (KV_DEVERR_* bits)."""
+    word = ctypes.c_int32(0)
+    _check(library().spec_kv_commit_read_error(_ptr(workspace), ctypes.byref(word), _stream(stream)))
+    return int(word.value)

@@ -17,8 +17,9 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libspec_verify.so")
 
-SOURCES = ["capi.cu", "lm_head_sm103.cu", "verify_sm103.cu"]
-HEADERS = ["internal.h", "sm103_ptx.cuh"]
+SOURCES = sorted(f for f in os.listdir(CSRC) if f.endswith(".cu"))
+HEADERS = sorted(f for f in os.listdir(CSRC) if f.endswith((".h", ".cuh")))
+PUBLIC_HEADERS = sorted(f for f in os.listdir(INCLUDE) if f.endswith(".h"))
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]
@@ -35,8 +36,9 @@ def _fingerprint() -> str:
     for name in SOURCES + HEADERS:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + f.read())
-    with open(os.path.join(INCLUDE, "spec_verify.h"), "rb") as f:
-        h.update(f.read())
+    for name in PUBLIC_HEADERS:
+        with open(os.path.join(INCLUDE, name), "rb") as f:
+            h.update(name.encode() + f.read())
     h.update(" ".join(ARCH + FLAGS).encode())
     h.update(os.uname().machine.encode())
     return h.hexdigest()

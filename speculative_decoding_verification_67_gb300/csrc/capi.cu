@@ -8,6 +8,36 @@
 #include "internal.h"
 #include "spec_verify.h"
 
+namespace sv {
+
+namespace {
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+}  // namespace
+
+int current_device(DeviceInfo& out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return SPEC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (di.device < 0) {
+    DeviceInfo t;
+    t.device = dev;
+    if (cudaDeviceGetAttribute(&t.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&t.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      return SPEC_ERR_CUDA;
+    di = t;
+  }
+  out = di;
+  if (out.cc_major != 10 || out.cc_minor != 3) return SPEC_ERR_ARCH;
+  return SPEC_OK;
+}
+
+}  // namespace sv
+
 namespace {
 
 using sv::DeviceInfo;
@@ -73,29 +103,7 @@ bool dims_ok(const spec_dims& d, bool need_head) {
   return true;
 }
 
-std::mutex g_dev_mu;
-DeviceInfo g_dev[64];
-
-spec_status current_device(DeviceInfo& out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return SPEC_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_dev_mu);
-  DeviceInfo& di = g_dev[dev];
-  if (di.device < 0) {
-    DeviceInfo t;
-    t.device = dev;
-    if (cudaDeviceGetAttribute(&t.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&t.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&t.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&t.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
-      return SPEC_ERR_CUDA;
-    di = t;
-  }
-  out = di;
-  if (out.cc_major != 10 || out.cc_minor != 3) return SPEC_ERR_ARCH;
-  return SPEC_OK;
-}
+spec_status device_status(DeviceInfo& out) { return static_cast<spec_status>(sv::current_device(out)); }
 
 spec_status check_sampling_inputs(const spec_dims& d, float T, const float* draft_logits,
                                   const int32_t* draft_tokens, const float* uniforms, const int32_t* out_tokens,
@@ -208,7 +216,7 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
   if (!workspace || workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return SPEC_ERR_ALIGN;
   DeviceInfo dev;
-  st = current_device(dev);
+  st = device_status(dev);
   if (st != SPEC_OK) return st;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -305,7 +313,7 @@ spec_status spec_verify_from_logits(const float* target_logits, const float* dra
   if (!workspace || workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return SPEC_ERR_ALIGN;
   DeviceInfo dev;
-  st = current_device(dev);
+  st = device_status(dev);
   if (st != SPEC_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* ws = static_cast<char*>(workspace);
@@ -370,7 +378,7 @@ spec_status spec_verify_from_logits_noalloc(const float* target_logits, const fl
   const size_t need = make_layout(dims.B, dims.K, dims.V, temperature == 0.f, false, true).total;
   if (need > SPEC_NOALLOC_SCRATCH_BYTES) return SPEC_ERR_SCRATCH_LIMIT;
   DeviceInfo dev;
-  spec_status st = current_device(dev);
+  spec_status st = device_status(dev);
   if (st != SPEC_OK) return st;
   char* scratch = nullptr;
   st = noalloc_scratch(dev, &scratch);
@@ -382,7 +390,7 @@ spec_status spec_verify_from_logits_noalloc(const float* target_logits, const fl
 spec_status spec_verify_noalloc_read_error(int32_t* error_word, spec_stream_t stream) {
   if (!error_word) return SPEC_ERR_ARG;
   DeviceInfo dev;
-  spec_status st = current_device(dev);
+  spec_status st = device_status(dev);
   if (st != SPEC_OK) return st;
   char* scratch = nullptr;
   st = noalloc_scratch(dev, &scratch);
@@ -396,7 +404,7 @@ spec_status spec_lm_head(const void* hidden, const void* W_lm, float* logits, in
   if (!hidden || !W_lm || !logits) return SPEC_ERR_ARG;
   if (!aligned(hidden, 16) || !aligned(W_lm, 16) || !aligned(logits, 16)) return SPEC_ERR_ALIGN;
   DeviceInfo dev;
-  spec_status st = current_device(dev);
+  spec_status st = device_status(dev);
   if (st != SPEC_OK) return st;
   bool enc_fail = false;
   const cudaError_t e = sv::launch_head(hidden, W_lm, M, d, V, sv::HeadOut::kLogits, logits, nullptr, nullptr,

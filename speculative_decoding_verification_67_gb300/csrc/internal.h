@@ -18,6 +18,10 @@ struct DeviceInfo {
   int max_smem_optin = 0;
 };
 
+// The current device's facts (cached per device); SPEC_ERR_ARCH unless it
+// is compute capability 10.3.  Returns a spec_status value.
+int current_device(DeviceInfo& out);
+
 // Device error word bits (mirror SPEC_DEVERR_* of the public header).
 constexpr int kErrTokenRange = 0x1;
 constexpr int kErrNonFinite = 0x2;

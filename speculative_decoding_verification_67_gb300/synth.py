@@ -175,3 +175,78 @@ def fresh_uniforms(B: int, K: int, count: int, device="cpu", seed: int = 99) -> 
     """``count`` independent sets of uniforms [count, B, K+1] (repeat draws over fixed logits)."""
     g = _gen(torch.device(device), seed)
     return torch.rand((count, B, K + 1), generator=g, device=device, dtype=torch.float32)
+
+
+# ---------------------------------------------------------------------------
+# KV-cache commit inputs.  Paged caches shaped like the models whose heads the
+# verify workloads use: an entry is one layer's key and value for one position
+# (8 KV heads x 128 dims x 2 (K and V) x bf16 = 4096 bytes).  Committed lengths
+# are uniform in [min_len, max_len); the number of accepted drafts is the run
+# length of Bernoulli(accept_rate) successes, capped at K (the shape the
+# verify step produces for i.i.d. acceptance).  Only the pages the commit can
+# touch (the columns covering positions L .. L+S-1) are distinct pool pages,
+# in shuffled order; every other block-table column names page 0, which a
+# commit of these lengths never writes.
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class KvWorkload:
+    name: str
+    B: int
+    K: int
+    layers: int
+    entry_bytes: int
+    page_size: int
+    min_len: int
+    max_len: int
+    accept_rate: float
+    draft_cache: bool = False   # S = K (a separate draft model's cache) instead of K+1
+    seed: int = 0
+
+    @property
+    def S(self) -> int:
+        return self.K if self.draft_cache else self.K + 1
+
+    @property
+    def max_pages(self) -> int:
+        return (self.max_len + self.S + self.page_size - 1) // self.page_size
+
+
+KV_WORKLOADS = {
+    w.name: w
+    for w in (
+        KvWorkload("kv_B8_K4_L32_E4096", B=8, K=4, layers=32, entry_bytes=4096, page_size=16,
+                   min_len=512, max_len=4096, accept_rate=0.75, seed=6711),
+        KvWorkload("kv_B64_K8_L80_E4096", B=64, K=8, layers=80, entry_bytes=4096, page_size=16,
+                   min_len=512, max_len=8192, accept_rate=0.3, seed=6712),
+    )
+}
+
+
+def make_kv_inputs(w: KvWorkload, device="cpu", seed: int | None = None, bad_rows: int = 0) -> dict:
+    """num_accepted, seq_len, block_table (int32), pool uint8
+    [layers][num_pages][page_size][E], staged uint8 [layers][B][S][E].
+    ``bad_rows`` sequences get num_accepted = -1 (a row the verify step
+    flagged)."""
+    g = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    B, S, ps = w.B, w.S, w.page_size
+    seq_len = torch.randint(w.min_len, w.max_len, (B,), generator=g, dtype=torch.int64)
+    succ = torch.rand((B, w.K), generator=g) < w.accept_rate
+    n = torch.cumprod(succ.to(torch.int64), dim=1).sum(dim=1)
+    if bad_rows:
+        n[torch.randperm(B, generator=g)[:bad_rows]] = -1
+    cols = [list(range(int(L) // ps, (int(L) + S - 1) // ps + 1)) for L in seq_len]
+    num_pages = 1 + sum(len(c) for c in cols)
+    perm = (torch.randperm(num_pages - 1, generator=g) + 1).tolist()
+    bt = torch.zeros((B, w.max_pages), dtype=torch.int32)
+    k = 0
+    for b in range(B):
+        for c in cols[b]:
+            bt[b, c] = perm[k]
+            k += 1
+    E = w.entry_bytes
+    gd = _gen(torch.device(device), (w.seed if seed is None else seed) + 1)
+    pool = torch.randint(0, 256, (w.layers, num_pages, ps, E), generator=gd, dtype=torch.uint8,
+                         device=device)
+    staged = torch.randint(0, 256, (w.layers, B, S, E), generator=gd, dtype=torch.uint8, device=device)
+    return dict(num_accepted=n.to(torch.int32).to(device), seq_len=seq_len.to(torch.int32).to(device),
+                block_table=bt.to(device), pool=pool, staged=staged)

@@ -1,5 +1,5 @@
 """The C-ABI library: it builds for sm_103a, loads without a GPU, exports every
-symbol include/spec_verify.h declares, and rejects bad host-side arguments
+symbol the headers under include/ declare, and rejects bad host-side arguments
 before touching CUDA."""
 import ctypes
 import os
@@ -10,7 +10,7 @@ import pytest
 import speculative_decoding_verification_67_gb300 as sv
 from speculative_decoding_verification_67_gb300 import _build
 
-HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "spec_verify.h")
+INCLUDE = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
 
 
 @pytest.fixture(scope="module")
@@ -20,8 +20,12 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    return sorted(set(re.findall(r"SPEC_API\s+[\w\s\*]*?\b(spec_\w+)\s*\(", text)))
+    names = set()
+    for header in sorted(os.listdir(INCLUDE)):
+        if header.endswith(".h"):
+            text = open(os.path.join(INCLUDE, header)).read()
+            names |= set(re.findall(r"SPEC_API\s+[\w\s\*]*?\b(spec_\w+)\s*\(", text))
+    return sorted(names)
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -89,3 +93,27 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(sv, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         sv.library()
+
+
+def test_kv_commit_host_side_errors(lib):
+    good = _fake(0x10000)
+    d = sv.SpecKvDims(4, 5, 2, 16, 100, 10, 4096)
+
+    nws = lib.spec_kv_commit_workspace_bytes(d)
+    assert nws >= 256 + 8 * 4 * 5
+    assert lib.spec_kv_commit_workspace_bytes(sv.SpecKvDims(0, 5, 2, 16, 100, 10, 4096)) == 0
+
+    def call(n=good, L=good, bt=good, st=good, pool=good, dims=d, ws=good, size=nws):
+        return lib.spec_kv_commit(n, L, bt, st, pool, dims, ws, size, _fake(None))
+
+    assert call(n=_fake(None)) == 1
+    assert call(ws=_fake(None)) == 1
+    assert call(pool=_fake(None)) == 1                          # staged mode needs the pool
+    assert call(dims=sv.SpecKvDims(0, 5, 2, 16, 100, 10, 4096)) == 2
+    assert call(dims=sv.SpecKvDims(4, 257, 2, 16, 100, 10, 4096)) == 2
+    assert call(dims=sv.SpecKvDims(4, 5, 2, 16, 100, 10, 24)) == 2   # entry_bytes % 16
+    assert call(dims=sv.SpecKvDims(4, 5, 2, 0, 100, 10, 4096)) == 2
+    assert call(st=_fake(0x10008)) == 3
+    assert call(ws=_fake(0x10004)) == 3
+    assert call(L=_fake(0x10002)) == 3
+    assert call(size=nws - 1) == 4
