@@ -154,3 +154,16 @@ def load_golden(name):
             key, *vals = line.split()
             out[key] = np.array([float(v) for v in vals])
     return out
+
+
+def load_golden_text(name):
+    """Like :func:`load_golden`, values kept as strings."""
+    out = {}
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *vals = line.split()
+            out[key] = vals
+    return out
