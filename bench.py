@@ -1,7 +1,7 @@
 """Benchmark of the verify-and-accept step on GB300.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
-               [--row verify|kv_commit]
+               [--row verify|kv_commit|ngram]
 
 A step is one call of the whole step (LM head, softmax statistics, accept
 test, accepted prefix, residual / bonus draw) on one batch of the workload,
@@ -18,7 +18,8 @@ inputs resident in HBM.  Prints ONE JSON line on rank 0.
 --row kv_commit measures the KV-cache commit that follows the step instead
 (one spec_kv_commit call per step -- a plan kernel and a copy kernel -- on a
 paged cache, KV workloads of synth.KV_WORKLOADS; value = kept entry bytes
-read and written per second).
+read and written per second).  --row ngram measures the prompt-lookup
+drafter (spec_ngram_propose; value = history tokens searched per second).
 
 With N > 1 (torchrun) every rank runs its own copy of the workload (the
 sequences of different ranks are independent problems): weak scaling, no
@@ -267,6 +268,36 @@ def dataclasses_replace(w, **kw):
     return dataclasses.replace(w, **kw)
 
 
+# ------------------------------------------------------------ follow-on rows
+class L2Flush:
+    """Between timed launches: a 256 MB write, then a 256 MB read, so that
+    neither the launch's inputs nor dirty lines of the flush stay in L2."""
+
+    def __init__(self, dev):
+        self.wr = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.rd = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.wr.fill_(1)
+        self.rd.sum()
+
+
+def time_launches(call, steps: int, stream, before=None, flush=None) -> list:
+    """CUDA-event time (ms) of each of ``steps`` calls, each bracketed alone on
+    ``stream``; ``before`` (state reset) and ``flush`` run outside the pairs."""
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in pairs:
+        if before is not None:
+            before()
+        if flush is not None:
+            flush()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in pairs]
+
+
 # ------------------------------------------------------------------ KV commit
 KV_METRIC = "KV-cache commit: kept entry bytes copied (read + written) per second"
 
@@ -289,8 +320,7 @@ def run_kv_commit(args):
     stream = torch.cuda.current_stream(dev)
     ws = sv.kv_workspace(inp["pool"], w.B, w.S, w.max_pages)
     seq0 = inp["seq_len"].clone()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)   # > L2 (129 MB)
-    flush_rd = torch.ones(64 << 20, dtype=torch.float32, device=dev)  # 256 MB
+    flush = L2Flush(dev)
     nbytes = kv_bytes(w, inp["num_accepted"].cpu().tolist())
     fused = w.B <= 4096   # the library's one-kernel path (plan + copy above that)
 
@@ -307,22 +337,11 @@ def run_kv_commit(args):
     torch.cuda.synchronize()
     barrier(world)
     # each launch timed alone between events; the lengths are reset and L2 is
-    # flushed between launches, outside the event pairs: a 256 MB write, then a
-    # 256 MB read so that the write-back of the dirty lines is not charged to
-    # the commit (a decode step reaches the commit with L2 full of the LM
-    # head's clean weight lines, not of dirty ones)
-    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for e0, e1 in pairs:
-        inp["seq_len"].copy_(seq0)
-        flush.fill_(1)
-        flush_rd.sum()
-        e0.record(stream)
-        commit()
-        e1.record(stream)
-    torch.cuda.synchronize()
+    # flushed between launches, outside the event pairs (a decode step reaches
+    # the commit with L2 full of the LM head's clean weight lines)
+    launch_ms = time_launches(commit, args.steps, stream, before=lambda: inp["seq_len"].copy_(seq0), flush=flush)
     barrier(world)
     clk = clocks.stop()
-    launch_ms = [a.elapsed_time(b) for a, b in pairs]
     mean_ms = max_over_ranks(statistics.mean(launch_ms), world)
     err = sv.kv_commit_read_error(ws, stream=stream)  # of the last timed call
     gbs = nbytes / (mean_ms * 1e-3) / 1e9
@@ -404,6 +423,121 @@ def run_kv_reference(args):
     print(json.dumps(line), flush=True)
 
 
+
+# ---------------------------------------------------------- prompt lookup
+NGRAM_METRIC = "prompt-lookup drafting: history tokens searched per second"
+
+
+def ngram_bytes(w, lengths) -> int:
+    """Algorithmic bytes of one call: every history token read once, the
+    lengths read, drafts and counts written."""
+    return 4 * int(sum(int(x) for x in lengths)) + 4 * w.B + 4 * w.B * (w.K + 1)
+
+
+def run_ngram(args):
+    import speculative_decoding_verification_67_gb300 as sv
+
+    w = synth.NGRAM_WORKLOADS[args.ngram_workload]
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    inp = {k: v.to(dev) for k, v in synth.make_ngram_inputs(w, seed=w.seed + rank).items()}
+    stream = torch.cuda.current_stream(dev)
+    ws = sv.ngram_workspace(w.B, w.max_len, w.K, w.n_min, w.n_max, device=dev)
+    drafts = torch.empty((w.B, w.K), dtype=torch.int32, device=dev)
+    count = torch.empty((w.B,), dtype=torch.int32, device=dev)
+    lengths = inp["lengths"].cpu().tolist()
+    tokens = sum(lengths)
+    nbytes = ngram_bytes(w, lengths)
+
+    def call():
+        sv.spec_ngram_propose(inp["history"], inp["lengths"], w.K, w.n_min, w.n_max, out_drafts=drafts,
+                              out_count=count, workspace=ws, stream=stream)
+
+    peak_gbs, _, _, peak_kind = load_peaks()
+    flush = L2Flush(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    barrier(world)
+    launch_ms = time_launches(call, args.steps, stream, flush=flush)
+    barrier(world)
+    clk = clocks.stop()
+    mean_ms = max_over_ranks(statistics.mean(launch_ms), world)
+    err = sv.ngram_read_error(ws, stream=stream)
+    gbs = nbytes / (mean_ms * 1e-3) / 1e9
+
+    # end to end: lengths in from pinned host memory, drafts and counts out;
+    # the history is the engine's resident token buffer
+    len_host = inp["lengths"].cpu().pin_memory()
+    d_host = torch.empty((w.B, w.K), dtype=torch.int32).pin_memory()
+    c_host = torch.empty((w.B,), dtype=torch.int32).pin_memory()
+    len_dev = torch.empty_like(inp["lengths"])
+    e2e_steps = max(10, min(args.steps, 200))
+    e2e_s = 0.0
+    for _ in range(e2e_steps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        len_dev.copy_(len_host, non_blocking=True)
+        sv.spec_ngram_propose(inp["history"], len_dev, w.K, w.n_min, w.n_max, out_drafts=drafts, out_count=count,
+                              workspace=ws, stream=stream)
+        d_host.copy_(drafts, non_blocking=True)
+        c_host.copy_(count, non_blocking=True)
+        torch.cuda.synchronize()
+        e2e_s += time.perf_counter() - t0
+    e2e_s = max_over_ranks(e2e_s, world)
+    e2e = {"value": world * tokens * e2e_steps / e2e_s, "unit": "tokens/s", "h2d_bytes_per_step": 4 * w.B,
+           "d2h_bytes_per_step": 4 * w.B * (w.K + 1), "steps": e2e_steps, "ms_per_step": 1e3 * e2e_s / e2e_steps,
+           "timer": "host wall clock: H2D lengths, spec_ngram_propose, D2H drafts + counts, synchronise"}
+    line = {
+        "metric": NGRAM_METRIC, "value": world * tokens / (mean_ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "max_len": w.max_len, "K": w.K, "n_min": w.n_min, "n_max": w.n_max,
+                   "history_tokens": tokens, "mean_count": float(count.float().mean().item()),
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "flushed between launches (256 MB write + 256 MB read, outside the event pairs)"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs,
+                     "traffic": None, "peak_kind": peak_kind, "kernel": "ngram_kernel", "bytes_per_launch": nbytes,
+                     "launch_ms": mean_ms, "launch_ms_min": min(launch_ms)},
+        "e2e": e2e, "gpu_launches": args.steps, "clocks": clk, "device_error_word": err,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = ngram_cpu_baseline(w, inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def ngram_cpu_baseline(w, inp, reps: int = 3) -> dict:
+    """The oracle's drafter on the host cores, whole workload, a few repeats."""
+    from oracle import ngram_drafter
+    h = inp["history"].cpu().numpy()
+    L = inp["lengths"].cpu().numpy()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        ngram_drafter.propose_batch(h, L, w.K, w.n_min, w.n_max)
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": float(L.sum()) / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"whole workload {w.name}, {reps} calls, numpy on one host thread"}
+
+
+def run_ngram_reference(args):
+    w = synth.NGRAM_WORKLOADS[args.ngram_workload]
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    inp = synth.make_ngram_inputs(w)
+    base = ngram_cpu_baseline(w, inp, reps=max(1, min(args.steps, 20)))
+    line = {"impl": "reference", "metric": NGRAM_METRIC, "value": base["value"], "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "int32", "data": "synthetic", "config": {"workload": w.name}, "cpu_baseline": base,
+            "e2e": {"value": base["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -412,8 +546,9 @@ def main():
     ap.add_argument("--workload", default="head_B8_K4_V128256", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--row", default="verify", choices=["verify", "kv_commit"])
+    ap.add_argument("--row", default="verify", choices=["verify", "kv_commit", "ngram"])
     ap.add_argument("--kv-workload", default="kv_B64_K8_L80_E4096", choices=sorted(synth.KV_WORKLOADS))
+    ap.add_argument("--ngram-workload", default="ngram_B256_L32768_K8", choices=sorted(synth.NGRAM_WORKLOADS))
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.row == "kv_commit":
@@ -421,6 +556,11 @@ def main():
             return run_kv_reference(args)
         args.steps = min(args.steps, 500)
         return run_kv_commit(args)
+    if args.row == "ngram":
+        if args.impl == "reference":
+            return run_ngram_reference(args)
+        args.steps = min(args.steps, 500)
+        return run_ngram(args)
     w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

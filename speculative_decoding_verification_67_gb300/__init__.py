@@ -14,7 +14,8 @@ Names follow the C ABI:
 * :func:`spec_verify_host` -- :func:`spec_verify` with host (CPU) tensors;
 * :func:`read_error` -- the device error word of a workspace;
 * :func:`spec_kv_commit` -- commit the kept cache entries of a round
-  (``include/spec_kv_commit.h``).
+  (``include/spec_kv_commit.h``);
+* :func:`spec_ngram_propose` -- prompt-lookup drafts (``include/spec_ngram.h``).
 """
 from __future__ import annotations
 
@@ -28,6 +29,7 @@ __all__ = [
     "spec_verify", "spec_verify_from_logits", "spec_lm_head", "spec_verify_host", "read_error",
     "spec_verify_from_logits_noalloc", "noalloc_read_error", "Verifier",
     "kv_workspace", "spec_kv_commit", "kv_commit_read_error",
+    "ngram_workspace", "spec_ngram_propose", "ngram_read_error",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspec_verify.so")
@@ -43,6 +45,11 @@ class SpecKvDims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("S", ctypes.c_int32), ("layers", ctypes.c_int32),
                 ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("max_pages", ctypes.c_int32),
                 ("entry_bytes", ctypes.c_int64)]
+
+
+class SpecNgramDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("max_len", ctypes.c_int32), ("K", ctypes.c_int32),
+                ("n_min", ctypes.c_int32), ("n_max", ctypes.c_int32)]
 
 
 class SpecError(RuntimeError):
@@ -71,6 +78,9 @@ _SIGS = {
     "spec_kv_commit_workspace_bytes": (_SZ, [SpecKvDims]),
     "spec_kv_commit": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, SpecKvDims, _VP, _SZ, _VP]),
     "spec_kv_commit_read_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32), _VP]),
+    "spec_ngram_workspace_bytes": (_SZ, [SpecNgramDims]),
+    "spec_ngram_propose": (ctypes.c_int, [_VP, _VP, _VP, _VP, SpecNgramDims, _VP, _SZ, _VP]),
+    "spec_ngram_read_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32), _VP]),
 }
 NOALLOC_SCRATCH_BYTES = 1 << 20
 
@@ -379,4 +389,47 @@ def kv_commit_read_error(workspace, stream=None) -> int:
     on ``workspace`` (KV_DEVERR_* bits)."""
     word = ctypes.c_int32(0)
     _check(library().spec_kv_commit_read_error(_ptr(workspace), ctypes.byref(word), _stream(stream)))
+    return int(word.value)
+
+
+# ---------------------------------------------------------- prompt lookup
+NGRAM_DEVERR_LENGTH, NGRAM_DEVERR_TIMEOUT = 1, 2
+
+
+def ngram_workspace(B: int, max_len: int, K: int, n_min: int = 1, n_max: int = 3, device="cuda") -> torch.Tensor:
+    """A zeroed workspace for :func:`spec_ngram_propose` (reusable across calls)."""
+    n = library().spec_ngram_workspace_bytes(SpecNgramDims(B, max_len, K, n_min, n_max))
+    if n == 0:
+        raise ValueError("invalid sizes")
+    return torch.zeros(int(n), dtype=torch.uint8, device=device)
+
+
+def spec_ngram_propose(history, lengths, K: int, n_min: int = 1, n_max: int = 3, *, out_drafts=None,
+                       out_count=None, workspace=None, stream=None):
+    """Prompt-lookup drafts: ``history`` int32 [B][max_len] (max_len a
+    multiple of 4), ``lengths`` int32 [B] -> (drafts int32 [B][K], count
+    int32 [B])."""
+    if history is None or history.dim() != 2:
+        raise ValueError("history must be [B][max_len]")
+    B, max_len = history.shape
+    _need(history, "history", torch.int32, (B, max_len), "cuda")
+    _need(lengths, "lengths", torch.int32, (B,), "cuda")
+    if out_drafts is None:
+        out_drafts = torch.empty((B, K), dtype=torch.int32, device=history.device)
+    if out_count is None:
+        out_count = torch.empty((B,), dtype=torch.int32, device=history.device)
+    _need(out_drafts, "out_drafts", torch.int32, (B, K), "cuda")
+    _need(out_count, "out_count", torch.int32, (B,), "cuda")
+    if workspace is None:
+        workspace = ngram_workspace(B, max_len, K, n_min, n_max, device=history.device)
+    dims = SpecNgramDims(B, max_len, K, n_min, n_max)
+    _check(library().spec_ngram_propose(_ptr(history), _ptr(lengths), _ptr(out_drafts), _ptr(out_count), dims,
+                                        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out_drafts, out_count
+
+
+def ngram_read_error(workspace, stream=None) -> int:
+    """Synchronises the stream; the error word of the latest proposal call."""
+    word = ctypes.c_int32(0)
+    _check(library().spec_ngram_read_error(_ptr(workspace), ctypes.byref(word), _stream(stream)))
     return int(word.value)

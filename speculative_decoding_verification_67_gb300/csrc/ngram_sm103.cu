@@ -1,0 +1,225 @@
+// Prompt-lookup (n-gram) drafter (quochung.cyou A.I article on speculative
+// decoding, section "Vấn đề 3: Làm sao khi không muốn train drafter?").
+// Declared in include/spec_ngram.h.
+//
+// One kernel.  A CTA takes one chunk of candidate end positions e of one
+// sequence (up to kNgMaxChunk; smaller chunks when there are few sequences,
+// so that the grid still covers the SMs).  Thread 0 reads the length and
+// brings the chunk, plus the kNgMaxN tokens before it, into shared memory
+// with two TMA bulk copies; every thread then scans its positions there, four
+// per 16-byte load, for the number of the history's last tokens ending at e,
+// up to n_max.  The best (length, -e) key of the CTA
+// goes to the sequence's slot with one 64-bit atomicMax; the last CTA of the
+// sequence (a ticket) reads the key, resets slot and ticket, and writes the
+// proposal.  The history is read from HBM once.
+#include <cstdint>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+#include "spec_ngram.h"
+
+namespace {
+
+constexpr int kNgThreads = 256;
+constexpr int kNgMaxChunk = 8192;
+constexpr int kNgMinChunk = 1024;
+constexpr int kNgMaxN = 16;
+constexpr int kNgMaxK = 32;
+constexpr size_t kCtrlBytes = 256;  // [0] error accumulator, [1] error word, [2] sequences finished
+
+struct NgArgs {
+  const int32_t* hist;
+  const int32_t* len;
+  int32_t* drafts;
+  int32_t* count;
+  int B, max_len, K, n_min, n_max, chunk;
+  int* ctrl;
+  unsigned long long* key;  // [B] best (length << 32 | ~e) so far, 0 = none
+  unsigned* ticket;         // [B]
+};
+
+__global__ void __launch_bounds__(kNgThreads) ngram_kernel(const NgArgs a) {
+  __shared__ __align__(128) int s_tok[kNgMaxN + kNgMaxChunk + 4];  // [0, kNgMaxN): the tokens before the chunk
+  __shared__ int s_suf[kNgMaxN];                                     // s_suf[t] = h[L-1-t]
+  __shared__ unsigned long long s_red[kNgThreads / 32];
+  __shared__ __align__(8) uint64_t s_bar;
+  __shared__ int s_L, s_ok, s_last;
+  __shared__ unsigned long long s_key;
+  const int b = blockIdx.y;
+  const long long row = static_cast<long long>(b) * a.max_len;
+  const int c0 = blockIdx.x * a.chunk;
+
+  if (threadIdx.x == 0) {
+    const int L = a.len[b];
+    s_L = L;
+    const bool valid = L >= 0 && L <= a.max_len;
+    const int e_end = valid ? min(c0 + a.chunk, L - 1) : 0;
+    int ok = 1;
+    if (e_end > c0) {
+      // the chunk's tokens [c0, e_end), rounded up to whole 16-byte words
+      // (rows are whole words long), and the kNgMaxN tokens before c0
+      const uint32_t body = static_cast<uint32_t>((e_end - c0 + 3) & ~3) * 4u;
+      const uint32_t halo = c0 > 0 ? kNgMaxN * 4u : 0u;
+      sv::mbar_init(&s_bar, 1);
+      sv::fence_barrier_init();
+      sv::mbar_arrive_expect_tx(&s_bar, body + halo);
+      sv::bulk_load(s_tok + kNgMaxN, a.hist + row + c0, body, &s_bar);
+      if (halo) sv::bulk_load(s_tok, a.hist + row + c0 - kNgMaxN, halo, &s_bar);
+      ok = sv::mbar_wait(&s_bar, 0) ? 1 : 0;
+      if (!ok) {
+        atomicOr(a.ctrl, SPEC_NGRAM_DEVERR_TIMEOUT);
+        (void)sv::mbar_wait(&s_bar, 0);  // give the copies in flight one more bounded wait before leaving
+      }
+    }
+    s_ok = ok;
+  }
+  if (threadIdx.x < a.n_max) {
+    const int L = a.len[b];
+    s_suf[threadIdx.x] = (L >= 0 && L <= a.max_len && static_cast<int>(threadIdx.x) < L)
+                             ? a.hist[row + L - 1 - threadIdx.x] : 0;
+  }
+  __syncthreads();
+  const int L = s_L;
+  const bool valid = L >= 0 && L <= a.max_len;
+  const int e_end = (valid && s_ok) ? min(c0 + a.chunk, L - 1) : 0;
+  const int last_tok = s_suf[0];
+  unsigned long long best = 0ull;
+  // four positions per 16-byte shared load (consecutive threads, consecutive
+  // words: conflict-free); only a token equal to the last one looks further
+  const int n_e = e_end - c0;
+  for (int q0 = 4 * static_cast<int>(threadIdx.x); q0 < n_e; q0 += 4 * kNgThreads) {
+    const int4 v4 = *reinterpret_cast<const int4*>(s_tok + kNgMaxN + q0);
+    const int vq[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (vq[q] == last_tok && q0 + q < n_e) {
+        const int e = c0 + q0 + q;
+        const int* t = s_tok + kNgMaxN + q0 + q;  // t[-l] = h[e-l] for l <= kNgMaxN
+        const int lim = min(a.n_max, e + 1);
+        int l = 1;
+        while (l < lim && t[-l] == s_suf[l]) ++l;
+        if (l >= a.n_min) {
+          const unsigned long long k =
+              (static_cast<unsigned long long>(l) << 32) | (0xffffffffu - static_cast<unsigned>(e));
+          best = k > best ? k : best;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
+    best = o > best ? o : best;
+  }
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long m = 0ull;
+    for (int w = 0; w < kNgThreads / 32; ++w) m = s_red[w] > m ? s_red[w] : m;
+    if (m) atomicMax(a.key + b, m);
+    __threadfence();
+    s_last = atomicAdd(a.ticket + b, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+
+  // the last CTA of sequence b writes its proposal
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_key = atomicExch(a.key + b, 0ull);
+    a.ticket[b] = 0u;
+  }
+  __syncthreads();
+  const unsigned long long k = s_key;
+  int32_t* out = a.drafts + static_cast<long long>(b) * a.K;
+  if (!valid) {
+    if (threadIdx.x < a.K) out[threadIdx.x] = -1;
+    if (threadIdx.x == 0) {
+      a.count[b] = -1;
+      atomicOr(a.ctrl, SPEC_NGRAM_DEVERR_LENGTH);
+    }
+  } else if (k == 0ull) {
+    const int fill = L > 0 ? s_suf[0] : 0;
+    if (threadIdx.x < a.K) out[threadIdx.x] = fill;
+    if (threadIdx.x == 0) a.count[b] = 0;
+  } else {
+    const int e = static_cast<int>(0xffffffffu - static_cast<unsigned>(k & 0xffffffffull));
+    const int cnt = min(a.K, L - 1 - e);
+    if (threadIdx.x < a.K) out[threadIdx.x] = a.hist[row + e + 1 + min(static_cast<int>(threadIdx.x), cnt - 1)];
+    if (threadIdx.x == 0) a.count[b] = cnt;
+  }
+  // the last sequence to finish publishes the call's error word
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(reinterpret_cast<unsigned*>(a.ctrl + 2), 1u) == static_cast<unsigned>(a.B) - 1) {
+      __threadfence();
+      a.ctrl[1] = atomicExch(a.ctrl, 0);
+      a.ctrl[2] = 0;
+    }
+  }
+}
+
+bool dims_ok(const spec_ngram_dims& d) {
+  return d.B >= 1 && d.B <= 65535 && d.max_len >= 4 && d.max_len <= (1 << 30) && d.max_len % 4 == 0 && d.K >= 1 &&
+         d.K <= kNgMaxK && d.n_min >= 1 && d.n_min <= d.n_max && d.n_max <= kNgMaxN;
+}
+
+size_t workspace_bytes(const spec_ngram_dims& d) {
+  const size_t keys = (8u * static_cast<size_t>(d.B) + 255) / 256 * 256;
+  const size_t tickets = (4u * static_cast<size_t>(d.B) + 255) / 256 * 256;
+  return kCtrlBytes + keys + tickets;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_ngram_workspace_bytes(spec_ngram_dims dims) { return dims_ok(dims) ? workspace_bytes(dims) : 0; }
+
+spec_status spec_ngram_propose(const int32_t* history, const int32_t* lengths, int32_t* out_drafts,
+                               int32_t* out_count, spec_ngram_dims dims, void* workspace, size_t workspace_bytes_given,
+                               spec_stream_t stream) {
+  if (!history || !lengths || !out_drafts || !out_count || !workspace) return SPEC_ERR_ARG;
+  if (!dims_ok(dims)) return SPEC_ERR_DIMS;
+  const uintptr_t any4 = reinterpret_cast<uintptr_t>(history) | reinterpret_cast<uintptr_t>(lengths) |
+                         reinterpret_cast<uintptr_t>(out_drafts) | reinterpret_cast<uintptr_t>(out_count);
+  if ((any4 & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 15u) || (reinterpret_cast<uintptr_t>(history) & 15u))
+    return SPEC_ERR_ALIGN;
+  if (workspace_bytes_given < workspace_bytes(dims)) return SPEC_ERR_WORKSPACE;
+  sv::DeviceInfo dev;
+  const int st = sv::current_device(dev);
+  if (st != SPEC_OK) return static_cast<spec_status>(st);
+  NgArgs a;
+  a.hist = history;
+  a.len = lengths;
+  a.drafts = out_drafts;
+  a.count = out_count;
+  a.B = dims.B;
+  a.max_len = dims.max_len;
+  a.K = dims.K;
+  a.n_min = dims.n_min;
+  a.n_max = dims.n_max;
+  a.ctrl = static_cast<int*>(workspace);
+  char* p = static_cast<char*>(workspace) + kCtrlBytes;
+  a.key = reinterpret_cast<unsigned long long*>(p);
+  a.ticket = reinterpret_cast<unsigned*>(p + (8u * static_cast<size_t>(dims.B) + 255) / 256 * 256);
+  // the largest chunk that still gives two CTAs per SM
+  int chunk = kNgMaxChunk;
+  while (chunk > kNgMinChunk &&
+         static_cast<long long>(dims.B) * ((dims.max_len + chunk - 1) / chunk) < 2ll * dev.sm_count)
+    chunk >>= 1;
+  a.chunk = chunk;
+  const dim3 grid((dims.max_len + chunk - 1) / chunk, dims.B);
+  ngram_kernel<<<grid, kNgThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(a);
+  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status spec_ngram_read_error(void* workspace, int32_t* error_word, spec_stream_t stream) {
+  if (!workspace || !error_word) return SPEC_ERR_ARG;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      cudaMemcpy(error_word, static_cast<int*>(workspace) + 1, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return SPEC_OK;
+}
+
+}  // extern "C"

@@ -250,3 +250,70 @@ def make_kv_inputs(w: KvWorkload, device="cpu", seed: int | None = None, bad_row
     staged = torch.randint(0, 256, (w.layers, B, S, E), generator=gd, dtype=torch.uint8, device=device)
     return dict(num_accepted=n.to(torch.int32).to(device), seq_len=seq_len.to(torch.int32).to(device),
                 block_table=bt.to(device), pool=pool, staged=staged)
+
+
+# ---------------------------------------------------------------------------
+# Prompt-lookup drafter inputs: histories shaped like an output rewriting its
+# prompt (the case the drafter is meant for).  Each history is a prompt of
+# tokens drawn from a Zipf(1.2) law over the vocabulary (common tokens recur,
+# as in text and code), followed by an output built from copies of prompt
+# spans (start uniform, length geometric with mean 32) with probability 0.85
+# and otherwise 1-4 fresh Zipf tokens (the edits).  The prompt is 60% of the
+# history; history lengths are uniform in [max_len/2, max_len].
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class NgramWorkload:
+    name: str
+    B: int
+    max_len: int
+    K: int
+    n_min: int
+    n_max: int
+    V: int = 128256
+    seed: int = 0
+
+
+NGRAM_WORKLOADS = {
+    w.name: w
+    for w in (
+        NgramWorkload("ngram_B8_L8192_K4", B=8, max_len=8192, K=4, n_min=1, n_max=3, seed=6721),
+        NgramWorkload("ngram_B256_L32768_K8", B=256, max_len=32768, K=8, n_min=1, n_max=3, seed=6722),
+    )
+}
+
+
+def _zipf_tokens(n: int, V: int, g: torch.Generator) -> torch.Tensor:
+    """n token ids with P(rank r) proportional to r^-1.2, ranks shuffled onto ids."""
+    u = torch.rand(n, generator=g, dtype=torch.float64)
+    # inverse CDF of the continuous power law on [1, V+1), floored to a rank
+    a = 1.2
+    lo, hi = 1.0, float(V + 1) ** (1 - a)
+    r = ((lo + u * (hi - lo)) ** (1.0 / (1 - a))).floor().clamp(1, V).to(torch.int64) - 1
+    return r
+
+
+def make_ngram_inputs(w: NgramWorkload, device="cpu", seed: int | None = None) -> dict:
+    """history int32 [B][max_len] (zero past each length), lengths int32 [B]."""
+    g = torch.Generator().manual_seed(w.seed if seed is None else seed)
+    perm = torch.randperm(w.V, generator=g)
+    hist = torch.zeros((w.B, w.max_len), dtype=torch.int64)
+    lens = torch.randint(w.max_len // 2, w.max_len + 1, (w.B,), generator=g)
+    for b in range(w.B):
+        L = int(lens[b])
+        P = max(1, int(0.6 * L))
+        prompt = _zipf_tokens(P, w.V, g)
+        out = [prompt]
+        n = P
+        while n < L:
+            if float(torch.rand(1, generator=g)) < 0.85:
+                # geometric span length, mean 32, by inverse CDF
+                span = int(math.floor(math.log(1 - float(torch.rand(1, generator=g))) / math.log(1 - 1 / 32))) + 1
+                s = int(torch.randint(0, P, (1,), generator=g))
+                piece = prompt[s:s + span]
+            else:
+                piece = _zipf_tokens(int(torch.randint(1, 5, (1,), generator=g)), w.V, g)
+            out.append(piece)
+            n += len(piece)
+        row = torch.cat(out)[:L]
+        hist[b, :L] = perm[row]
+    return dict(history=hist.to(torch.int32).to(device), lengths=lens.to(torch.int32).to(device))

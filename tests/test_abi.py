@@ -117,3 +117,23 @@ def test_kv_commit_host_side_errors(lib):
     assert call(ws=_fake(0x10004)) == 3
     assert call(L=_fake(0x10002)) == 3
     assert call(size=nws - 1) == 4
+
+
+def test_ngram_host_side_errors(lib):
+    good = _fake(0x10000)
+    d = sv.SpecNgramDims(4, 1024, 4, 1, 3)
+    nws = lib.spec_ngram_workspace_bytes(d)
+    assert nws >= 256 + 4 * 12
+    for bad in (sv.SpecNgramDims(0, 1024, 4, 1, 3), sv.SpecNgramDims(4, 1022, 4, 1, 3),
+                sv.SpecNgramDims(4, 1024, 33, 1, 3), sv.SpecNgramDims(4, 1024, 4, 3, 2),
+                sv.SpecNgramDims(4, 1024, 4, 1, 17), sv.SpecNgramDims(4, 1024, 4, 0, 3)):
+        assert lib.spec_ngram_workspace_bytes(bad) == 0
+
+    def call(h=good, L=good, od=good, oc=good, dims=d, ws=good, size=nws):
+        return lib.spec_ngram_propose(h, L, od, oc, dims, ws, size, _fake(None))
+
+    assert call(h=_fake(None)) == 1
+    assert call(dims=sv.SpecNgramDims(4, 1022, 4, 1, 3)) == 2
+    assert call(h=_fake(0x10004)) == 3
+    assert call(oc=_fake(0x10002)) == 3
+    assert call(size=nws - 1) == 4
