@@ -1,7 +1,7 @@
 """Benchmark of the verify-and-accept step on GB300.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
-               [--row verify|kv_commit|ngram]
+               [--row verify|kv_commit|ngram|draft]
 
 A step is one call of the whole step (LM head, softmax statistics, accept
 test, accepted prefix, residual / bonus draw) on one batch of the workload,
@@ -20,6 +20,8 @@ inputs resident in HBM.  Prints ONE JSON line on rank 0.
 paged cache, KV workloads of synth.KV_WORKLOADS; value = kept entry bytes
 read and written per second).  --row ngram measures the prompt-lookup
 drafter (spec_ngram_propose; value = history tokens searched per second).
+--row draft measures one draft step through the target's LM head
+(spec_draft_step; value = draft tokens per second).
 
 With N > 1 (torchrun) every rank runs its own copy of the workload (the
 sequences of different ranks are independent problems): weak scaling, no
@@ -538,6 +540,127 @@ def run_ngram_reference(args):
     print(json.dumps(line), flush=True)
 
 
+
+# --------------------------------------------------------------- draft step
+DRAFT_METRIC = "draft tokens/sec of one draft step through the target LM head (V=128256)"
+
+
+def run_draft(args):
+    """One draft step per timed step: the target's LM head on B draft rows
+    (logits written to slot 0 of a [B][K][V] draft-logits buffer) and the
+    inverse-CDF draft draw."""
+    import speculative_decoding_verification_67_gb300 as sv
+
+    w = synth.DRAFT_WORKLOADS[args.draft_workload]
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    inp = synth.make_draft_inputs(w, device=dev, seed=w.seed + rank)
+    B, K, d, V, T = w.B, w.K, w.d, w.V, w.temperature
+    stream = torch.cuda.current_stream(dev)
+    dl = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+    tok = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = torch.empty(sv.draft_step_workspace_bytes(B, d, V, T), dtype=torch.uint8, device=dev)
+    h, u = inp["draft_hidden"][0], inp["draft_uniforms"][0]
+
+    def step():
+        sv.spec_draft_step(h, inp["W"], u, T, out_tokens=tok, out_logits=dl[:, 0, :], workspace=ws, stream=stream)
+
+    peak_gbs, _, _, peak_kind = load_peaks()
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    value, ms = job_throughput(e0.elapsed_time(e1), world, B, args.steps)
+    ms_per_step = ms / args.steps
+    nbytes = 2 * V * d + 2 * B * d + 4 * B * V
+    gbs = nbytes / (ms_per_step * 1e-3) / 1e9
+
+    # end to end: h-hat and the uniforms in from pinned host memory, the
+    # draft tokens out, host wall clock
+    h_host = h.cpu().pin_memory()
+    u_host = u.cpu().pin_memory()
+    t_host = torch.empty((B,), dtype=torch.int32).pin_memory()
+    h_dev, u_dev = torch.empty_like(h), torch.empty_like(u)
+    e2e_steps = max(10, min(args.steps, 300))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        h_dev.copy_(h_host, non_blocking=True)
+        u_dev.copy_(u_host, non_blocking=True)
+        sv.spec_draft_step(h_dev, inp["W"], u_dev, T, out_tokens=tok, out_logits=dl[:, 0, :], workspace=ws,
+                           stream=stream)
+        t_host.copy_(tok, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": world * B * e2e_steps / e2e_s, "unit": "draft tokens/s", "h2d_bytes_per_step": 2 * B * d + 4 * B,
+           "d2h_bytes_per_step": 4 * B, "steps": e2e_steps, "ms_per_step": 1e3 * e2e_s / e2e_steps,
+           "timer": "host wall clock: H2D h-hat + uniforms, spec_draft_step, D2H tokens, synchronise"}
+    line = {
+        "metric": DRAFT_METRIC, "value": value, "unit": "draft tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "d": d, "V": V, "T": T,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": f"inputs exceed L2: W_lm {2 * V * d / 1e9:.2f} GB is streamed every step"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs,
+                     "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "head_kernel + finish_kernel (the whole step, both launches)",
+                     "bytes_per_launch": nbytes, "launch_ms": ms_per_step},
+        "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = draft_cpu_baseline(w, inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def draft_cpu_baseline(w, inp, budget_s: float = 12.0) -> dict:
+    """The oracle's draft step (fp64 LM head + draw) on the host cores for a
+    bounded vocabulary slice of one sequence, scaled to the whole step."""
+    from oracle import draft_head
+    h = inp["draft_hidden"][0][:1].double().cpu().numpy()
+    u = inp["draft_uniforms"][0][:1].double().cpu().numpy()
+    W = inp["W"]
+    Vs = 4096
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < budget_s and (n + 1) * Vs <= w.V:
+        Wc = W[n * Vs:(n + 1) * Vs].double().cpu().numpy()
+        draft_head.draft_step(h, Wc, u, w.temperature)
+        n += 1
+    dt = time.perf_counter() - t0
+    per_seq = dt * (w.V / (n * Vs))
+    return {"value": 1.0 / per_seq, "unit": "draft tokens/s", "cores": torch.get_num_threads(), "kind": "oracle",
+            "sample": f"one sequence, {n * Vs} of {w.V} vocabulary rows, scaled to the full head"}
+
+
+def run_draft_reference(args):
+    w = synth.DRAFT_WORKLOADS[args.draft_workload]
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    inp = synth.make_draft_inputs(w)
+    base = draft_cpu_baseline(w, inp, budget_s=min(60.0, 5.0 * max(1, args.steps)))
+    line = {"impl": "reference", "metric": DRAFT_METRIC, "value": base["value"], "unit": "draft tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "f64", "data": "synthetic", "config": {"workload": w.name}, "cpu_baseline": base,
+            "e2e": {"value": base["value"], "unit": "draft tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -546,9 +669,10 @@ def main():
     ap.add_argument("--workload", default="head_B8_K4_V128256", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--row", default="verify", choices=["verify", "kv_commit", "ngram"])
+    ap.add_argument("--row", default="verify", choices=["verify", "kv_commit", "ngram", "draft"])
     ap.add_argument("--kv-workload", default="kv_B64_K8_L80_E4096", choices=sorted(synth.KV_WORKLOADS))
     ap.add_argument("--ngram-workload", default="ngram_B256_L32768_K8", choices=sorted(synth.NGRAM_WORKLOADS))
+    ap.add_argument("--draft-workload", default="draft_B8_K4_V128256", choices=sorted(synth.DRAFT_WORKLOADS))
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.row == "kv_commit":
@@ -556,6 +680,10 @@ def main():
             return run_kv_reference(args)
         args.steps = min(args.steps, 500)
         return run_kv_commit(args)
+    if args.row == "draft":
+        if args.impl == "reference":
+            return run_draft_reference(args)
+        return run_draft(args)
     if args.row == "ngram":
         if args.impl == "reference":
             return run_ngram_reference(args)

@@ -36,7 +36,8 @@ def draft_step(hidden, W, uniforms, temperature: float) -> dict:
     """One draft step for B sequences: ``hidden`` [B, d] (the draft model's
     estimate h-hat, bf16 values), ``W`` [V, d], ``uniforms`` [B] (ignored at
     T = 0).  Returns tokens [B], logits [B, V] (float64) and, at T > 0, the
-    draw margins (lo, hi) of the inverse-CDF rule."""
+    draw margins (lo, hi) of the inverse-CDF rule and the drawn token's
+    probability (the width of its CDF step)."""
     z = spec_oracle.lm_head(hidden, W)
     return draft_step_from_logits(z, uniforms, temperature)
 
@@ -48,4 +49,4 @@ def draft_step_from_logits(z, uniforms, temperature: float) -> dict:
         return dict(tokens=spec_oracle.argmax_lowest(z), logits=z, top2_gap=top2[:, 1] - top2[:, 0])
     q = spec_oracle.softmax_t(z, temperature)
     y, lo, hi, _ = spec_oracle.inverse_cdf(q, np.asarray(uniforms, dtype=np.float64))
-    return dict(tokens=y, logits=z, draw_lo=lo, draw_hi=hi)
+    return dict(tokens=y, logits=z, draw_lo=lo, draw_hi=hi, draw_mass=q[np.arange(len(y)), y])

@@ -15,7 +15,9 @@ Names follow the C ABI:
 * :func:`read_error` -- the device error word of a workspace;
 * :func:`spec_kv_commit` -- commit the kept cache entries of a round
   (``include/spec_kv_commit.h``);
-* :func:`spec_ngram_propose` -- prompt-lookup drafts (``include/spec_ngram.h``).
+* :func:`spec_ngram_propose` -- prompt-lookup drafts (``include/spec_ngram.h``);
+* :func:`spec_draft_step` -- one draft step through the target's LM head
+  (``include/spec_draft.h``).
 """
 from __future__ import annotations
 
@@ -30,6 +32,7 @@ __all__ = [
     "spec_verify_from_logits_noalloc", "noalloc_read_error", "Verifier",
     "kv_workspace", "spec_kv_commit", "kv_commit_read_error",
     "ngram_workspace", "spec_ngram_propose", "ngram_read_error",
+    "draft_step_workspace_bytes", "spec_draft_step",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspec_verify.so")
@@ -79,6 +82,8 @@ _SIGS = {
     "spec_kv_commit": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, SpecKvDims, _VP, _SZ, _VP]),
     "spec_kv_commit_read_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32), _VP]),
     "spec_ngram_workspace_bytes": (_SZ, [SpecNgramDims]),
+    "spec_draft_step_workspace_bytes": (_SZ, [SpecDims, _F32]),
+    "spec_draft_step": (ctypes.c_int, [_VP, _VP, _VP, _F32, _VP, _VP, ctypes.c_int64, SpecDims, _VP, _SZ, _VP]),
     "spec_ngram_propose": (ctypes.c_int, [_VP, _VP, _VP, _VP, SpecNgramDims, _VP, _SZ, _VP]),
     "spec_ngram_read_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32), _VP]),
 }
@@ -433,3 +438,42 @@ def ngram_read_error(workspace, stream=None) -> int:
     word = ctypes.c_int32(0)
     _check(library().spec_ngram_read_error(_ptr(workspace), ctypes.byref(word), _stream(stream)))
     return int(word.value)
+
+
+# --------------------------------------------------------------- draft step
+def draft_step_workspace_bytes(B: int, d: int, V: int, temperature: float) -> int:
+    n = library().spec_draft_step_workspace_bytes(SpecDims(B, 0, d, V), float(temperature))
+    if n == 0:
+        raise ValueError("invalid sizes")
+    return int(n)
+
+
+def spec_draft_step(hidden, W_lm, uniforms, temperature: float, *, out_tokens=None, out_logits=None,
+                    workspace=None, stream=None):
+    """One draft step through the target's LM head: ``hidden`` bf16 [B, d]
+    (the draft model's estimate of the target's hidden state), ``W_lm`` bf16
+    [V, d], ``uniforms`` f32 [B] (None at T = 0).  ``out_logits`` (T > 0
+    only) is an f32 [B, V] view whose rows may be strided, e.g. slot j of a
+    [B, K, V] draft-logits buffer.  Returns (tokens int32 [B], out_logits)."""
+    B, d = hidden.shape
+    V = W_lm.shape[0]
+    T = float(temperature)
+    _need(hidden, "hidden", torch.bfloat16, (B, d), "cuda")
+    _need(W_lm, "W_lm", torch.bfloat16, (V, d), "cuda")
+    if T > 0:
+        _need(uniforms, "uniforms", torch.float32, (B,), "cuda")
+    ld = 0
+    if out_logits is not None:
+        if out_logits.dtype != torch.float32 or tuple(out_logits.shape) != (B, V) or out_logits.stride(1) != 1 \
+                or not out_logits.is_cuda:
+            raise ValueError("out_logits must be a CUDA f32 [B, V] view with unit column stride")
+        ld = out_logits.stride(0)
+    if out_tokens is None:
+        out_tokens = torch.empty((B,), dtype=torch.int32, device=hidden.device)
+    _need(out_tokens, "out_tokens", torch.int32, (B,), "cuda")
+    if workspace is None:
+        workspace = torch.empty(draft_step_workspace_bytes(B, d, V, T), dtype=torch.uint8, device=hidden.device)
+    _check(library().spec_draft_step(_ptr(hidden), _ptr(W_lm), _ptr(uniforms if T > 0 else None), T,
+                                     _ptr(out_tokens), _ptr(out_logits), ld, SpecDims(B, 0, d, V),
+                                     _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out_tokens, out_logits

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "spec_draft.h"
 #include "spec_verify.h"
 
 namespace sv {
@@ -132,6 +133,7 @@ sv::VerifyArgs sampling_args(const Layout& L, const spec_dims& d, float T, const
   a.V = d.V;
   sv::exponent_constant(T, &a.c_hi, &a.c_lo);
   a.zp = zp;
+  a.ldp = d.V;
   a.zq = zq;
   a.x = x;
   a.u = u;
@@ -202,7 +204,7 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
                         const int32_t* draft_tokens, const float* uniforms, float temperature,
                         int32_t* out_tokens, int32_t* out_num_accepted, spec_dims dims, void* workspace,
                         size_t workspace_bytes, float* out_target_logits, float* out_debug,
-                        spec_stream_t stream, void* const* ev) {
+                        spec_stream_t stream, void* const* ev, long long ldz = 0) {
   if (!dims_ok(dims, true)) return SPEC_ERR_DIMS;
   if (!hidden || !W_lm) return SPEC_ERR_ARG;
   if (!aligned(hidden, 16) || !aligned(W_lm, 16)) return SPEC_ERR_ALIGN;
@@ -211,7 +213,7 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
   if (st != SPEC_OK) return st;
   const bool greedy = temperature == 0.f;
   if (greedy && out_target_logits) return SPEC_ERR_ARG;
-  if (out_target_logits && !aligned(out_target_logits, 16)) return SPEC_ERR_ALIGN;
+  if (out_target_logits && !aligned(out_target_logits, 4)) return SPEC_ERR_ALIGN;
   const Layout L = make_layout(dims.B, dims.K, dims.V, greedy, !greedy && !out_target_logits, false);
   if (!workspace || workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return SPEC_ERR_ALIGN;
@@ -239,6 +241,7 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
     return (e == cudaSuccess && mark(2)) ? SPEC_OK : SPEC_ERR_CUDA;
   }
   float* logits = out_target_logits ? out_target_logits : reinterpret_cast<float*>(ws + L.logits);
+  if (!out_target_logits || ldz <= 0) ldz = dims.V;
   const sv::HeadPlan plan = sv::plan_head(M, dims.d, dims.V, sv::HeadOut::kStats, dev);
   sv::HeadStats hs;
   sv::exponent_constant(temperature, &hs.c_hi, &hs.c_lo);
@@ -252,22 +255,23 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
   if (plan.precise) {
     // small batch: the LM head's epilogue and side warps produce the statistics
     e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kStats, logits, nullptr, nullptr, &hs, err,
-                        true, dev, s, &enc_fail);
+                        true, dev, s, &enc_fail, ldz);
     if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
     Pt = plan.target_parts;
   } else {
     // large batch (compute-bound head): logits, then one statistics pass
     e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kLogits, logits, nullptr, nullptr, nullptr,
-                        err, true, dev, s, &enc_fail);
+                        err, true, dev, s, &enc_fail, ldz);
     if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
     e = sv::launch_row_stats(logits, draft_logits, M, dims.B * dims.K, dims.V, hs.c_hi, hs.c_lo, hs.tpart, hs.dpart,
-                             nullptr, hs.tickets, hs.n_tickets, s);
+                             nullptr, hs.tickets, hs.n_tickets, s, ldz);
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
     Pt = L.CA;
   }
   if (!mark(1)) return SPEC_ERR_CUDA;
-  const sv::VerifyArgs a = sampling_args(L, dims, temperature, logits, draft_logits, draft_tokens, uniforms,
-                                         out_tokens, out_num_accepted, out_debug, ws, Pt);
+  sv::VerifyArgs a = sampling_args(L, dims, temperature, logits, draft_logits, draft_tokens, uniforms,
+                                   out_tokens, out_num_accepted, out_debug, ws, Pt);
+  a.ldp = ldz;
   e = sv::launch_verify_sampling(a, s);
   return (e == cudaSuccess && mark(2)) ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -396,6 +400,35 @@ spec_status spec_verify_noalloc_read_error(int32_t* error_word, spec_stream_t st
   st = noalloc_scratch(dev, &scratch);
   if (st != SPEC_OK) return st;
   return spec_verify_read_error(scratch, error_word, stream);
+}
+
+// One draft step = the verify path with no drafts: the LM head on the B
+// draft rows (fused softmax statistics), then the bonus draw from row 0 of
+// each sequence (or the greedy argmax).  The accept counts it also produces
+// (always 0, or -1 for a row with non-finite logits) go to the end of the
+// workspace.
+size_t spec_draft_step_workspace_bytes(spec_dims dims, float temperature) {
+  dims.K = 0;
+  if (!dims_ok(dims, true) || !(temperature >= 0.f) || !std::isfinite(temperature)) return 0;
+  const Layout L = make_layout(dims.B, 0, dims.V, temperature == 0.f, temperature > 0.f, false);
+  return L.total + round_up(sizeof(int32_t) * static_cast<size_t>(dims.B));
+}
+
+spec_status spec_draft_step(const void* hidden, const void* W_lm, const float* uniforms, float temperature,
+                            int32_t* out_tokens, float* out_logits, int64_t ld, spec_dims dims, void* workspace,
+                            size_t workspace_bytes, spec_stream_t stream) {
+  dims.K = 0;
+  if (!dims_ok(dims, true)) return SPEC_ERR_DIMS;
+  if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SPEC_ERR_ARG;
+  const bool greedy = temperature == 0.f;
+  if (greedy && out_logits) return SPEC_ERR_ARG;
+  if (out_logits && ld < dims.V) return SPEC_ERR_ARG;
+  const Layout L = make_layout(dims.B, 0, dims.V, greedy, !greedy && !out_logits, false);
+  const size_t need = L.total + round_up(sizeof(int32_t) * static_cast<size_t>(dims.B));
+  if (!workspace || workspace_bytes < need) return SPEC_ERR_WORKSPACE;
+  int32_t* n_scratch = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + L.total);
+  return verify_impl(hidden, W_lm, nullptr, nullptr, uniforms, temperature, out_tokens, n_scratch, dims, workspace,
+                     L.total, out_logits, nullptr, stream, nullptr, out_logits ? ld : 0);
 }
 
 spec_status spec_lm_head(const void* hidden, const void* W_lm, float* logits, int32_t M, int32_t d, int32_t V,

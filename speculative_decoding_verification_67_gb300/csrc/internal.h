@@ -84,15 +84,18 @@ struct HeadStats {
 // Enqueues the LM head.  Returns cudaSuccess or the first CUDA error;
 // *encode_failed is set when building a TMA descriptor failed.  When
 // zero_err is set, the kernel clears *err before anything can report.
+// `ldz` is the row stride of `logits` in floats (0: V).
 cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, HeadOut mode,
                         float* logits, float* part_max, int* part_idx, const HeadStats* stats, int* err,
-                        bool zero_err, const DeviceInfo& dev, cudaStream_t stream, bool* encode_failed);
+                        bool zero_err, const DeviceInfo& dev, cudaStream_t stream, bool* encode_failed,
+                        long long ldz = 0);
 
 // ------------------------------------------------------------------ verify
 struct VerifyArgs {
   int B, K, V;
   float c_hi, c_lo;         // log2(e) / T as a float pair
-  const float* zp;          // [B*(K+1)][V]
+  const float* zp;          // [B*(K+1)] rows of V, row stride ldp
+  long long ldp;            // row stride of zp in floats (>= V)
   const float* zq;          // [B*K][V]
   const int32_t* x;         // [B][K]
   const float* u;           // [B][K+1]
@@ -114,9 +117,10 @@ void exponent_constant(float temperature, float* c_hi, float* c_lo);
 
 // Softmax partials of given target and draft logits (per row and 4096-token
 // chunk); clears *err first when err is given, and the n_tickets tickets.
+// Target row r starts at zp + r * ldp (ldp 0: V).
 cudaError_t launch_row_stats(const float* zp, const float* zq, int M, int draft_rows, int V, float c_hi, float c_lo,
                              StatPart* tpart, StatPart* dpart, int* err, unsigned* tickets, int n_tickets,
-                             cudaStream_t stream);
+                             cudaStream_t stream, long long ldp = 0);
 
 // Decision and residual draw (one launch, chained with programmatic
 // dependent launch after the statistics).

@@ -63,6 +63,7 @@ struct HeadParams {
   int N, num_chunks, num_vt, num_tiles, num_kb, stages;
   uint32_t tmem_cols;
   float* logits;
+  long long ldz;       // row stride of logits in floats
   float* part_max;
   int* part_idx;
   int* err;
@@ -98,7 +99,7 @@ __device__ __forceinline__ void emit16(const HeadParams& p, const float (&val)[1
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const int m = m0 + c0 + i;
-        if (m < p.M) p.logits[static_cast<size_t>(m) * p.V + v] = val[i];
+        if (m < p.M) p.logits[static_cast<size_t>(m) * p.ldz + v] = val[i];
       }
     }
   }
@@ -533,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < kPrecN; ++i) {
               if (i >= p.M) break;
               const float z = acc[i];
-              p.logits[static_cast<size_t>(i) * p.V + v] = z;
+              p.logits[static_cast<size_t>(i) * p.ldz + v] = z;
               const float h = expo_hi(z, c);
               if (!isfinite(h)) {
                 badmask |= 1ull << i;
@@ -764,7 +765,7 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev) {
 
 cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, HeadOut mode, float* logits,
                         float* part_max, int* part_idx, const HeadStats* stats, int* err, bool zero_err,
-                        const DeviceInfo& dev, cudaStream_t stream, bool* encode_failed) {
+                        const DeviceInfo& dev, cudaStream_t stream, bool* encode_failed, long long ldz) {
   *encode_failed = false;
   const HeadPlan h = plan_head(M, d, V, mode, dev);
   CUtensorMap map_w, map_h;
@@ -786,6 +787,7 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
   p.stages = h.stages;
   p.tmem_cols = h.tmem_cols;
   p.logits = logits;
+  p.ldz = ldz > 0 ? ldz : V;
   p.part_max = part_max;
   p.part_idx = part_idx;
   p.err = err;

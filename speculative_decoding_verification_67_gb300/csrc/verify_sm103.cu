@@ -130,9 +130,9 @@ __device__ __forceinline__ void load16(const float* __restrict__ row, int e0, in
 // merged across the block (exact rescaling), no barrier before the merge.
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) row_stats_kernel(const float* __restrict__ zp,
-                                                             const float* __restrict__ zq, int M, int V, Expo c,
-                                                             StatPart* tpart, StatPart* dpart, int P, int* err,
-                                                             unsigned* tickets, int n_tickets) {
+                                                             const float* __restrict__ zq, int M, int V,
+                                                             long long ldp, Expo c, StatPart* tpart, StatPart* dpart,
+                                                             int P, int* err, unsigned* tickets, int n_tickets) {
   __shared__ Partial sm[kWarps];
   const int row = blockIdx.x, chunk = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(const float* __rest
     for (int i = threadIdx.x; i < n_tickets; i += kThreads) tickets[i] = 0u;
   }
   const bool target = row < M;
-  const float* z = target ? zp + static_cast<size_t>(row) * V : zq + static_cast<size_t>(row - M) * V;
+  const float* z = target ? zp + static_cast<size_t>(row) * ldp : zq + static_cast<size_t>(row - M) * V;
   float v[kPer];
   unsigned valid;
   load16<kVec>(z, chunk * kChunk + threadIdx.x * kPer, V, v, valid);
@@ -232,7 +232,7 @@ __device__ void decide(const VerifyArgs& a, int b, DecideSmem& ds) {
   float zpx = 0.f;
   if (warp == kWarps - 1 && lane < K) {
     const int xj = ds.xj[lane];
-    if (xj >= 0 && xj < a.V) zpx = __ldcg(&a.zp[static_cast<size_t>(b * (K + 1) + lane) * a.V + xj]);
+    if (xj >= 0 && xj < a.V) zpx = __ldcg(&a.zp[static_cast<size_t>(b * (K + 1) + lane) * a.ldp + xj]);
   }
   for (int r = warp; r < nrows; r += kWarps) {
     const StatPart* pp = r <= K ? a.tpart + static_cast<size_t>(b * (K + 1) + r) * a.Pt
@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyArgs a) {
   const int n = d.n;
   ResRow R;
   R.rej = n < K;
-  R.zp = a.zp + static_cast<size_t>(b * (K + 1) + n) * a.V;
+  R.zp = a.zp + static_cast<size_t>(b * (K + 1) + n) * a.ldp;
   R.zq = R.rej ? a.zq + static_cast<size_t>(b * K + n) * a.V : nullptr;
   R.c = {a.c_hi, a.c_lo};
   R.k_p = d.k_p;
@@ -771,20 +771,26 @@ void exponent_constant(float temperature, float* c_hi, float* c_lo) {
 
 cudaError_t launch_row_stats(const float* zp, const float* zq, int M, int draft_rows, int V, float c_hi, float c_lo,
                              StatPart* tpart, StatPart* dpart, int* err, unsigned* tickets, int n_tickets,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, long long ldp) {
   const int P = (V + kChunk - 1) / kChunk;
   const dim3 g(M + draft_rows, P);
   const Expo c{c_hi, c_lo};
-  if (V % 4 == 0)
-    row_stats_kernel<true><<<g, kThreads, 0, stream>>>(zp, zq, M, V, c, tpart, dpart, P, err, tickets, n_tickets);
+  if (ldp <= 0) ldp = V;
+  if (V % 4 == 0 && ldp % 4 == 0 && (reinterpret_cast<uintptr_t>(zp) & 15u) == 0 &&
+      (reinterpret_cast<uintptr_t>(zq) & 15u) == 0)
+    row_stats_kernel<true><<<g, kThreads, 0, stream>>>(zp, zq, M, V, ldp, c, tpart, dpart, P, err, tickets,
+                                                       n_tickets);
   else
-    row_stats_kernel<false><<<g, kThreads, 0, stream>>>(zp, zq, M, V, c, tpart, dpart, P, err, tickets, n_tickets);
+    row_stats_kernel<false><<<g, kThreads, 0, stream>>>(zp, zq, M, V, ldp, c, tpart, dpart, P, err, tickets,
+                                                        n_tickets);
   return cudaGetLastError();
 }
 
 cudaError_t launch_verify_sampling(const VerifyArgs& a, cudaStream_t stream) {
   const dim3 g(a.B, a.CB);
-  if (a.V % 4 == 0) return launch_dependent(finish_kernel<true>, g, dim3(kThreads), stream, a);
+  // 16-byte loads need every target row 16-byte aligned
+  const bool vec = a.V % 4 == 0 && a.ldp % 4 == 0 && (reinterpret_cast<uintptr_t>(a.zp) & 15u) == 0;
+  if (vec) return launch_dependent(finish_kernel<true>, g, dim3(kThreads), stream, a);
   return launch_dependent(finish_kernel<false>, g, dim3(kThreads), stream, a);
 }
 

@@ -317,3 +317,35 @@ def make_ngram_inputs(w: NgramWorkload, device="cpu", seed: int | None = None) -
         row = torch.cat(out)[:L]
         hist[b, :L] = perm[row]
     return dict(history=hist.to(torch.int32).to(device), lengths=lens.to(torch.int32).to(device))
+
+
+# ---------------------------------------------------------------------------
+# Drafter that reuses the target's LM head (EAGLE-style): the draft model's
+# estimate h-hat of the target's hidden state at slot j is a noisy copy of
+# it, h_hat[j][b] = bf16(h[b, j] + noise * eps); the draft logits of slot j
+# are h_hat[j] through the same bf16 LM-head weight.  Uniforms: one per
+# (draft step, sequence) for the draft draws, and the verify step's [B][K+1].
+# ---------------------------------------------------------------------------
+DRAFT_WORKLOADS = {
+    w.name: w
+    for w in (
+        Workload("draft_B8_K4_V128256", B=8, K=4, d=4096, V=128256, temperature=0.8, noise=0.3, seed=6731),
+        Workload("draft_B64_K4_V128256", B=64, K=4, d=4096, V=128256, temperature=0.8, noise=0.3, seed=6732),
+    )
+}
+
+
+def make_draft_inputs(w: Workload, device="cpu", seed: int | None = None) -> dict:
+    """hidden bf16 [B*(K+1), d] (target), W bf16 [V, d], draft_hidden bf16
+    [K, B, d], draft_uniforms f32 [K, B], uniforms f32 [B, K+1]."""
+    device = torch.device(device)
+    g = _gen(device, w.seed if seed is None else seed)
+    B, K, d, V = w.B, w.K, w.d, w.V
+    h = _randn_bf16((B * (K + 1), d), 1.0, g, device)
+    W = _randn_bf16((V, d), 1.0 / math.sqrt(d), g, device)
+    hk = h.view(B, K + 1, d)[:, :K, :].float().permute(1, 0, 2)          # [K, B, d]
+    eps = _randn((K * B, d), g, device).view(K, B, d)
+    draft_hidden = (hk + w.noise * eps).to(torch.bfloat16).contiguous()
+    draft_uniforms = torch.rand((K, B), generator=g, device=device, dtype=torch.float32)
+    uniforms = torch.rand((B, K + 1), generator=g, device=device, dtype=torch.float32)
+    return dict(hidden=h, W=W, draft_hidden=draft_hidden, draft_uniforms=draft_uniforms, uniforms=uniforms)

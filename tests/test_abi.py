@@ -137,3 +137,23 @@ def test_ngram_host_side_errors(lib):
     assert call(h=_fake(0x10004)) == 3
     assert call(oc=_fake(0x10002)) == 3
     assert call(size=nws - 1) == 4
+
+
+def test_draft_step_host_side_errors(lib):
+    good = _fake(0x10000)
+    d = sv.SpecDims(4, 0, 512, 5000)
+    nws = lib.spec_draft_step_workspace_bytes(d, 0.8)
+    assert nws > 0 and lib.spec_draft_step_workspace_bytes(d, -1.0) == 0
+    assert lib.spec_draft_step_workspace_bytes(sv.SpecDims(4, 0, 500, 5000), 0.8) == 0   # d % 8
+
+    def call(h=good, W=good, u=good, T=0.8, ot=good, ol=good, ld=5000, dims=d, ws=good, size=nws):
+        return lib.spec_draft_step(h, W, u, T, ot, ol, ld, dims, ws, size, _fake(None))
+
+    assert call(h=_fake(None)) == 1
+    assert call(u=_fake(None)) == 1                 # sampling needs uniforms
+    assert call(T=0.0) == 1                         # greedy never writes logits
+    assert call(ld=4999) == 1
+    assert call(T=float("nan")) == 1
+    assert call(dims=sv.SpecDims(0, 0, 512, 5000)) == 2
+    assert call(h=_fake(0x10008)) == 3
+    assert call(ol=_fake(None), size=nws - 1) == 4   # logits kept in the workspace
