@@ -1,7 +1,7 @@
 """Benchmark of the verify-and-accept step on GB300.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
-               [--row verify|kv_commit|ngram|draft]
+               [--row verify|kv_commit|ngram|draft|tree]
 
 A step is one call of the whole step (LM head, softmax statistics, accept
 test, accepted prefix, residual / bonus draw) on one batch of the workload,
@@ -21,7 +21,9 @@ paged cache, KV workloads of synth.KV_WORKLOADS; value = kept entry bytes
 read and written per second).  --row ngram measures the prompt-lookup
 drafter (spec_ngram_propose; value = history tokens searched per second).
 --row draft measures one draft step through the target's LM head
-(spec_draft_step; value = draft tokens per second).
+(spec_draft_step; value = draft tokens per second).  --row tree measures
+tree-shaped candidate verification (spec_tree_verify; value = verified tree
+nodes per second).
 
 With N > 1 (torchrun) every rank runs its own copy of the workload (the
 sequences of different ranks are independent problems): weak scaling, no
@@ -661,6 +663,129 @@ def run_draft_reference(args):
     print(json.dumps(line), flush=True)
 
 
+
+# -------------------------------------------------------------- tree verify
+TREE_METRIC = "verified tree nodes/sec (tree-shaped candidates, V=128256)"
+
+
+def run_tree(args):
+    """One tree verification per step: the LM head over every node's hidden
+    state (logits), then the cluster walk (sampling) or the argmax walk."""
+    import speculative_decoding_verification_67_gb300 as sv
+
+    w = synth.TREE_WORKLOADS[args.tree_workload]
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    inp = synth.make_tree_inputs(w, device=dev, seed=w.seed + rank)
+    B, N, d, V, T = w.B, w.N, w.d, w.V, w.temperature
+    M = B * N
+    stream = torch.cuda.current_stream(dev)
+    ws = torch.empty(sv.tree_workspace_bytes(B, N, V, T), dtype=torch.uint8, device=dev)
+    outs = (torch.empty((B, N), dtype=torch.int32, device=dev), torch.empty((B, N), dtype=torch.int32, device=dev),
+            torch.empty((B,), dtype=torch.int32, device=dev))
+
+    def step(hidden=inp["hidden"], tok=inp["tokens"], par=inp["parents"], u=inp["uniforms"]):
+        sv.spec_tree_verify(hidden, inp["W"], inp["draft_logits"], tok, par, u, T, out_tokens=outs[0],
+                            out_path=outs[1], out_num_accepted=outs[2], workspace=ws, stream=stream)
+
+    peak_gbs, _, _, peak_kind = load_peaks()
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    value, ms = job_throughput(e0.elapsed_time(e1), world, M, args.steps)
+    ms_per_step = ms / args.steps
+    n = outs[2].cpu()
+    visited = int((n.clamp_min(0) + 1).sum())
+    # W once, hidden once, logits written once; the walk reads the target and
+    # draft rows of the nodes it visits
+    nbytes = 2 * V * d + 2 * M * d + 4 * M * V + 2 * 4 * V * visited
+    gbs = nbytes / (ms_per_step * 1e-3) / 1e9
+
+    # end to end: hidden states, tokens, parents, uniforms in from pinned host
+    # memory (the draft logits stay resident), the outputs back
+    host = {k: inp[k].cpu().pin_memory() for k in ("hidden", "tokens", "parents", "uniforms")}
+    dev_in = {k: torch.empty_like(inp[k]) for k in host}
+    out_host = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    e2e_steps = max(10, min(args.steps, 300))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        for k in host:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        step(dev_in["hidden"], dev_in["tokens"], dev_in["parents"], dev_in["uniforms"])
+        for o, oh in zip(outs, out_host):
+            oh.copy_(o, non_blocking=True)
+        torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    h2d = 2 * M * d + 3 * 4 * M
+    e2e = {"value": world * M * e2e_steps / e2e_s, "unit": "verified tree nodes/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": 4 * (2 * M + B), "steps": e2e_steps, "ms_per_step": 1e3 * e2e_s / e2e_steps,
+           "timer": "host wall clock: H2D hidden/tokens/parents/uniforms, spec_tree_verify, D2H outputs"}
+    line = {
+        "metric": TREE_METRIC, "value": value, "unit": "verified tree nodes/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "N": N, "branching": list(w.branching), "d": d, "V": V, "T": T,
+                   "mean_accepted": float(n.float().mean()),
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": f"inputs exceed L2: W_lm {2 * V * d / 1e9:.2f} GB is streamed every step"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs,
+                     "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "head_kernel + tree_sample_kernel (the whole step, both launches)",
+                     "bytes_per_launch": nbytes, "launch_ms": ms_per_step},
+        "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = tree_cpu_baseline(w, inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def tree_cpu_baseline(w, inp, budget_s: float = 12.0) -> dict:
+    """The oracle (fp64 LM head of one sequence's N rows over a vocabulary
+    slice, scaled to the full head; the walk itself is negligible next to it)."""
+    from oracle import spec_oracle
+    h = inp["hidden"][: w.N].double().cpu().numpy()
+    Vs = 4096
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < budget_s and (n + 1) * Vs <= w.V:
+        spec_oracle.lm_head(h, inp["W"][n * Vs:(n + 1) * Vs].double().cpu().numpy())
+        n += 1
+    dt = time.perf_counter() - t0
+    per_seq = dt * (w.V / (n * Vs))
+    return {"value": w.N / per_seq, "unit": "verified tree nodes/s", "cores": torch.get_num_threads(),
+            "kind": "oracle", "sample": f"one tree ({w.N} rows), {n * Vs} of {w.V} vocabulary rows, scaled"}
+
+
+def run_tree_reference(args):
+    w = synth.TREE_WORKLOADS[args.tree_workload]
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    inp = synth.make_tree_inputs(w)
+    base = tree_cpu_baseline(w, inp, budget_s=min(60.0, 5.0 * max(1, args.steps)))
+    line = {"impl": "reference", "metric": TREE_METRIC, "value": base["value"], "unit": "verified tree nodes/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+            "dtype": "f64", "data": "synthetic", "config": {"workload": w.name}, "cpu_baseline": base,
+            "e2e": {"value": base["value"], "unit": "verified tree nodes/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -669,10 +794,11 @@ def main():
     ap.add_argument("--workload", default="head_B8_K4_V128256", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--row", default="verify", choices=["verify", "kv_commit", "ngram", "draft"])
+    ap.add_argument("--row", default="verify", choices=["verify", "kv_commit", "ngram", "draft", "tree"])
     ap.add_argument("--kv-workload", default="kv_B64_K8_L80_E4096", choices=sorted(synth.KV_WORKLOADS))
     ap.add_argument("--ngram-workload", default="ngram_B256_L32768_K8", choices=sorted(synth.NGRAM_WORKLOADS))
     ap.add_argument("--draft-workload", default="draft_B8_K4_V128256", choices=sorted(synth.DRAFT_WORKLOADS))
+    ap.add_argument("--tree-workload", default="tree_B8_N16_V128256", choices=sorted(synth.TREE_WORKLOADS))
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.row == "kv_commit":
@@ -680,6 +806,10 @@ def main():
             return run_kv_reference(args)
         args.steps = min(args.steps, 500)
         return run_kv_commit(args)
+    if args.row == "tree":
+        if args.impl == "reference":
+            return run_tree_reference(args)
+        return run_tree(args)
     if args.row == "draft":
         if args.impl == "reference":
             return run_draft_reference(args)

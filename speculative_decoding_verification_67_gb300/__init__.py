@@ -17,7 +17,9 @@ Names follow the C ABI:
   (``include/spec_kv_commit.h``);
 * :func:`spec_ngram_propose` -- prompt-lookup drafts (``include/spec_ngram.h``);
 * :func:`spec_draft_step` -- one draft step through the target's LM head
-  (``include/spec_draft.h``).
+  (``include/spec_draft.h``);
+* :func:`spec_tree_verify` / :func:`spec_tree_verify_from_logits` -- tree-shaped
+  candidates (``include/spec_tree.h``).
 """
 from __future__ import annotations
 
@@ -33,6 +35,7 @@ __all__ = [
     "kv_workspace", "spec_kv_commit", "kv_commit_read_error",
     "ngram_workspace", "spec_ngram_propose", "ngram_read_error",
     "draft_step_workspace_bytes", "spec_draft_step",
+    "tree_workspace_bytes", "spec_tree_verify", "spec_tree_verify_from_logits",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspec_verify.so")
@@ -53,6 +56,10 @@ class SpecKvDims(ctypes.Structure):
 class SpecNgramDims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("max_len", ctypes.c_int32), ("K", ctypes.c_int32),
                 ("n_min", ctypes.c_int32), ("n_max", ctypes.c_int32)]
+
+
+class SpecTreeDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("N", ctypes.c_int32), ("d", ctypes.c_int32), ("V", ctypes.c_int32)]
 
 
 class SpecError(RuntimeError):
@@ -83,6 +90,11 @@ _SIGS = {
     "spec_kv_commit_read_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32), _VP]),
     "spec_ngram_workspace_bytes": (_SZ, [SpecNgramDims]),
     "spec_draft_step_workspace_bytes": (_SZ, [SpecDims, _F32]),
+    "spec_tree_workspace_bytes": (_SZ, [SpecTreeDims, _F32, _I32]),
+    "spec_tree_verify": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _F32, _VP, _VP, _VP, SpecTreeDims, _VP, _SZ,
+                                        _VP, _VP]),
+    "spec_tree_verify_from_logits": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _F32, _VP, _VP, _VP, SpecTreeDims, _VP,
+                                                    _SZ, _VP]),
     "spec_draft_step": (ctypes.c_int, [_VP, _VP, _VP, _F32, _VP, _VP, ctypes.c_int64, SpecDims, _VP, _SZ, _VP]),
     "spec_ngram_propose": (ctypes.c_int, [_VP, _VP, _VP, _VP, SpecNgramDims, _VP, _SZ, _VP]),
     "spec_ngram_read_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32), _VP]),
@@ -477,3 +489,78 @@ def spec_draft_step(hidden, W_lm, uniforms, temperature: float, *, out_tokens=No
                                      _ptr(out_tokens), _ptr(out_logits), ld, SpecDims(B, 0, d, V),
                                      _ptr(workspace), workspace.numel(), _stream(stream)))
     return out_tokens, out_logits
+
+
+# --------------------------------------------------------------- tree verify
+def tree_workspace_bytes(B: int, N: int, V: int, temperature: float, logits_in_workspace: bool = True) -> int:
+    n = library().spec_tree_workspace_bytes(SpecTreeDims(B, N, 0, V), float(temperature), int(logits_in_workspace))
+    if n == 0:
+        raise ValueError("invalid sizes")
+    return int(n)
+
+
+def _tree_outputs(B, N, device, out_tokens, out_path, out_num_accepted):
+    if out_tokens is None:
+        out_tokens = torch.empty((B, N), dtype=torch.int32, device=device)
+    if out_path is None:
+        out_path = torch.empty((B, N), dtype=torch.int32, device=device)
+    if out_num_accepted is None:
+        out_num_accepted = torch.empty((B,), dtype=torch.int32, device=device)
+    _need(out_tokens, "out_tokens", torch.int32, (B, N), "cuda")
+    _need(out_path, "out_path", torch.int32, (B, N), "cuda")
+    _need(out_num_accepted, "out_num_accepted", torch.int32, (B,), "cuda")
+    return out_tokens, out_path, out_num_accepted
+
+
+def _tree_inputs(tokens, parents, uniforms, draft_logits, B, N, V, T):
+    _need(tokens, "tokens", torch.int32, (B, N), "cuda")
+    _need(parents, "parents", torch.int32, (B, N), "cuda")
+    if T > 0:
+        _need(uniforms, "uniforms", torch.float32, (B, N), "cuda")
+        _need(draft_logits, "draft_logits", torch.float32, (B * N, V), "cuda")
+
+
+def spec_tree_verify(hidden, W_lm, draft_logits, tokens, parents, uniforms, temperature: float, *, out_tokens=None,
+                     out_path=None, out_num_accepted=None, workspace=None, out_target_logits=None, stream=None):
+    """Tree verification from every node's hidden state: ``hidden`` bf16
+    [B*N, d], ``W_lm`` bf16 [V, d], ``draft_logits`` f32 [B*N, V] (T > 0),
+    ``tokens`` / ``parents`` int32 [B, N], ``uniforms`` f32 [B, N] (T > 0).
+    Returns (tokens, path, num_accepted)."""
+    B, N = tokens.shape
+    M, d = hidden.shape
+    V = W_lm.shape[0]
+    T = float(temperature)
+    _need(hidden, "hidden", torch.bfloat16, (B * N, d), "cuda")
+    _need(W_lm, "W_lm", torch.bfloat16, (V, d), "cuda")
+    _tree_inputs(tokens, parents, uniforms, draft_logits, B, N, V, T)
+    outs = _tree_outputs(B, N, hidden.device, out_tokens, out_path, out_num_accepted)
+    if out_target_logits is not None:
+        _need(out_target_logits, "out_target_logits", torch.float32, (B * N, V), "cuda")
+    if workspace is None:
+        workspace = torch.empty(tree_workspace_bytes(B, N, V, T, out_target_logits is None), dtype=torch.uint8,
+                                device=hidden.device)
+    _check(library().spec_tree_verify(
+        _ptr(hidden), _ptr(W_lm), _ptr(draft_logits if T > 0 else None), _ptr(tokens), _ptr(parents),
+        _ptr(uniforms if T > 0 else None), T, _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]),
+        SpecTreeDims(B, N, d, V), _ptr(workspace), workspace.numel(), _ptr(out_target_logits), _stream(stream)))
+    return outs
+
+
+def spec_tree_verify_from_logits(target_logits, draft_logits, tokens, parents, uniforms, temperature: float, *,
+                                 out_tokens=None, out_path=None, out_num_accepted=None, workspace=None, stream=None):
+    """Tree verification on given target logits f32 [B*N, V]."""
+    B, N = tokens.shape
+    V = target_logits.shape[1]
+    T = float(temperature)
+    _need(target_logits, "target_logits", torch.float32, (B * N, V), "cuda")
+    _tree_inputs(tokens, parents, uniforms, draft_logits, B, N, V, T)
+    outs = _tree_outputs(B, N, target_logits.device, out_tokens, out_path, out_num_accepted)
+    if workspace is None:
+        # (sized for the LM-head path, which holds more partials than this one)
+        workspace = torch.empty(tree_workspace_bytes(B, N, V, T, False), dtype=torch.uint8,
+                                device=target_logits.device)
+    _check(library().spec_tree_verify_from_logits(
+        _ptr(target_logits), _ptr(draft_logits if T > 0 else None), _ptr(tokens), _ptr(parents),
+        _ptr(uniforms if T > 0 else None), T, _ptr(outs[0]), _ptr(outs[1]), _ptr(outs[2]), SpecTreeDims(B, N, 0, V),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return outs

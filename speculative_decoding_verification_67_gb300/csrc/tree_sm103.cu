@@ -1,0 +1,846 @@
+// Tree-shaped candidate verification ("Speculative Decoding: Memverifikasi
+// Token Draft secara Paralel", section "Sampling eksak memerlukan aturan
+// koreksi").  Declared in include/spec_tree.h.
+//
+// Sampling: one thread-block cluster of kTC CTAs per sequence.  CTA r owns
+// the vocabulary slice [r*S, (r+1)*S) and keeps the current node's target and
+// draft rows of that slice in shared memory, as probabilities.  Every
+// reduction of the walk -- a node's two softmax normalisers, the residual
+// mass after a rejection, the slice masses of the final draw -- is a block
+// reduction followed by an exchange of one value per CTA through distributed
+// shared memory; every CTA merges the kTC values in rank order, so all of
+// them reach the same decisions and walk the tree in lockstep.  A rejection
+// costs one pass over shared memory and one cluster barrier; the rows of a
+// node are read from HBM / L2 once, when the walk reaches it.
+//
+// The residual after k rejections against the same draft row q is
+// max(0, p - lambda_k q) / S'_k with lambda_1 = 1, lambda_{k+1} =
+// lambda_k + S'_k and S'_k = sum(max(0, p - lambda_k q)): one scalar per
+// rejection instead of a rewritten row.
+//
+// Greedy: one CTA per sequence reduces the LM head's per-tile argmax
+// partials of the rows it visits.
+#include <climits>
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+#include "sm103_ptx.cuh"
+#include "spec_tree.h"
+#include "verify_math.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kTC = 8;            // CTAs per cluster (one cluster per sequence)
+constexpr int kTT = 512;          // threads per CTA
+constexpr int kTW = kTT / 32;
+constexpr int kMaxSlice = 24576;  // vocabulary entries per CTA
+constexpr int kMaxNodes = 256;
+
+struct TreeArgs {
+  int B, N, V, S;
+  int bulk;  // rows start on 16-byte boundaries (V % 4 == 0): node rows come in by TMA bulk copies
+  float c_hi, c_lo;
+  const float* zp;  // [B*N][V]
+  const float* zq;  // [B*N][V]
+  const int32_t* tok;
+  const int32_t* par;
+  const float* u;
+  int32_t* out_tok;
+  int32_t* out_path;
+  int32_t* out_n;
+  int* err;
+  const float* pmax;  // greedy: [B*N][P]
+  const int* pidx;
+  int P;
+};
+
+struct TreeShared {
+  float4 ex[2][2];  // cluster exchange slots [pass parity][value]
+  int par[kMaxNodes];
+  int tok[kMaxNodes];
+  int path[kMaxNodes];
+  float wk[kTW], wsh[kTW];
+  ff scan[kTW];
+  int si[2 * kTW];
+  float4 res;  // broadcast of a block or cluster reduction
+  int res_i;
+  ff pre[kTC + 1];
+  float zs[kTC];
+  int flag;
+  uint64_t bar;  // completion of the node-row bulk copies
+};
+
+__device__ ff block_sum(ff v, TreeShared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum_ff(v);
+  if (lane == 0) sh.scan[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    ff w = lane < kTW ? sh.scan[lane] : ff{0.f, 0.f};
+    w = warp_sum_ff(w);
+    if (lane == 0) sh.res = make_float4(w.hi, w.lo, 0.f, 0.f);
+  }
+  __syncthreads();
+  return ff{sh.res.x, sh.res.y};
+}
+
+__device__ int block_max_i(int v, TreeShared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, off));
+  if (lane == 0) sh.si[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kTW ? sh.si[lane] : INT_MIN;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) w = max(w, __shfl_xor_sync(0xffffffffu, w, off));
+    if (lane == 0) sh.res_i = w;
+  }
+  __syncthreads();
+  return sh.res_i;
+}
+
+// Publishes two values of this CTA for the current pass; after the cluster
+// barrier every CTA's values of the pass are readable.
+__device__ __forceinline__ void publish(TreeShared& sh, int ph, float4 a, float4 b) {
+  if (threadIdx.x == 0) {
+    sh.ex[ph][0] = a;
+    sh.ex[ph][1] = b;
+  }
+  cluster_sync();
+}
+
+__device__ __forceinline__ float4 fetch(TreeShared& sh, int ph, int which, int rank) {
+  return ld_cluster_f4(cluster_map(&sh.ex[ph][which], static_cast<uint32_t>(rank)));
+}
+
+__device__ ff cluster_sum_ff(TreeShared& sh, int ph) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    ff v = {0.f, 0.f};
+    if (lane < kTC) {
+      const float4 f = fetch(sh, ph, 0, lane);
+      v = ff{f.x, f.y};
+    }
+    v = warp_sum_ff(v);
+    if (lane == 0) sh.res = make_float4(v.hi, v.lo, 0.f, 0.f);
+  }
+  __syncthreads();
+  const ff r = {sh.res.x, sh.res.y};
+  __syncthreads();
+  return r;
+}
+
+// Inclusive prefix over ranks of the pass's published float pairs (x, y of
+// value 0); lane r of warp 0 holds rank r's.  Returns the prefix ending at
+// `rank` in pre_end and the total.
+__device__ void cluster_scan_ff(TreeShared& sh, int ph, ff* pre /*[kTC + 1]*/, float* zs /*[kTC]*/) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    float4 v = lane < kTC ? fetch(sh, ph, 0, lane) : make_float4(0.f, 0.f, -1.f, 0.f);
+    ff incl = {v.x, v.y};
+#pragma unroll
+    for (int off = 1; off < kTC; off <<= 1) {
+      const ff o{__shfl_up_sync(0xffffffffu, incl.hi, off), __shfl_up_sync(0xffffffffu, incl.lo, off)};
+      if (lane >= off) incl = ff_add(o, incl);
+    }
+    if (lane < kTC) {
+      sh.pre[lane + 1] = incl;
+      sh.zs[lane] = v.z;
+    }
+    if (lane == 0) sh.pre[0] = ff{0.f, 0.f};
+  }
+  __syncthreads();
+  for (int r = 0; r <= kTC; ++r) pre[r] = sh.pre[r];
+  for (int r = 0; r < kTC; ++r) zs[r] = sh.zs[r];
+  __syncthreads();
+}
+
+struct NodeStats {
+  float kp, inv_p, kq, inv_q;
+  int bad;
+};
+
+// Cluster-wide max of two values (and OR of two flags) published as
+// (mx_p, mx_q, bad_p, bad_q) by every CTA.
+__device__ float4 cluster_max2(TreeShared& sh, int ph) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    float4 v = lane < kTC ? fetch(sh, ph, 0, lane) : make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      v.x = fmaxf(v.x, __shfl_xor_sync(0xffffffffu, v.x, off));
+      v.y = fmaxf(v.y, __shfl_xor_sync(0xffffffffu, v.y, off));
+      v.z = fmaxf(v.z, __shfl_xor_sync(0xffffffffu, v.z, off));
+      v.w = fmaxf(v.w, __shfl_xor_sync(0xffffffffu, v.w, off));
+    }
+    if (lane == 0) sh.res = v;
+  }
+  __syncthreads();
+  const float4 r = sh.res;
+  __syncthreads();
+  return r;
+}
+
+__device__ float block_max_f(float v, TreeShared& sh, int slot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_max_f(v);
+  if (lane == 0) sh.wk[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    float w = lane < kTW ? sh.wk[lane] : -INFINITY;
+    w = warp_max_f(w);
+    if (lane == 0) sh.wsh[slot] = w;
+  }
+  __syncthreads();
+  return sh.wsh[slot];
+}
+
+// Sum of two ff values per thread over the cluster (after block sums):
+// returns (sum_a, sum_b).
+__device__ void cluster_sum2(TreeShared& sh, int ph, ff& a, ff& b) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    float4 f = lane < kTC ? fetch(sh, ph, 0, lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    ff x = {f.x, f.y}, y = {f.z, f.w};
+    x = warp_sum_ff(x);
+    y = warp_sum_ff(y);
+    if (lane == 0) sh.res = make_float4(x.hi, x.lo, y.hi, y.lo);
+  }
+  __syncthreads();
+  a = ff{sh.res.x, sh.res.y};
+  b = ff{sh.res.z, sh.res.w};
+  __syncthreads();
+}
+
+// Loads node `node`'s target row (and draft row if need_q) of this CTA's
+// slice into shared memory as 2^(z*c - k) against the cluster-wide reference
+// k of the row (p_v = sp[v] * inv_p); a non-finite logit, or a row without
+// mass, marks the node bad in every CTA.
+__device__ NodeStats load_node(const TreeArgs& a, TreeShared& sh, float* sp, float* sq, int b, int node, bool need_q,
+                               int rank, int& ph, uint32_t& bar_phase, Expo c) {
+  const int base = rank * a.S;
+  const int cnt = max(0, min(a.S, a.V - base));
+  const size_t row = (static_cast<size_t>(b) * a.N + node) * a.V + base;
+  int bad_p = 0, bad_q = 0;
+  if (a.bulk) {
+    // the slice of both rows by TMA; every thread of the CTA finished with the
+    // previous node's rows at the cluster barrier that ended its last pass
+    if (cnt > 0) {
+      if (threadIdx.x == 0) {
+        const uint32_t bytes = static_cast<uint32_t>(cnt) * 4u;
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&sh.bar, need_q ? 2u * bytes : bytes);
+        bulk_load(sp, a.zp + row, bytes, &sh.bar);
+        if (need_q) bulk_load(sq, a.zq + row, bytes, &sh.bar);
+      }
+      if (!mbar_wait(&sh.bar, bar_phase)) {
+        bad_p = 1;  // reported through the cluster exchange, so every CTA sees it
+        if (threadIdx.x == 0) atomicOr(a.err, kErrTimeout);
+        (void)mbar_wait(&sh.bar, bar_phase);  // one more bounded wait for the copies in flight
+      }
+      bar_phase ^= 1u;
+    }
+  } else {
+    for (int i = threadIdx.x; i < cnt; i += kTT) {
+      sp[i] = __ldcg(a.zp + row + i);
+      if (need_q) sq[i] = __ldcg(a.zq + row + i);
+    }
+  }
+  __syncthreads();
+  // pass 1: largest exponent of each row (cnt is a multiple of 4 with bulk rows)
+  float mp = -INFINITY, mq = -INFINITY;
+  if (!bad_p) {
+    const int c4 = a.bulk ? cnt / 4 : 0;
+    for (int i = threadIdx.x; i < c4; i += kTT) {
+      const float4 z = reinterpret_cast<const float4*>(sp)[i];
+      const float h0 = expo_hi(z.x, c), h1 = expo_hi(z.y, c), h2 = expo_hi(z.z, c), h3 = expo_hi(z.w, c);
+      if (!(isfinite(h0) && isfinite(h1) && isfinite(h2) && isfinite(h3))) bad_p = 1;
+      mp = fmaxf(mp, fmaxf(fmaxf(h0, h1), fmaxf(h2, h3)));
+      if (need_q) {
+        const float4 w = reinterpret_cast<const float4*>(sq)[i];
+        const float g0 = expo_hi(w.x, c), g1 = expo_hi(w.y, c), g2 = expo_hi(w.z, c), g3 = expo_hi(w.w, c);
+        if (!(isfinite(g0) && isfinite(g1) && isfinite(g2) && isfinite(g3))) bad_q = 1;
+        mq = fmaxf(mq, fmaxf(fmaxf(g0, g1), fmaxf(g2, g3)));
+      }
+    }
+    for (int i = 4 * c4 + threadIdx.x; i < cnt; i += kTT) {
+      const float h = expo_hi(sp[i], c);
+      if (!isfinite(h)) bad_p = 1; else mp = fmaxf(mp, h);
+      if (need_q) {
+        const float g = expo_hi(sq[i], c);
+        if (!isfinite(g)) bad_q = 1; else mq = fmaxf(mq, g);
+      }
+    }
+  }
+  mp = block_max_f(mp, sh, 0);
+  mq = block_max_f(mq, sh, 1);
+  const int bp = __syncthreads_or(bad_p), bq = __syncthreads_or(bad_q);
+  publish(sh, ph, make_float4(mp, mq, static_cast<float>(bp), static_cast<float>(bq)), make_float4(0.f, 0.f, 0.f, 0.f));
+  const float4 gm = cluster_max2(sh, ph);
+  ph ^= 1;
+  NodeStats st;
+  st.bad = gm.z != 0.f || gm.x == -INFINITY || (need_q && (gm.w != 0.f || gm.y == -INFINITY));
+  st.kp = st.bad ? 0.f : ceilf(gm.x);
+  st.kq = (st.bad || !need_q) ? 0.f : ceilf(gm.y);
+  st.inv_p = st.inv_q = 0.f;
+  if (st.bad) return st;
+  // pass 2: 2^(z*c - k) in place and the slice sums
+  float ph_ = 0.f, pl = 0.f, qh = 0.f, ql = 0.f;
+  {
+    const int c4 = a.bulk ? cnt / 4 : 0;
+    for (int i = threadIdx.x; i < c4; i += kTT) {
+      float4 z = reinterpret_cast<const float4*>(sp)[i];
+      z.x = pow2_rel(z.x, c, st.kp);
+      z.y = pow2_rel(z.y, c, st.kp);
+      z.z = pow2_rel(z.z, c, st.kp);
+      z.w = pow2_rel(z.w, c, st.kp);
+      reinterpret_cast<float4*>(sp)[i] = z;
+      ff_accumulate(ph_, pl, (z.x + z.y) + (z.z + z.w));
+      if (need_q) {
+        float4 w = reinterpret_cast<const float4*>(sq)[i];
+        w.x = pow2_rel(w.x, c, st.kq);
+        w.y = pow2_rel(w.y, c, st.kq);
+        w.z = pow2_rel(w.z, c, st.kq);
+        w.w = pow2_rel(w.w, c, st.kq);
+        reinterpret_cast<float4*>(sq)[i] = w;
+        ff_accumulate(qh, ql, (w.x + w.y) + (w.z + w.w));
+      }
+    }
+    for (int i = 4 * c4 + threadIdx.x; i < cnt; i += kTT) {
+      const float e = pow2_rel(sp[i], c, st.kp);
+      sp[i] = e;
+      ff_accumulate(ph_, pl, e);
+      if (need_q) {
+        const float f = pow2_rel(sq[i], c, st.kq);
+        sq[i] = f;
+        ff_accumulate(qh, ql, f);
+      }
+    }
+  }
+  const ff sp_sum = block_sum(ff_norm(ph_, pl), sh);
+  const ff sq_sum = block_sum(ff_norm(qh, ql), sh);
+  publish(sh, ph, make_float4(sp_sum.hi, sp_sum.lo, sq_sum.hi, sq_sum.lo), make_float4(0.f, 0.f, 0.f, 0.f));
+  ff Sp, Sq;
+  cluster_sum2(sh, ph, Sp, Sq);
+  ph ^= 1;
+  st.inv_p = 1.f / (Sp.hi + Sp.lo);
+  st.inv_q = need_q ? 1.f / (Sq.hi + Sq.lo) : 0.f;
+  return st;
+}
+
+// r_v = max(0, p_v - lam q_v) (lam = 0: p_v), p_v = sp[v]*ip, q_v = sq[v]*iq.
+__device__ __forceinline__ float rval(float e_p, float e_q, float ip, float iq, float lam) {
+  return lam > 0.f ? fmaxf(0.f, e_p * ip - lam * (e_q * iq)) : e_p * ip;
+}
+
+// Mass of max(0, p - lam q) over the whole row.
+__device__ ff residual_mass(const TreeArgs& a, TreeShared& sh, const float* sp, const float* sq, const NodeStats& st,
+                            float lam, int rank, int& ph) {
+  const int cnt = max(0, min(a.S, a.V - rank * a.S));
+  float hi = 0.f, lo = 0.f;
+  const int c4 = a.bulk ? cnt / 4 : 0;
+  for (int i = threadIdx.x; i < c4; i += kTT) {
+    const float4 e = reinterpret_cast<const float4*>(sp)[i];
+    const float4 f = reinterpret_cast<const float4*>(sq)[i];
+    ff_accumulate(hi, lo, (rval(e.x, f.x, st.inv_p, st.inv_q, lam) + rval(e.y, f.y, st.inv_p, st.inv_q, lam)) +
+                              (rval(e.z, f.z, st.inv_p, st.inv_q, lam) + rval(e.w, f.w, st.inv_p, st.inv_q, lam)));
+  }
+  for (int i = 4 * c4 + threadIdx.x; i < cnt; i += kTT) ff_accumulate(hi, lo, rval(sp[i], sq[i], st.inv_p, st.inv_q, lam));
+  const ff s = block_sum(ff_norm(hi, lo), sh);
+  publish(sh, ph, make_float4(s.hi, s.lo, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f));
+  const ff tot = cluster_sum_ff(sh, ph);
+  ph ^= 1;
+  return tot;
+}
+
+// Inverse-CDF draw over max(0, p - lam q) (lam = 0: over p) with uniform u.
+// Returns y in every CTA.
+__device__ int draw(const TreeArgs& a, TreeShared& sh, const float* sp, const float* sq, const NodeStats& st,
+                    float lam, float u, int rank, int& ph) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int base = rank * a.S;
+  const int cnt = max(0, min(a.S, a.V - base));
+  const float ip = st.inv_p, iq = st.inv_q;
+  // this CTA's slice mass and last token with mass; warp w covers the
+  // contiguous block [w*blk, (w+1)*blk) so that the owner can be found by warp
+  const int blk = ((cnt + kTW - 1) / kTW + 31) / 32 * 32;
+  const int w0 = min(cnt, warp * blk), w1 = min(cnt, w0 + blk);
+  float hi = 0.f, lo = 0.f;
+  int lastp = -1;
+  for (int i = w0 + lane; i < w1; i += 32) {
+    const float d = rval(sp[i], lam > 0.f ? sq[i] : 0.f, ip, iq, lam);
+    if (d > 0.f) {
+      ff_accumulate(hi, lo, d);
+      lastp = base + i;
+    }
+  }
+  const ff wsum = warp_sum_ff(ff_norm(hi, lo));  // this warp's block
+  if (lane == 0) sh.scan[warp] = wsum;
+  __syncthreads();
+  ff cta = {0.f, 0.f};
+  for (int w = 0; w < kTW; ++w) cta = ff_add(cta, sh.scan[w]);
+  lastp = block_max_i(lastp, sh);
+  publish(sh, ph, make_float4(cta.hi, cta.lo, static_cast<float>(lastp), 0.f), make_float4(0.f, 0.f, 0.f, 0.f));
+  ff pre[kTC + 1];
+  float zs[kTC];
+  cluster_scan_ff(sh, ph, pre, zs);
+  int last_all = -1;
+  for (int r = 0; r < kTC; ++r) last_all = max(last_all, static_cast<int>(zs[r]));
+  ph ^= 1;
+  const ff t = ff_mul_f(pre[kTC], u);
+  int owner = -1;
+  for (int r = 0; r < kTC && owner < 0; ++r)
+    if (ff_gt(pre[r + 1], t)) owner = r;
+  int y = -1;
+  if (owner == rank) {
+    // the warp whose block holds t, then 32 tokens at a time with a warp scan
+    const ff tl = ff_add(t, ff{-pre[rank].hi, -pre[rank].lo});
+    ff run = {0.f, 0.f};
+    int ow = -1;
+    for (int w = 0; w < kTW; ++w) {
+      const ff nxt = ff_add(run, sh.scan[w]);
+      if (ow < 0 && ff_gt(nxt, tl)) ow = w;
+      if (ow < 0) run = nxt;
+    }
+    if (warp == ow) {
+      const int v0 = min(cnt, ow * blk), v1 = min(cnt, v0 + blk);
+      for (int i0 = v0; i0 < v1 && y < 0; i0 += 32) {
+        const int i = i0 + lane;
+        const float d = i < v1 ? rval(sp[i], lam > 0.f ? sq[i] : 0.f, ip, iq, lam) : 0.f;
+        ff incl = {d, 0.f};
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const ff o{__shfl_up_sync(0xffffffffu, incl.hi, off), __shfl_up_sync(0xffffffffu, incl.lo, off)};
+          if (lane >= off) incl = ff_add(o, incl);
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, i < v1 && ff_gt(ff_add(run, incl), tl));
+        if (hit) y = base + i0 + __ffs(hit) - 1;
+        const ff tot{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
+        run = ff_add(run, tot);
+      }
+      if (lane == 0) sh.res_i = y;
+    }
+    __syncthreads();
+    y = ow < 0 ? -1 : sh.res_i;
+    __syncthreads();
+  }
+  // the owner's y (or, when rounding left t past every slice or past the
+  // owner's last step, the last token with mass) to every CTA
+  const float yv = owner == rank ? static_cast<float>(y) : -2.f;
+  publish(sh, ph, make_float4(yv, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f));
+  int yy = -1;
+  if (owner >= 0) yy = static_cast<int>(fetch(sh, ph, 0, owner).x);
+  ph ^= 1;
+  if (owner < 0 || yy < 0) yy = last_all;
+  return yy;
+}
+
+__global__ void __launch_bounds__(kTT, 1) tree_sample_kernel(const TreeArgs a) {
+  __shared__ TreeShared sh;
+  extern __shared__ float4 dyn[];
+  float* sp = reinterpret_cast<float*>(dyn);
+  float* sq = sp + a.S;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int b = blockIdx.x / kTC;
+  const Expo c{a.c_hi, a.c_lo};
+  griddep_wait();
+  // tree structure and validity
+  if (threadIdx.x == 0) {
+    sh.flag = 0;
+    mbar_init(&sh.bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  uint32_t bar_phase = 0;
+  for (int i = threadIdx.x; i < a.N; i += kTT) {
+    const int p = a.par[static_cast<size_t>(b) * a.N + i];
+    const int t = a.tok[static_cast<size_t>(b) * a.N + i];
+    sh.par[i] = p;
+    sh.tok[i] = t;
+    const bool ok = i == 0 ? p == -1 : (p >= 0 && p < i && t >= 0 && t < a.V);
+    if (!ok) atomicOr(&sh.flag, kErrTokenRange);
+  }
+  __syncthreads();
+  int bad = sh.flag;
+  int ph = 0;
+  int cur = 0, n = 0, y = -1;
+  auto next_child = [&](int node, int after) {
+    for (int i = after + 1; i < a.N; ++i)
+      if (sh.par[i] == node) return i;
+    return -1;
+  };
+  while (!bad) {
+    const int first = next_child(cur, 0);
+    const NodeStats st = load_node(a, sh, sp, sq, b, cur, first >= 0, rank, ph, bar_phase, c);
+    if (st.bad) {
+      bad = kErrNonFinite;
+      break;
+    }
+    float lam = 0.f;       // 0: r = p
+    ff sres = {1.f, 0.f};  // mass of max(0, p - lam q) (1 for r = p)
+    int accepted = -1;
+    const size_t row = (static_cast<size_t>(b) * a.N + cur) * a.V;
+    for (int ch = first; ch >= 0; ch = next_child(cur, ch)) {
+      const int x = sh.tok[ch];
+      const float px = pow2_rel(__ldcg(a.zp + row + x), c, st.kp) * st.inv_p;
+      const float qx = pow2_rel(__ldcg(a.zq + row + x), c, st.kq) * st.inv_q;  // = the smem values' scale
+      const float rx = lam > 0.f ? fmaxf(0.f, px - lam * qx) / (sres.hi + sres.lo) : px;
+      const float acc = qx > 0.f ? fminf(1.f, rx / qx) : (rx > 0.f ? 1.f : 0.f);
+      if (__ldcg(a.u + static_cast<size_t>(b) * a.N + ch) < acc) {
+        accepted = ch;
+        break;
+      }
+      const float lam_new = lam > 0.f ? lam + (sres.hi + sres.lo) : 1.f;
+      const ff s_new = residual_mass(a, sh, sp, sq, st, lam_new, rank, ph);
+      if (s_new.hi > 0.f) {
+        lam = lam_new;
+        sres = s_new;
+      }  // no mass left: the working distribution stays as it was
+    }
+    const float u0 = __ldcg(a.u + static_cast<size_t>(b) * a.N);
+    if (accepted < 0) {
+      y = draw(a, sh, sp, sq, st, lam, u0, rank, ph);
+      break;
+    }
+    sh.path[n++] = accepted;  // every thread writes the same value
+    cur = accepted;
+    if (next_child(cur, 0) < 0) {
+      const NodeStats sb = load_node(a, sh, sp, sq, b, cur, false, rank, ph, bar_phase, c);
+      if (sb.bad) {
+        bad = kErrNonFinite;
+        break;
+      }
+      y = draw(a, sh, sp, sq, sb, 0.f, u0, rank, ph);
+      break;
+    }
+  }
+  __syncthreads();
+  if (rank == 0) {
+    const size_t o = static_cast<size_t>(b) * a.N;
+    for (int i = threadIdx.x; i < a.N; i += kTT) {
+      int tv = -1, pv = -1;
+      if (!bad) {
+        if (i < n) {
+          pv = sh.path[i];
+          tv = sh.tok[pv];
+        } else if (i == n) {
+          tv = y;
+        }
+      }
+      a.out_tok[o + i] = tv;
+      a.out_path[o + i] = pv;
+    }
+    if (threadIdx.x == 0) {
+      a.out_n[b] = bad ? -1 : n;
+      if (bad) atomicOr(a.err, bad);
+    }
+  }
+  cluster_sync();  // no CTA leaves while another may still read its shared memory
+}
+
+// ---------------------------------------------------------------- greedy
+__global__ void __launch_bounds__(kTT) tree_greedy_kernel(const TreeArgs a) {
+  __shared__ TreeShared sh;
+  __shared__ float sv_[kTW];
+  __shared__ int si_[kTW], sb_[kTW];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.x;
+  griddep_wait();
+  if (threadIdx.x == 0) sh.flag = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < a.N; i += kTT) {
+    const int p = a.par[static_cast<size_t>(b) * a.N + i];
+    const int t = a.tok[static_cast<size_t>(b) * a.N + i];
+    sh.par[i] = p;
+    sh.tok[i] = t;
+    const bool ok = i == 0 ? p == -1 : (p >= 0 && p < i && t >= 0 && t < a.V);
+    if (!ok) atomicOr(&sh.flag, kErrTokenRange);
+  }
+  __syncthreads();
+  int bad = sh.flag;
+  int cur = 0, n = 0, y = -1;
+  while (!bad) {
+    const size_t row = static_cast<size_t>(b) * a.N + cur;
+    const float* pv = a.pmax + row * a.P;
+    const int* pi = a.pidx + row * a.P;
+    float bv = -INFINITY;
+    int bi = INT_MAX, bb = 0;
+    for (int p = threadIdx.x; p < a.P; p += kTT) {
+      const float v = __ldcg(pv + p);
+      const int ix = __ldcg(pi + p);
+      if (ix == -2) bb = 1;
+      else if (v > bv || (v == bv && ix < bi)) {
+        bv = v;
+        bi = ix;
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    bb = __any_sync(0xffffffffu, bb) ? 1 : 0;
+    if (lane == 0) {
+      sv_[warp] = bv;
+      si_[warp] = bi;
+      sb_[warp] = bb;
+    }
+    __syncthreads();
+    float v0 = sv_[0];
+    int i0 = si_[0], b0 = sb_[0];
+    for (int w = 1; w < kTW; ++w) {
+      b0 |= sb_[w];
+      if (sv_[w] > v0 || (sv_[w] == v0 && si_[w] < i0)) {
+        v0 = sv_[w];
+        i0 = si_[w];
+      }
+    }
+    __syncthreads();
+    if (b0 || i0 == INT_MAX) {
+      bad = kErrNonFinite;
+      break;
+    }
+    int nxt = -1;
+    for (int i = 1; i < a.N; ++i)
+      if (sh.par[i] == cur && sh.tok[i] == i0) {
+        nxt = i;
+        break;
+      }
+    if (nxt < 0) {
+      y = i0;
+      break;
+    }
+    sh.path[n++] = nxt;
+    cur = nxt;
+  }
+  __syncthreads();
+  const size_t o = static_cast<size_t>(b) * a.N;
+  for (int i = threadIdx.x; i < a.N; i += kTT) {
+    int tv = -1, pv = -1;
+    if (!bad) {
+      if (i < n) {
+        pv = sh.path[i];
+        tv = sh.tok[pv];
+      } else if (i == n) {
+        tv = y;
+      }
+    }
+    a.out_tok[o + i] = tv;
+    a.out_path[o + i] = pv;
+  }
+  if (threadIdx.x == 0) {
+    a.out_n[b] = bad ? -1 : n;
+    if (bad) atomicOr(a.err, bad);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+size_t round_up(size_t x) { return (x + 255) / 256 * 256; }
+
+bool tree_dims_ok(const spec_tree_dims& d, bool need_head) {
+  if (d.B < 1 || d.N < 1 || d.N > kMaxNodes || d.V < 1 || d.V > kTC * kMaxSlice) return false;
+  if (static_cast<long long>(d.B) * d.N > (1ll << 24)) return false;
+  if (need_head && (d.d < 8 || d.d % 8 != 0 || d.d > (1 << 20))) return false;
+  return true;
+}
+
+struct TreeLayout {
+  size_t logits = 0, pmax = 0, pidx = 0, total = 0;
+  int P = 0;
+};
+
+// [0, 256): error word; then the logits (sampling, when kept here) or the
+// argmax partials (greedy).
+TreeLayout tree_layout(const spec_tree_dims& d, bool greedy, bool logits_in_ws, bool from_logits) {
+  TreeLayout L;
+  size_t off = 256;
+  const size_t M = static_cast<size_t>(d.B) * d.N;
+  if (greedy) {
+    L.P = from_logits ? (d.V + kChunk - 1) / kChunk : (d.V + kHeadTileV - 1) / kHeadTileV;
+    L.pmax = off;
+    off += round_up(sizeof(float) * M * L.P);
+    L.pidx = off;
+    off += round_up(sizeof(int) * M * L.P);
+  } else if (logits_in_ws) {
+    L.logits = off;
+    off += round_up(sizeof(float) * M * d.V);
+  }
+  L.total = off;
+  return L;
+}
+
+bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+spec_status check_tree_args(const spec_tree_dims& d, float T, const float* draft_logits, const int32_t* tokens,
+                            const int32_t* parents, const float* uniforms, const int32_t* out_tokens,
+                            const int32_t* out_path, const int32_t* out_n) {
+  if (!(T >= 0.f) || !std::isfinite(T)) return SPEC_ERR_ARG;
+  if (!tokens || !parents || !out_tokens || !out_path || !out_n) return SPEC_ERR_ARG;
+  if (T > 0.f && (!draft_logits || !uniforms)) return SPEC_ERR_ARG;
+  if (draft_logits && !aligned(draft_logits, 16)) return SPEC_ERR_ALIGN;
+  const uintptr_t any4 = reinterpret_cast<uintptr_t>(tokens) | reinterpret_cast<uintptr_t>(parents) |
+                         reinterpret_cast<uintptr_t>(out_tokens) | reinterpret_cast<uintptr_t>(out_path) |
+                         reinterpret_cast<uintptr_t>(out_n) | reinterpret_cast<uintptr_t>(uniforms);
+  if (any4 & 3u) return SPEC_ERR_ALIGN;
+  return SPEC_OK;
+}
+
+TreeArgs tree_args(const spec_tree_dims& d, float T, const float* zp, const float* zq, const int32_t* tokens,
+                   const int32_t* parents, const float* uniforms, int32_t* out_tokens, int32_t* out_path,
+                   int32_t* out_n, int* err) {
+  TreeArgs a;
+  a.B = d.B;
+  a.N = d.N;
+  a.V = d.V;
+  a.S = ((d.V + kTC - 1) / kTC + 3) / 4 * 4;
+  a.bulk = d.V % 4 == 0 && (reinterpret_cast<uintptr_t>(zp) & 15u) == 0 && (reinterpret_cast<uintptr_t>(zq) & 15u) == 0;
+  if (T > 0.f) exponent_constant(T, &a.c_hi, &a.c_lo); else a.c_hi = a.c_lo = 0.f;
+  a.zp = zp;
+  a.zq = zq;
+  a.tok = tokens;
+  a.par = parents;
+  a.u = uniforms;
+  a.out_tok = out_tokens;
+  a.out_path = out_path;
+  a.out_n = out_n;
+  a.err = err;
+  a.pmax = nullptr;
+  a.pidx = nullptr;
+  a.P = 0;
+  return a;
+}
+
+cudaError_t launch_tree_sample(const TreeArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+  static bool attr_done[64] = {false};
+  const size_t smem = 2u * sizeof(float) * static_cast<size_t>(a.S);
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev.device]) {
+    const cudaError_t e = cudaFuncSetAttribute(tree_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               2 * static_cast<int>(sizeof(float)) * kMaxSlice);
+    if (e != cudaSuccess) return e;
+    attr_done[dev.device] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.B * kTC);
+  cfg.blockDim = dim3(kTT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kTC;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, tree_sample_kernel, a);
+}
+
+}  // namespace
+}  // namespace sv
+
+extern "C" {
+
+size_t spec_tree_workspace_bytes(spec_tree_dims dims, float temperature, int32_t logits_in_workspace) {
+  if (!sv::tree_dims_ok(dims, false) || !(temperature >= 0.f) || !std::isfinite(temperature)) return 0;
+  return sv::tree_layout(dims, temperature == 0.f, logits_in_workspace != 0, false).total;
+}
+
+spec_status spec_tree_verify(const void* hidden, const void* W_lm, const float* draft_logits, const int32_t* tokens,
+                             const int32_t* parents, const float* uniforms, float temperature, int32_t* out_tokens,
+                             int32_t* out_path, int32_t* out_num_accepted, spec_tree_dims dims, void* workspace,
+                             size_t workspace_bytes, float* out_target_logits, spec_stream_t stream) {
+  using namespace sv;
+  if (!tree_dims_ok(dims, true)) return SPEC_ERR_DIMS;
+  if (!hidden || !W_lm) return SPEC_ERR_ARG;
+  if (!aligned(hidden, 16) || !aligned(W_lm, 16)) return SPEC_ERR_ALIGN;
+  spec_status st = check_tree_args(dims, temperature, draft_logits, tokens, parents, uniforms, out_tokens, out_path,
+                                   out_num_accepted);
+  if (st != SPEC_OK) return st;
+  const bool greedy = temperature == 0.f;
+  if (greedy && out_target_logits) return SPEC_ERR_ARG;
+  if (out_target_logits && !aligned(out_target_logits, 16)) return SPEC_ERR_ALIGN;
+  const TreeLayout L = tree_layout(dims, greedy, !greedy && !out_target_logits, false);
+  if (!workspace || workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return SPEC_ERR_ALIGN;
+  DeviceInfo dev;
+  const int ds = current_device(dev);
+  if (ds != SPEC_OK) return static_cast<spec_status>(ds);
+  char* ws = static_cast<char*>(workspace);
+  int* err = reinterpret_cast<int*>(ws);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int M = dims.B * dims.N;
+  bool enc_fail = false;
+  if (greedy) {
+    float* pmax = reinterpret_cast<float*>(ws + L.pmax);
+    int* pidx = reinterpret_cast<int*>(ws + L.pidx);
+    const cudaError_t e = launch_head(hidden, W_lm, M, dims.d, dims.V, HeadOut::kArgmax, nullptr, pmax, pidx, nullptr,
+                                      err, true, dev, s, &enc_fail);
+    if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
+    TreeArgs a = tree_args(dims, 0.f, nullptr, nullptr, tokens, parents, nullptr, out_tokens, out_path,
+                           out_num_accepted, err);
+    a.pmax = pmax;
+    a.pidx = pidx;
+    a.P = L.P;
+    return launch_dependent(tree_greedy_kernel, dim3(dims.B), dim3(kTT), s, a) == cudaSuccess ? SPEC_OK
+                                                                                              : SPEC_ERR_CUDA;
+  }
+  float* logits = out_target_logits ? out_target_logits : reinterpret_cast<float*>(ws + L.logits);
+  const cudaError_t e = launch_head(hidden, W_lm, M, dims.d, dims.V, HeadOut::kLogits, logits, nullptr, nullptr,
+                                    nullptr, err, true, dev, s, &enc_fail);
+  if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
+  const TreeArgs a = tree_args(dims, temperature, logits, draft_logits, tokens, parents, uniforms, out_tokens,
+                               out_path, out_num_accepted, err);
+  return launch_tree_sample(a, dev, s) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status spec_tree_verify_from_logits(const float* target_logits, const float* draft_logits,
+                                         const int32_t* tokens, const int32_t* parents, const float* uniforms,
+                                         float temperature, int32_t* out_tokens, int32_t* out_path,
+                                         int32_t* out_num_accepted, spec_tree_dims dims, void* workspace,
+                                         size_t workspace_bytes, spec_stream_t stream) {
+  using namespace sv;
+  if (!tree_dims_ok(dims, false)) return SPEC_ERR_DIMS;
+  if (!target_logits) return SPEC_ERR_ARG;
+  if (!aligned(target_logits, 16)) return SPEC_ERR_ALIGN;
+  spec_status st = check_tree_args(dims, temperature, draft_logits, tokens, parents, uniforms, out_tokens, out_path,
+                                   out_num_accepted);
+  if (st != SPEC_OK) return st;
+  const bool greedy = temperature == 0.f;
+  const TreeLayout L = tree_layout(dims, greedy, false, true);
+  if (!workspace || workspace_bytes < L.total) return SPEC_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return SPEC_ERR_ALIGN;
+  DeviceInfo dev;
+  const int ds = current_device(dev);
+  if (ds != SPEC_OK) return static_cast<spec_status>(ds);
+  char* ws = static_cast<char*>(workspace);
+  int* err = reinterpret_cast<int*>(ws);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const int M = dims.B * dims.N;
+  if (greedy) {
+    float* pmax = reinterpret_cast<float*>(ws + L.pmax);
+    int* pidx = reinterpret_cast<int*>(ws + L.pidx);
+    if (launch_row_argmax(target_logits, M, dims.V, pmax, pidx, err, s) != cudaSuccess) return SPEC_ERR_CUDA;
+    TreeArgs a = tree_args(dims, 0.f, target_logits, nullptr, tokens, parents, nullptr, out_tokens, out_path,
+                           out_num_accepted, err);
+    a.pmax = pmax;
+    a.pidx = pidx;
+    a.P = L.P;
+    return launch_dependent(tree_greedy_kernel, dim3(dims.B), dim3(kTT), s, a) == cudaSuccess ? SPEC_OK
+                                                                                              : SPEC_ERR_CUDA;
+  }
+  if (cudaMemsetAsync(err, 0, sizeof(int), s) != cudaSuccess) return SPEC_ERR_CUDA;
+  const TreeArgs a = tree_args(dims, temperature, target_logits, draft_logits, tokens, parents, uniforms, out_tokens,
+                               out_path, out_num_accepted, err);
+  return launch_tree_sample(a, dev, s) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // extern "C"

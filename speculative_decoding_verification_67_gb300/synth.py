@@ -349,3 +349,81 @@ def make_draft_inputs(w: Workload, device="cpu", seed: int | None = None) -> dic
     draft_uniforms = torch.rand((K, B), generator=g, device=device, dtype=torch.float32)
     uniforms = torch.rand((B, K + 1), generator=g, device=device, dtype=torch.float32)
     return dict(hidden=h, W=W, draft_hidden=draft_hidden, draft_uniforms=draft_uniforms, uniforms=uniforms)
+
+
+# ---------------------------------------------------------------------------
+# Tree-shaped candidates.  A tree of fixed shape per workload: the root has
+# branching[0] children, each of those branching[1], and so on; nodes are
+# numbered level by level (parents before children).  Every node has a
+# target hidden state h ~ N(0, 1) bf16 (one tree-attention target pass) and
+# a draft row z_q = (h + noise * eps) W^T in fp32 (the draft model at that
+# node); the children of a node are independent draws from softmax(z_q / T)
+# (Gumbel-max), the condition of the tree rule's exactness.  Uniforms
+# [B][N]: u[b][i] tests node i, u[b][0] is the final draw.
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class TreeWorkload:
+    name: str
+    B: int
+    branching: tuple
+    d: int
+    V: int
+    temperature: float
+    noise: float
+    seed: int = 0
+
+    @property
+    def N(self) -> int:
+        n, width = 1, 1
+        for k in self.branching:
+            width *= k
+            n += width
+        return n
+
+
+TREE_WORKLOADS = {
+    w.name: w
+    for w in (
+        TreeWorkload("tree_B8_N16_V128256", B=8, branching=(3, 2, 1), d=4096, V=128256, temperature=0.8,
+                     noise=0.3, seed=6741),
+        TreeWorkload("tree_B4_N40_V128256", B=4, branching=(3, 3, 3), d=4096, V=128256, temperature=1.0,
+                     noise=0.5, seed=6742),
+    )
+}
+
+
+def tree_parents(branching) -> list:
+    parents = [-1]
+    level = [0]
+    for k in branching:
+        nxt = []
+        for p in level:
+            for _ in range(k):
+                parents.append(p)
+                nxt.append(len(parents) - 1)
+        level = nxt
+    return parents
+
+
+def make_tree_inputs(w: TreeWorkload, device="cpu", seed: int | None = None, greedy_drafts: bool = False) -> dict:
+    """hidden bf16 [B*N, d], W bf16 [V, d], draft_logits f32 [B*N, V],
+    tokens / parents int32 [B, N], uniforms f32 [B, N]."""
+    device = torch.device(device)
+    g = _gen(device, w.seed if seed is None else seed)
+    B, N, d, V = w.B, w.N, w.d, w.V
+    h = _randn_bf16((B * N, d), 1.0, g, device)
+    W = _randn_bf16((V, d), 1.0 / math.sqrt(d), g, device)
+    eps = _randn((B * N, d), g, device)
+    zq = _project(h.float() + w.noise * eps, W)
+    par = torch.tensor(tree_parents(w.branching), dtype=torch.int32, device=device).repeat(B, 1)
+    tok = torch.zeros((B, N), dtype=torch.int32, device=device)
+    T = w.temperature if w.temperature > 0 else 1.0
+    zq3 = zq.view(B, N, V)
+    for i in range(1, N):
+        pi = int(par[0, i])
+        if greedy_drafts:
+            tok[:, i] = torch.argmax(zq3[:, pi, :], dim=-1).to(torch.int32)
+        else:
+            tok[:, i] = gumbel_max_tokens(zq3[:, pi, :], T, g)
+    u = torch.rand((B, N), generator=g, device=device, dtype=torch.float32)
+    return dict(hidden=h, W=W, draft_logits=zq.contiguous(), tokens=tok, parents=par, uniforms=u)

@@ -157,3 +157,25 @@ def test_draft_step_host_side_errors(lib):
     assert call(dims=sv.SpecDims(0, 0, 512, 5000)) == 2
     assert call(h=_fake(0x10008)) == 3
     assert call(ol=_fake(None), size=nws - 1) == 4   # logits kept in the workspace
+
+
+def test_tree_host_side_errors(lib):
+    good = _fake(0x10000)
+    d = sv.SpecTreeDims(2, 16, 512, 5000)
+    nws = lib.spec_tree_workspace_bytes(d, 0.8, 1)
+    assert nws >= 256 + 4 * 32 * 5000
+    assert lib.spec_tree_workspace_bytes(sv.SpecTreeDims(2, 257, 512, 5000), 0.8, 1) == 0     # N > 256
+    assert lib.spec_tree_workspace_bytes(sv.SpecTreeDims(2, 16, 512, 200000), 0.8, 1) == 0    # V too large
+
+    def call(h=good, W=good, dl=good, tok=good, par=good, u=good, T=0.8, ot=good, op=good, on=good, dims=d, ws=good,
+             size=nws, otl=_fake(None)):
+        return lib.spec_tree_verify(h, W, dl, tok, par, u, T, ot, op, on, dims, ws, size, otl, _fake(None))
+
+    assert call(h=_fake(None)) == 1
+    assert call(par=_fake(None)) == 1
+    assert call(u=_fake(None)) == 1
+    assert call(T=0.0, otl=good) == 1
+    assert call(dims=sv.SpecTreeDims(2, 0, 512, 5000)) == 2
+    assert call(dims=sv.SpecTreeDims(2, 16, 500, 5000)) == 2
+    assert call(dl=_fake(0x10004)) == 3
+    assert call(size=nws - 1) == 4
