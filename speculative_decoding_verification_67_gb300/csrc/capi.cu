@@ -56,6 +56,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // softmax statistics clears the tickets the finishing kernel counts on.
 struct Layout {
   size_t ctrl_bytes = 0;
+  size_t fix = 0;                                     // stream-K fixup of the precise LM head (M <= 64)
   size_t tpart = 0, dpart = 0, res = 0, logits = 0;  // sampling
   size_t pmax = 0, pidx = 0;                                   // greedy
   int CA = 0, P = 0;
@@ -72,9 +73,17 @@ Layout make_layout(int B, int K, int V, bool greedy, bool logits_in_ws, bool fro
   size_t off = round_up(sizeof(int) * (kCtrlTickets + static_cast<size_t>(B)));
   L.ctrl_bytes = off;
   L.CA = (V + sv::kChunk - 1) / sv::kChunk;
+  const bool precise_head = !from_logits && M <= 64;
+  if (precise_head) {
+    L.fix = off;
+    off += round_up(sv::kFixupBytes);
+  }
   if (!greedy) {
-    L.tpart = off;  // per-tile partials are the most the LM head ever writes
-    off += round_up(sizeof(sv::StatPart) * M * (from_logits ? static_cast<size_t>(L.CA) : num_vt));
+    // the LM head writes one partial per tile, or one per CTA (precise)
+    L.tpart = off;
+    const size_t parts = from_logits ? static_cast<size_t>(L.CA)
+                                     : std::max(num_vt, static_cast<size_t>(precise_head ? sv::kMaxHeadGrid : 0));
+    off += round_up(sizeof(sv::StatPart) * M * parts);
     L.dpart = off;
     off += round_up(sizeof(sv::StatPart) * static_cast<size_t>(B) * K * L.CA);
     L.res = off;
@@ -234,7 +243,7 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
   if (greedy) {
     e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kArgmax, nullptr,
                         reinterpret_cast<float*>(ws + L.pmax), reinterpret_cast<int*>(ws + L.pidx), nullptr, err,
-                        true, dev, s, &enc_fail);
+                        true, dev, s, &enc_fail, 0, L.fix ? ws + L.fix : nullptr);
     if (enc_fail || e != cudaSuccess || !mark(1)) return SPEC_ERR_CUDA;
     const sv::GreedyArgs g = greedy_args(L, dims, draft_tokens, out_tokens, out_num_accepted, out_debug, ws);
     e = sv::launch_greedy_finish(g, s);
@@ -242,7 +251,7 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
   }
   float* logits = out_target_logits ? out_target_logits : reinterpret_cast<float*>(ws + L.logits);
   if (!out_target_logits || ldz <= 0) ldz = dims.V;
-  const sv::HeadPlan plan = sv::plan_head(M, dims.d, dims.V, sv::HeadOut::kStats, dev);
+  const sv::HeadPlan plan = sv::plan_head(M, dims.d, dims.V, sv::HeadOut::kStats, dev, L.fix != 0);
   sv::HeadStats hs;
   sv::exponent_constant(temperature, &hs.c_hi, &hs.c_lo);
   hs.tpart = reinterpret_cast<sv::StatPart*>(ws + L.tpart);
@@ -255,7 +264,7 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
   if (plan.precise) {
     // small batch: the LM head's epilogue and side warps produce the statistics
     e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kStats, logits, nullptr, nullptr, &hs, err,
-                        true, dev, s, &enc_fail, ldz);
+                        true, dev, s, &enc_fail, ldz, L.fix ? ws + L.fix : nullptr);
     if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
     Pt = plan.target_parts;
   } else {

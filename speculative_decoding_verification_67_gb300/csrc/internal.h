@@ -66,9 +66,20 @@ struct HeadPlan {
   // target-row partials: one per CTA (num_chunks == 1) or one per tile
   bool per_cta_partials = false;
   int target_parts = 0;  // partials per target row
+  // stream-K schedule (precise scheme with a fixup buffer): every CTA takes an
+  // equal contiguous range of the num_tiles * groups (tile, 4-block group) units
+  bool streamk = false;
+  int groups = 1;        // units per tile
 };
 
-HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev);
+// Upper bound of the LM head's grid (sizes the per-CTA workspace areas).
+constexpr int kMaxHeadGrid = 256;
+// Fixup area of the stream-K schedule: 128 x 64 floats per CTA, then 4
+// 64-bit flags per CTA.
+constexpr size_t kFixupFloatsPerCta = 128 * 64;
+constexpr size_t kFixupBytes = kMaxHeadGrid * (kFixupFloatsPerCta * 4 + 4 * 8);
+
+HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, bool streamk = false);
 
 // Sampling-step statistics the LM head produces alongside the logits.
 struct HeadStats {
@@ -84,11 +95,12 @@ struct HeadStats {
 // Enqueues the LM head.  Returns cudaSuccess or the first CUDA error;
 // *encode_failed is set when building a TMA descriptor failed.  When
 // zero_err is set, the kernel clears *err before anything can report.
-// `ldz` is the row stride of `logits` in floats (0: V).
+// `ldz` is the row stride of `logits` in floats (0: V).  `fixup` (kFixupBytes,
+// no initialisation needed) enables the stream-K schedule of the precise scheme.
 cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, HeadOut mode,
                         float* logits, float* part_max, int* part_idx, const HeadStats* stats, int* err,
                         bool zero_err, const DeviceInfo& dev, cudaStream_t stream, bool* encode_failed,
-                        long long ldz = 0);
+                        long long ldz = 0, void* fixup = nullptr);
 
 // ------------------------------------------------------------------ verify
 struct VerifyArgs {

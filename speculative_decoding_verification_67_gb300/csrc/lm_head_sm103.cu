@@ -38,6 +38,8 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <mutex>
 
 #include "internal.h"
@@ -60,6 +62,10 @@ constexpr int kModeStats = static_cast<int>(HeadOut::kStats);
 
 struct HeadParams {
   int M, d, V;
+  int streamk, groups;          // stream-K schedule; units per tile
+  float* fix;                   // [grid][64][128] partial sums handed to a tile's first CTA
+  unsigned long long* flags;    // [grid][4] = epoch once the CTA's quadrant's sums are stored
+  unsigned long long epoch;     // unique per launch
   int N, num_chunks, num_vt, num_tiles, num_kb, stages;
   uint32_t tmem_cols;
   float* logits;
@@ -86,6 +92,39 @@ __device__ int g_head_timeout_word = 0;
 
 __device__ __forceinline__ void report_timeout(int* err) {
   atomicOr(err ? err : &g_head_timeout_word, kErrTimeout);
+}
+
+// The work of one CTA as items (tile, groups [g0, g1)).  Tile mode: whole
+// tiles blockIdx.x, blockIdx.x + gridDim.x, ...; stream-K: the CTA's equal
+// contiguous share of the num_tiles * groups units, split at tile ends.  Every
+// warp role walks the same items.
+struct WorkCursor {
+  long long u, end;
+};
+
+__device__ __forceinline__ long long streamk_start(const HeadParams& p, int cta) {
+  return static_cast<long long>(p.num_tiles) * p.groups * cta / gridDim.x;
+}
+
+__device__ __forceinline__ WorkCursor work_begin(const HeadParams& p) {
+  if (p.streamk) return {streamk_start(p, blockIdx.x), streamk_start(p, blockIdx.x + 1)};
+  return {static_cast<long long>(blockIdx.x), static_cast<long long>(p.num_tiles)};
+}
+
+__device__ __forceinline__ bool work_next(const HeadParams& p, WorkCursor& c, int& tile, int& g0, int& g1) {
+  if (c.u >= c.end) return false;
+  if (p.streamk) {
+    tile = static_cast<int>(c.u / p.groups);
+    g0 = static_cast<int>(c.u - static_cast<long long>(tile) * p.groups);
+    g1 = static_cast<int>(min(static_cast<long long>(p.groups), g0 + (c.end - c.u)));
+    c.u += g1 - g0;
+  } else {
+    tile = static_cast<int>(c.u);
+    g0 = 0;
+    g1 = p.groups;
+    c.u += gridDim.x;
+  }
+  return true;
 }
 
 // Output of 16 columns [c0, c0+16) of this thread's vocabulary row v.
@@ -356,10 +395,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       long long issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      WorkCursor wc = work_begin(p);
+      int tile, g0, g1;
+      while (ok && work_next(p, wc, tile, g0, g1)) {
         const int vt = tile / p.num_chunks;
         const int pc = tile - vt * p.num_chunks;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int kb0 = kPrecise ? g0 * kGroupPrecise : 0;
+        const int kb1 = kPrecise ? min(g1 * kGroupPrecise, p.num_kb) : p.num_kb;
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u)) {
             report_timeout(p.err);
             ok = false;
@@ -401,7 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int slot = 0;
       uint32_t sph = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      WorkCursor wc = work_begin(p);
+      int tile, g0, g1;
+      while (ok && work_next(p, wc, tile, g0, g1)) {
         if (!kPrecise) {
           if (!mbar_wait(&afree[slot], sph ^ 1u)) {
             report_timeout(p.err);
@@ -409,7 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after_sync();
         }
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        const int kb0 = kPrecise ? g0 * kGroupPrecise : 0;
+        const int kb1 = kPrecise ? min(g1 * kGroupPrecise, p.num_kb) : p.num_kb;
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[s], ph)) {
             report_timeout(p.err);
             ok = false;
@@ -481,7 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int slot = 0;
     uint32_t sph = 0, rph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+    WorkCursor wc = work_begin(p);
+    int tile, g0, g1;
+    while (ok && work_next(p, wc, tile, g0, g1)) {
       const int vt = tile / p.num_chunks;
       const int pc = tile - vt * p.num_chunks;
       const int v = vt * kHeadTileV + q * 32 + lane;
@@ -494,8 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float acc[kPrecN];
 #pragma unroll
         for (int i = 0; i < kPrecN; ++i) acc[i] = 0.f;
-        const int groups = (p.num_kb + kGroupPrecise - 1) / kGroupPrecise;
-        for (int g = 0; g < groups; ++g) {
+        for (int g = g0; g < g1; ++g) {
           if (!mbar_wait(&afull[slot], sph)) {
             report_timeout(p.err);
             ok = false;
@@ -525,6 +573,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
+        if (g0 > 0) {
+          // a later part of a tile: hand this quadrant's sums to the CTA that
+          // owns the tile's first group, and emit nothing
+          float* f = p.fix + static_cast<size_t>(blockIdx.x) * kFixupFloatsPerCta + et;
+#pragma unroll
+          for (int i = 0; i < kPrecN; ++i) f[i * 128] = acc[i];
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            st_release_u64(&p.flags[blockIdx.x * 4 + q], p.epoch);
+          }
+          continue;
+        }
+        if (g1 < p.groups) {
+          // the first part of a tile whose other groups belong to the next
+          // CTA(s), each of which stored them before anything else
+          for (int c2 = blockIdx.x + 1; c2 < static_cast<int>(gridDim.x); ++c2) {
+            if (streamk_start(p, c2) >= static_cast<long long>(tile + 1) * p.groups) break;
+            bool got = true;
+            if (lane == 0) {
+              const unsigned long long* fl = &p.flags[c2 * 4 + q];
+              if (ld_acquire_u64(fl) != p.epoch) {
+                const uint64_t t0 = global_timer_ns();
+                while (ld_acquire_u64(fl) != p.epoch) {
+                  if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    got = false;
+                    break;
+                  }
+                }
+              }
+            }
+            got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+            if (!got) {
+              report_timeout(p.err);
+              continue;
+            }
+            const float* f = p.fix + static_cast<size_t>(c2) * kFixupFloatsPerCta + et;
+#pragma unroll
+            for (int i = 0; i < kPrecN; ++i) acc[i] += __ldcg(f + i * 128);
+          }
+        }
         if constexpr (run_stats) {
           // logits out, and fold this row's value of every column into the
           // thread's running partial of that column (exact rescaling)
@@ -669,6 +758,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
 }
 
+// A 64-bit value unique to each launch in this process (the stream-K flags
+// compare against it, so a workspace needs no clearing between calls).
+unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> counter{
+      static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count()) * 0x9E3779B97F4A7C15ull};
+  unsigned long long e;
+  do {
+    e = counter.fetch_add(1ull) + 1ull;
+  } while (e == 0ull);
+  return e;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -725,7 +826,7 @@ cudaError_t launch_mode(HeadOut mode, const CUtensorMap& map_w, const CUtensorMa
 
 }  // namespace
 
-HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev) {
+HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, bool streamk) {
   HeadPlan h;
   if (M <= 64) {
     h.precise = true;
@@ -757,7 +858,10 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev) {
   stages = std::min(12, std::max(2, stages));
   h.stages = stages;
   h.smem_bytes = fixed + static_cast<size_t>(stages) * stage;
-  h.grid = std::min(h.num_tiles, dev.sm_count);
+  h.streamk = streamk && h.precise;
+  h.groups = h.precise ? (h.num_kb + kGroupPrecise - 1) / kGroupPrecise : 1;
+  const long long units = h.streamk ? static_cast<long long>(h.num_tiles) * h.groups : h.num_tiles;
+  h.grid = static_cast<int>(std::min<long long>(units, std::min(dev.sm_count, kMaxHeadGrid)));
   h.per_cta_partials = h.num_chunks == 1;
   h.target_parts = h.per_cta_partials ? h.grid : h.num_vt;
   return h;
@@ -765,9 +869,10 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev) {
 
 cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, HeadOut mode, float* logits,
                         float* part_max, int* part_idx, const HeadStats* stats, int* err, bool zero_err,
-                        const DeviceInfo& dev, cudaStream_t stream, bool* encode_failed, long long ldz) {
+                        const DeviceInfo& dev, cudaStream_t stream, bool* encode_failed, long long ldz,
+                        void* fixup) {
   *encode_failed = false;
-  const HeadPlan h = plan_head(M, d, V, mode, dev);
+  const HeadPlan h = plan_head(M, d, V, mode, dev, fixup != nullptr);
   CUtensorMap map_w, map_h;
   if (!encode_bf16_rows(&map_w, W, static_cast<uint64_t>(d), static_cast<uint64_t>(V), kHeadTileV) ||
       !encode_bf16_rows(&map_h, hidden, static_cast<uint64_t>(d), static_cast<uint64_t>(M),
@@ -788,6 +893,13 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
   p.tmem_cols = h.tmem_cols;
   p.logits = logits;
   p.ldz = ldz > 0 ? ldz : V;
+  p.streamk = h.streamk ? 1 : 0;
+  p.groups = h.groups;
+  p.fix = h.streamk ? static_cast<float*>(fixup) : nullptr;
+  p.flags = h.streamk ? reinterpret_cast<unsigned long long*>(static_cast<char*>(fixup) +
+                                                              kMaxHeadGrid * kFixupFloatsPerCta * 4)
+                      : nullptr;
+  p.epoch = next_epoch();
   p.part_max = part_max;
   p.part_idx = part_idx;
   p.err = err;

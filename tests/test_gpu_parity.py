@@ -362,3 +362,31 @@ def test_full_size_greedy_sampled_sequences():
     np.testing.assert_array_equal(np64(dbg)[seqs][:, :, 1].astype(np.int64), ref["argmax"])
     # the fused argmax epilogue saw exactly the values the plain LM head writes
     np.testing.assert_array_equal(np64(dbg)[seqs][:, :, 0].reshape(-1), np64(z_gpu).max(axis=1))
+
+
+@pytest.mark.parametrize("B,K,d,V,T", [(1, 4, 4096, 1000, 1.0),     # 8 tiles x 16 groups: 16-way splits
+                                       (2, 3, 1024, 5000, 0.9),     # 40 tiles x 4 groups on 152 CTAs
+                                       (8, 4, 4096, 20000, 0.8),    # 157 tiles x 16 groups: 2-way splits
+                                       (3, 3, 4096, 2000, 0.0)])    # greedy, 16 tiles x 16 groups
+def test_streamk_split_tiles(B, K, d, V, T):
+    """The precise LM head spreads (tile, group) units evenly over the CTAs; a
+    tile split across CTAs is finished by the CTA holding its first group with
+    the others' sums from the fixup area.  Logits and results against the
+    oracle as everywhere; the logits also agree with the whole-tile schedule
+    of the bare LM head to rounding."""
+    w = synth.custom("streamk", B=B, K=K, d=d, V=V, temperature=T, noise=0.3, seed=B * 100 + d + V)
+    inp, tok, n, logits, dbg = _run_head_case(w)
+    z_tile = sv.spec_lm_head(inp["hidden"], inp["W"])
+    torch.cuda.synchronize()
+    dl = np64(inp["draft_logits"]) if T > 0 else None
+    u = np64(inp["uniforms"]) if T > 0 else None
+    ref = oracle.spec_verify(np64(inp["hidden"]), np64(inp["W"]), dl, np_int(inp["draft_tokens"]), u, t32(T), B, K)
+    if T > 0:
+        err = logits_error(np64(logits), ref["target_logits"])
+        assert err["max_abs"] <= LOGIT_ATOL and err["rms"] < 1e-5, err
+        assert np.abs(np64(logits) - np64(z_tile)).max() < 1e-4
+        compare_sampling(np_int(tok), np_int(n), ref, K)
+    else:
+        err = logits_error(np64(z_tile), ref["target_logits"])
+        st = compare_greedy(np_int(tok), np_int(n), ref, err["max_abs"])
+        assert st["mismatched_near_ties"] == 0, st
