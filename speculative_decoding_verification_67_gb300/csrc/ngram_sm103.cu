@@ -82,30 +82,74 @@ __global__ void __launch_bounds__(kNgThreads) ngram_kernel(const NgArgs a) {
   const int L = s_L;
   const bool valid = L >= 0 && L <= a.max_len;
   const int e_end = (valid && s_ok) ? min(c0 + a.chunk, L - 1) : 0;
-  const int last_tok = s_suf[0];
-  unsigned long long best = 0ull;
   // four positions per 16-byte shared load (consecutive threads, consecutive
-  // words: conflict-free); only a token equal to the last one looks further
+  // words: conflict-free): one mask of the positions holding the last token (a
+  // group without one leaves at once), and for the others the masks of the
+  // three preceding tokens, whose ANDs give the match lengths of all four;
+  // only a match of four or more tokens when n_max > 4 looks further back.  A
+  // thread's positions increase, so it keeps its longest match and, for equal
+  // lengths, the earliest, and stops once it has one of n_max tokens.
   const int n_e = e_end - c0;
+  const int s0 = s_suf[0], s1 = s_suf[min(1, kNgMaxN - 1)], s2 = s_suf[min(2, kNgMaxN - 1)],
+            s3 = s_suf[min(3, kNgMaxN - 1)];
+  const int nmax4 = min(a.n_max, 4);
+  int best_l = 0, best_e = 0;
   for (int q0 = 4 * static_cast<int>(threadIdx.x); q0 < n_e; q0 += 4 * kNgThreads) {
-    const int4 v4 = *reinterpret_cast<const int4*>(s_tok + kNgMaxN + q0);
-    const int vq[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      if (vq[q] == last_tok && q0 + q < n_e) {
-        const int e = c0 + q0 + q;
-        const int* t = s_tok + kNgMaxN + q0 + q;  // t[-l] = h[e-l] for l <= kNgMaxN
-        const int lim = min(a.n_max, e + 1);
-        int l = 1;
-        while (l < lim && t[-l] == s_suf[l]) ++l;
-        if (l >= a.n_min) {
-          const unsigned long long k =
-              (static_cast<unsigned long long>(l) << 32) | (0xffffffffu - static_cast<unsigned>(e));
-          best = k > best ? k : best;
+    const int4 v = *reinterpret_cast<const int4*>(s_tok + kNgMaxN + q0);
+    const int rem = n_e - q0;
+    const unsigned live = rem >= 4 ? 0xfu : ((1u << rem) - 1u);
+    const unsigned B0 = ((v.x == s0) | ((v.y == s0) << 1) | ((v.z == s0) << 2) | ((v.w == s0) << 3)) & live;
+    if (B0 == 0u) continue;
+    const int4 pv = *reinterpret_cast<const int4*>(s_tok + kNgMaxN + q0 - 4);
+    // bit q of Bl: h[e - l] == s_l for e = c0 + q0 + q
+    const unsigned B1 = (pv.w == s1) | ((v.x == s1) << 1) | ((v.y == s1) << 2) | ((v.z == s1) << 3);
+    const unsigned B2 = (pv.z == s2) | ((pv.w == s2) << 1) | ((v.x == s2) << 2) | ((v.y == s2) << 3);
+    const unsigned B3 = (pv.y == s3) | ((pv.z == s3) << 1) | ((pv.w == s3) << 2) | ((v.x == s3) << 3);
+    // a match of j tokens needs j <= e + 1 (only at the history's start)
+    const bool head = c0 + q0 == 0;
+    const unsigned M1 = B0 & B1 & (head ? 0xeu : 0xfu);
+    const unsigned M2 = M1 & B2 & (head ? 0xcu : 0xfu);
+    const unsigned M3 = M2 & B3 & (head ? 0x8u : 0xfu);
+    int top;
+    unsigned tm;
+    if (nmax4 >= 4 && M3) {
+      top = 4;
+      tm = M3;
+    } else if (nmax4 >= 3 && M2) {
+      top = 3;
+      tm = M2;
+    } else if (nmax4 >= 2 && M1) {
+      top = 2;
+      tm = M1;
+    } else {
+      top = 1;
+      tm = B0;
+    }
+    if (top < a.n_min) continue;
+    int l = top;
+    int e = c0 + q0 + __ffs(tm) - 1;  // the earliest position at that length
+    if (top == 4 && a.n_max > 4) {
+      for (unsigned mm = M3; mm; mm &= mm - 1u) {
+        const int q = __ffs(mm) - 1;
+        const int ee = c0 + q0 + q;
+        const int lim = min(a.n_max, ee + 1);
+        const int* t = s_tok + kNgMaxN + q0 + q;  // t[-l] = h[ee - l]
+        int ll = 4;
+        while (ll < lim && t[-ll] == s_suf[ll]) ++ll;
+        if (ll > l) {
+          l = ll;
+          e = ee;
         }
       }
     }
+    if (l > best_l) {
+      best_l = l;
+      best_e = e;
+      if (l == a.n_max) break;  // this thread's later positions cannot do better
+    }
   }
+  unsigned long long best =
+      best_l ? (static_cast<unsigned long long>(best_l) << 32) | (0xffffffffu - static_cast<unsigned>(best_e)) : 0ull;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
     const unsigned long long o = __shfl_xor_sync(0xffffffffu, best, off);
