@@ -50,6 +50,12 @@ from speculative_decoding_verification_67_gb300 import synth  # noqa: E402
 METRIC = "verified positions/sec at V=128256; achieved HBM GB/s vs GB300 peak"
 
 
+# DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
+# capture summarised in profiles/head_kernel_stats_B8_K4_V128256.md (rounded to
+# 0.1 MB).  Valid only while head_kernel is unchanged since that capture.
+NCU_TRAFFIC = {"head_B8_K4_V128256": 1_072_900_000}
+
+
 def load_peaks():
     """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, kind)."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -884,7 +890,7 @@ def main():
         roofline = {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs}
     else:
         roofline = {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s", "frac": tflops / peak_tf}
-    roofline.update({"traffic": None, "peak_kind": peak_kind, "launch_ms": head_ms,
+    roofline.update({"traffic": NCU_TRAFFIC.get(w.name), "peak_kind": peak_kind, "launch_ms": head_ms,
                      "kernel": "head_kernel (LM head" + ("" if w.greedy else " + fused softmax statistics") + ")",
                      "bytes_per_launch": head_bytes, "flops_per_launch": nb["flops"],
                      "finish_kernel_ms": finish_ms})
