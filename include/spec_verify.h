@@ -245,6 +245,20 @@ SPEC_API spec_status spec_verify_host(const void *hidden_host, const void *W_lm_
                              spec_dims dims, void *device_workspace, size_t workspace_bytes,
                              spec_stream_t stream);
 
+/* spec_verify_host without the final synchronisation: the copies and the
+ * step are enqueued on `stream` and the call returns.  The host buffers must
+ * stay valid and unmodified, and the outputs must not be read, until the
+ * work on `stream` has completed (e.g. cudaStreamSynchronize or an event);
+ * with pinned host buffers the copies are asynchronous, so a caller can keep
+ * several steps in flight on several streams, each with its own workspace
+ * and buffers. */
+SPEC_API spec_status spec_verify_host_async(const void *hidden_host, const void *W_lm_device,
+                                            const float *draft_logits_host, const int32_t *draft_tokens_host,
+                                            const float *uniforms_host, float temperature,
+                                            int32_t *out_tokens_host, int32_t *out_num_accepted_host,
+                                            spec_dims dims, void *device_workspace, size_t workspace_bytes,
+                                            spec_stream_t stream);
+
 /*
  * Synchronises `stream`, then reads the device error word of `workspace`
  * (the one used by the last spec_verify / spec_verify_from_logits call) into

@@ -82,6 +82,7 @@ _SIGS = {
     "spec_lm_head": (ctypes.c_int, [_VP, _VP, _VP, _I32, _I32, _I32, _VP]),
     "spec_verify_host_workspace_bytes": (_SZ, [SpecDims, _F32]),
     "spec_verify_host": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _SZ, _VP]),
+    "spec_verify_host_async": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _SZ, _VP]),
     "spec_verify_read_error": (ctypes.c_int, [_VP, ctypes.POINTER(_I32), _VP]),
     "spec_verify_from_logits_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _VP]),
     "spec_verify_noalloc_read_error": (ctypes.c_int, [ctypes.POINTER(_I32), _VP]),
@@ -285,11 +286,13 @@ def spec_lm_head(hidden, W_lm, logits=None, stream=None):
 
 
 def spec_verify_host(hidden, W_lm, draft_logits, draft_tokens, uniforms, temperature: float, *,
-                     workspace=None, out_tokens=None, out_num_accepted=None, stream=None):
+                     workspace=None, out_tokens=None, out_num_accepted=None, stream=None, wait: bool = True):
     """spec_verify with the per-step tensors (hidden, draft_logits, draft_tokens,
     uniforms) and the outputs in host memory (pin them for asynchronous
     copies); W_lm stays on the device.  Returns host tensors once they are
-    ready."""
+    ready; with ``wait=False`` (spec_verify_host_async) it returns at once and
+    the outputs are valid after the stream's work completes -- the inputs must
+    stay unmodified until then."""
     B, K = draft_tokens.shape
     V, d = W_lm.shape
     T = float(temperature)
@@ -307,7 +310,8 @@ def spec_verify_host(hidden, W_lm, draft_logits, draft_tokens, uniforms, tempera
     _need(out_num_accepted, "out_num_accepted", torch.int32, (B,), "cpu")
     if workspace is None:
         workspace = torch.empty(host_workspace_bytes(B, K, d, V, T), dtype=torch.uint8, device=W_lm.device)
-    _check(library().spec_verify_host(
+    fn = library().spec_verify_host if wait else library().spec_verify_host_async
+    _check(fn(
         _ptr(hidden), _ptr(W_lm), _ptr(draft_logits if T > 0 else None), _ptr(draft_tokens if K > 0 else None),
         _ptr(uniforms if T > 0 else None), T, _ptr(out_tokens), _ptr(out_num_accepted), SpecDims(B, K, d, V),
         _ptr(workspace), workspace.numel(), _stream(stream)))

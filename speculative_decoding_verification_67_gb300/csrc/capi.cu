@@ -489,10 +489,10 @@ size_t spec_verify_host_workspace_bytes(spec_dims dims, float temperature) {
   return host_stage(dims, temperature).total;
 }
 
-spec_status spec_verify_host(const void* hidden_host, const void* W_lm_device, const float* draft_logits_host,
-                             const int32_t* draft_tokens_host, const float* uniforms_host, float temperature,
-                             int32_t* out_tokens_host, int32_t* out_num_accepted_host, spec_dims dims,
-                             void* device_workspace, size_t workspace_bytes, spec_stream_t stream) {
+spec_status spec_verify_host_async(const void* hidden_host, const void* W_lm_device, const float* draft_logits_host,
+                                   const int32_t* draft_tokens_host, const float* uniforms_host, float temperature,
+                                   int32_t* out_tokens_host, int32_t* out_num_accepted_host, spec_dims dims,
+                                   void* device_workspace, size_t workspace_bytes, spec_stream_t stream) {
   if (!dims_ok(dims, true)) return SPEC_ERR_DIMS;
   if (!hidden_host || !W_lm_device || !out_tokens_host || !out_num_accepted_host) return SPEC_ERR_ARG;
   if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SPEC_ERR_ARG;
@@ -527,8 +527,18 @@ spec_status spec_verify_host(const void* hidden_host, const void* W_lm_device, c
       cudaMemcpyAsync(out_num_accepted_host, ws + h.out_n, static_cast<size_t>(dims.B) * 4,
                       cudaMemcpyDeviceToHost, s) != cudaSuccess)
     return SPEC_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return SPEC_ERR_CUDA;
   return SPEC_OK;
+}
+
+spec_status spec_verify_host(const void* hidden_host, const void* W_lm_device, const float* draft_logits_host,
+                             const int32_t* draft_tokens_host, const float* uniforms_host, float temperature,
+                             int32_t* out_tokens_host, int32_t* out_num_accepted_host, spec_dims dims,
+                             void* device_workspace, size_t workspace_bytes, spec_stream_t stream) {
+  const spec_status st = spec_verify_host_async(hidden_host, W_lm_device, draft_logits_host, draft_tokens_host,
+                                                uniforms_host, temperature, out_tokens_host, out_num_accepted_host,
+                                                dims, device_workspace, workspace_bytes, stream);
+  if (st != SPEC_OK) return st;
+  return cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
 spec_status spec_verify_read_error(const void* workspace, int32_t* error_word, spec_stream_t stream) {

@@ -275,6 +275,35 @@ def test_host_buffer_entry_point_matches_device_entry_point():
     assert torch.equal(tok.cpu(), tok_h) and torch.equal(n.cpu(), n_h)
 
 
+def test_host_async_steps_in_flight_on_two_streams():
+    """spec_verify_host_async: several steps in flight on two streams, each
+    with its own workspace and pinned buffers, give the device entry point's
+    results step by step."""
+    w = synth.custom("host_async", B=6, K=3, d=512, V=7001, temperature=0.9, seed=8)
+    inp = synth.make_inputs(w, device="cuda")
+    us = synth.fresh_uniforms(w.B, w.K, 6, device="cuda", seed=5)
+    ref = []
+    for i in range(6):
+        t, n = sv.spec_verify(inp["hidden"], inp["W"], inp["draft_logits"], inp["draft_tokens"], us[i], 0.9)
+        ref.append((t.cpu(), n.cpu()))
+    host = {k: v.cpu().pin_memory() for k, v in inp.items() if isinstance(v, torch.Tensor) and k != "W"}
+    slots = [dict(stream=torch.cuda.Stream(), ws=torch.empty(sv.host_workspace_bytes(w.B, w.K, w.d, w.V, 0.9),
+                                                             dtype=torch.uint8, device="cuda"))
+             for _ in range(2)]
+    outs = []
+    for i in range(6):
+        sl = slots[i % 2]
+        u = us[i].cpu().pin_memory()
+        ot = torch.empty((w.B, w.K + 1), dtype=torch.int32).pin_memory()
+        on = torch.empty((w.B,), dtype=torch.int32).pin_memory()
+        sv.spec_verify_host(host["hidden"], inp["W"], host["draft_logits"], host["draft_tokens"], u, 0.9,
+                            workspace=sl["ws"], out_tokens=ot, out_num_accepted=on, stream=sl["stream"], wait=False)
+        outs.append((ot, on, u))
+    torch.cuda.synchronize()
+    for (ot, on, _), (rt, rn) in zip(outs, ref):
+        assert torch.equal(ot, rt) and torch.equal(on, rn)
+
+
 # ---------------------------------------------------------------- full-size workloads
 def _sample_rows(B, K, seqs):
     return np.concatenate([np.arange(b * (K + 1), (b + 1) * (K + 1)) for b in seqs])
