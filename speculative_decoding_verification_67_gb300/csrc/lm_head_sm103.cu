@@ -355,10 +355,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  if (blockIdx.x == 0) {
-    if (p.zero_err && threadIdx.x == 0) *p.err = 0;
-    for (int i = threadIdx.x; i < p.n_tickets; i += kThreads) p.tickets[i] = 0u;
-  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -512,6 +508,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;            // TMEM lane quadrant this warp may read
     const int et = threadIdx.x - 64;   // 0..127 among the epilogue threads
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    // This grid may start while the kernel before it in the stream (the
+    // previous step's finishing kernel) still runs: the producer and the MMA
+    // warp only read the weight and the hidden states, which that kernel does
+    // not write, but everything the epilogue writes (logits, partials, the
+    // error word and tickets) may still be read by it, so the epilogue waits
+    // for it before its first such write.
+    bool waited = false;
+    auto wait_prev = [&]() {
+      if (waited) return;
+      griddep_wait();
+      waited = true;
+      if (blockIdx.x == 0) {
+        if (p.zero_err && et == 0) *p.err = 0;
+        for (int i = et; i < p.n_tickets; i += 128) p.tickets[i] = 0u;
+      }
+    };
     // precise statistics keep per-thread running partials instead of
     // reducing every tile across the quadrants
     constexpr bool run_stats = kPrecise && kMode == kModeStats;
@@ -614,6 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < kPrecN; ++i) acc[i] += __ldcg(f + i * 128);
           }
         }
+        wait_prev();
         if constexpr (run_stats) {
           // logits out, and fold this row's value of every column into the
           // thread's running partial of that column (exact rescaling)
@@ -652,6 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after_sync();
+        wait_prev();
         const uint32_t t_row = t_lane + static_cast<uint32_t>(slot * N);
         for (int c0 = 0; c0 < N; c0 += 16) {
           float val[16];
@@ -680,6 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         rph ^= 1u;
       }
     }
+    wait_prev();  // (a CTA that finished no tile still writes its partials and clears the tickets)
     if constexpr (run_stats) {
       // Merge the 128 threads' running partials per column through shared
       // memory (the pipeline stages are idle now: every load has been
@@ -749,6 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (kMode == kModeStats) {
     // ------------------------------------------------------------ draft statistics
+    griddep_wait();  // the draft partials may still be read by the kernel before this one
     draft_stats(p, warp - 6, lane);
   }
 
@@ -809,8 +825,22 @@ cudaError_t launch_variant(const CUtensorMap& map_w, const CUtensorMap& map_h, c
     if (e != cudaSuccess) return e;
     attr_done[dev.device] = true;
   }
-  head_kernel<kPrecN, kMode><<<h.grid, kThreads, h.smem_bytes, stream>>>(map_w, map_h, p);
-  return cudaGetLastError();
+  // the precise scheme is launched as a programmatic dependent of the kernel
+  // before it (see the epilogue's wait): at B=8, V=128256 this hides most of
+  // the previous step's finishing kernel (177 vs 185 us per step); the large
+  // standard-scheme batches measured slightly slower with it, so they launch
+  // plainly
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(h.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = h.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = h.precise ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, head_kernel<kPrecN, kMode>, map_w, map_h, p);
 }
 
 template <int kPrecN>

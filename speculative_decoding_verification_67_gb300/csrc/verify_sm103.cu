@@ -464,6 +464,7 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyArgs a) {
   load_inputs(a, b, ds);
   __syncthreads();  // the drafts in shared memory are read by other warps below
   griddep_wait();
+  griddep_launch_dependents();  // the next kernel may start; the LM head grid is complete
   decide(a, b, ds);
   if (chunk == 0) write_prefix(a, b, ds);
   const Decision& d = ds.d;
@@ -610,6 +611,7 @@ __global__ void __launch_bounds__(kThreads) greedy_finish_kernel(const GreedyArg
   const int b = blockIdx.x;
   const int K = a.K;
   griddep_wait();
+  griddep_launch_dependents();  // the next kernel may start; the LM head grid is complete
   for (int j = 0; j <= K; ++j) {
     const size_t row = static_cast<size_t>(b) * (K + 1) + j;
     const float* pv = a.part_max + row * a.P;
