@@ -103,6 +103,57 @@ def test_verify_from_logits_matches_oracle(B, K, V, T):
     compare_debug(np64(dbg), ref, np_int(n), K, T)
 
 
+def _degenerate_case(kind, B=16, K=4, V=300, T=1.0, seed=0):
+    """Target / draft logit rows of a degenerate shape, drafts drawn from q
+    (Gumbel-max in float64), uniforms U[0, 1)."""
+    g = torch.Generator().manual_seed(seed)
+    if kind == "v1":
+        V = 1
+        zp = torch.zeros((B * (K + 1), V), dtype=torch.float64)
+        zq = torch.zeros((B * K, V), dtype=torch.float64)
+    elif kind == "uniform":
+        zp = torch.zeros((B * (K + 1), V), dtype=torch.float64)
+        zq = torch.zeros((B * K, V), dtype=torch.float64)
+    elif kind == "p_equals_q":
+        zp = torch.randn((B * (K + 1), V), generator=g, dtype=torch.float64) * 2
+        zq = zp.view(B, K + 1, V)[:, :K].reshape(B * K, V).clone()
+    elif kind == "spikes":
+        # target and draft each put (all but) all mass on one token, different ones
+        zp = torch.full((B * (K + 1), V), -1e30, dtype=torch.float64)
+        zq = torch.full((B * K, V), -1e30, dtype=torch.float64)
+        zp[torch.arange(B * (K + 1)), torch.randint(0, V, (B * (K + 1),), generator=g)] = 0.0
+        zq[torch.arange(B * K), torch.randint(0, V, (B * K,), generator=g)] = 0.0
+    else:  # random logits at an extreme temperature
+        zp = torch.randn((B * (K + 1), V), generator=g, dtype=torch.float64) * 2
+        zq = (zp.view(B, K + 1, V)[:, :K].reshape(B * K, V)
+              + 0.5 * torch.randn((B * K, V), generator=g, dtype=torch.float64))
+    zp, zq = zp.float(), zq.float()
+    x = synth.gumbel_max_tokens(zq.double(), T, g).view(B, K)
+    u = torch.rand((B, K + 1), generator=g, dtype=torch.float32)
+    return zp.cuda(), zq.cuda(), x.cuda(), u.cuda(), V
+
+
+@pytest.mark.parametrize("kind,T", [("v1", 1.0), ("uniform", 1.0), ("p_equals_q", 0.7), ("spikes", 1.0),
+                                    ("random", 0.05), ("random", 25.0)])
+def test_degenerate_distributions(kind, T):
+    """V = 1; uniform rows (every draw is a tie of equal steps); p equal to q
+    (everything accepted, the bonus drawn); one-hot target and draft on
+    different tokens (every draft rejected, the residual is the target's
+    spike); extreme temperatures."""
+    zp, zq, x, u, V = _degenerate_case(kind, T=T, seed=len(kind))
+    B, K = x.shape
+    tok, n = sv.spec_verify_from_logits(zp, zq, x, u, T)
+    torch.cuda.synchronize()
+    ref = oracle.verify_sampling(np64(zp).reshape(B, K + 1, V), np64(zq).reshape(B, K, V), np_int(x), np64(u), t32(T))
+    compare_sampling(np_int(tok), np_int(n), ref, K)
+    if kind in ("v1", "uniform", "p_equals_q"):
+        assert (np_int(n) == K).all()
+    if kind == "spikes":
+        spike = np.argmax(np64(zp).reshape(B, K + 1, V)[:, 0], axis=1)
+        same = np_int(x)[:, 0] == spike
+        assert (np_int(n)[~same] == 0).all() and (np_int(tok)[~same, 0] == spike[~same]).all()
+
+
 def test_tiny_logits_workload():
     w = synth.WORKLOADS["tiny_logits"]
     inp = synth.make_inputs(w, device="cuda")
