@@ -531,7 +531,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kRun = run_stats ? kPrecN : 1;
     Partial run[2] = {partial_empty(), partial_empty()};
     float rk[kRun], rs[kRun];
-    uint64_t badmask = 0;
 #pragma unroll
     for (int i = 0; i < kRun; ++i) {
       rk[i] = -INFINITY;
@@ -555,6 +554,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         float acc[kPrecN];
 #pragma unroll
         for (int i = 0; i < kPrecN; ++i) acc[i] = 0.f;
+        if (g0 == 0 && g1 < p.groups) {
+          // The first part of a tile whose other groups belong to the next
+          // CTA(s), each of which stored them before anything else: start
+          // from their sums (the loads' latency then hides behind this tile's
+          // own MMAs instead of following them; the order of the additions
+          // is fixed by the schedule, so results stay deterministic).
+          for (int c2 = blockIdx.x + 1; c2 < static_cast<int>(gridDim.x); ++c2) {
+            if (streamk_start(p, c2) >= static_cast<long long>(tile + 1) * p.groups) break;
+            bool got = true;
+            if (lane == 0) {
+              const unsigned long long* fl = &p.flags[c2 * 4 + q];
+              if (ld_acquire_u64(fl) != p.epoch) {
+                const uint64_t t0 = global_timer_ns();
+                while (ld_acquire_u64(fl) != p.epoch) {
+                  if (global_timer_ns() - t0 > kWaitLimitNs) {
+                    got = false;
+                    break;
+                  }
+                }
+              }
+            }
+            got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+            if (!got) {
+              report_timeout(p.err);
+              continue;
+            }
+            const float* f = p.fix + static_cast<size_t>(c2) * kFixupFloatsPerCta + et;
+#pragma unroll
+            for (int i = 0; i < kPrecN; ++i) acc[i] += __ldcg(f + i * 128);
+          }
+        }
         for (int g = g0; g < g1; ++g) {
           if (!mbar_wait(&afull[slot], sph)) {
             report_timeout(p.err);
@@ -598,56 +628,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           continue;
         }
-        if (g1 < p.groups) {
-          // the first part of a tile whose other groups belong to the next
-          // CTA(s), each of which stored them before anything else
-          for (int c2 = blockIdx.x + 1; c2 < static_cast<int>(gridDim.x); ++c2) {
-            if (streamk_start(p, c2) >= static_cast<long long>(tile + 1) * p.groups) break;
-            bool got = true;
-            if (lane == 0) {
-              const unsigned long long* fl = &p.flags[c2 * 4 + q];
-              if (ld_acquire_u64(fl) != p.epoch) {
-                const uint64_t t0 = global_timer_ns();
-                while (ld_acquire_u64(fl) != p.epoch) {
-                  if (global_timer_ns() - t0 > kWaitLimitNs) {
-                    got = false;
-                    break;
-                  }
-                }
-              }
-            }
-            got = __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
-            if (!got) {
-              report_timeout(p.err);
-              continue;
-            }
-            const float* f = p.fix + static_cast<size_t>(c2) * kFixupFloatsPerCta + et;
-#pragma unroll
-            for (int i = 0; i < kPrecN; ++i) acc[i] += __ldcg(f + i * 128);
-          }
-        }
         wait_prev();
         if constexpr (run_stats) {
           // logits out, and fold this row's value of every column into the
           // thread's running partial of that column (exact rescaling)
           const Expo c{p.c_hi, p.c_lo};
-          if (v < p.V) {
+          const bool in = v < p.V;  // rows past V (last tile) hold zeros and fold nothing
+          // Columns in chunks of 8 with no branch inside a chunk, so that the
+          // chunk's independent chains interleave; columns past M in the last
+          // chunk only see zeros and are never stored or merged.  The
+          // reference of each running partial is an integer >= every value
+          // folded so far and only rises; a rise rescales the sum by an exact
+          // power of two.  Reference and rescale use float adds and integer
+          // ops only (ceilf and float-to-int conversions issue ~12x slower
+          // than an add), and no per-column predicate: a non-finite value
+          // turns its column's sum into NaN, which the merge flags.
 #pragma unroll
-            for (int i = 0; i < kPrecN; ++i) {
-              if (i >= p.M) break;
+          for (int i0 = 0; i0 < kPrecN; i0 += 8) {
+            if (i0 >= p.M) break;
+#pragma unroll
+            for (int i = i0; i < i0 + 8; ++i) {
               const float z = acc[i];
-              p.logits[static_cast<size_t>(i) * p.ldz + v] = z;
+              if (in && i < p.M) p.logits[static_cast<size_t>(i) * p.ldz + v] = z;
               const float h = expo_hi(z, c);
-              if (!isfinite(h)) {
-                badmask |= 1ull << i;
-                continue;
-              }
-              const float kn = ceilf(h);
-              if (kn > rk[i]) {  // the reference rises (rarely after the first tile)
-                rs[i] *= pow2_int(rk[i] - kn);
-                rk[i] = kn;
-              }
-              rs[i] += exp2f((h - rk[i]) + expo_lo(z, h, c));
+              const float rn = fmaxf(rk[i], in ? ref_above(h) : -INFINITY);
+              rs[i] *= pow2_nonpos(rk[i] - rn);
+              rk[i] = rn;
+              const float t = exp2f((h - rn) + expo_lo(z, h, c));
+              rs[i] += in ? t : 0.f;
             }
           }
         } else {
@@ -699,50 +707,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Merge the 128 threads' running partials per column through shared
       // memory (the pipeline stages are idle now: every load has been
       // consumed), several threads per column, then one partial per CTA.
-      // [thread][column] with an odd pitch: thread et's writes and the
-      // column readers' loads both land in distinct banks
-      constexpr int kPitch = kPrecN + 1;
+      // [column][thread]: thread et's writes are consecutive words; a column
+      // reader takes every kTpc-th float4 of its column, and the pitch of
+      // 128 + 4 kTpc words puts the 8 float4 reads of each quarter-warp
+      // phase in distinct banks.
+      constexpr int kTpc = kPrecN == 32 ? 4 : 2;               // threads per column
+      constexpr int kPitch = 128 + 4 * kTpc;
+      constexpr int kVecs = 128 / 4 / kTpc;                    // float4 reads per thread and array
       float* trk = reinterpret_cast<float*>(smem);             // references
-      float* trs = trk + 128 * kPitch;                         // sums
-      uint64_t* bm = reinterpret_cast<uint64_t*>(trs + 128 * kPitch + 2);
+      float* trs = trk + kPrecN * kPitch;                      // sums
 #pragma unroll
       for (int i = 0; i < kPrecN; ++i) {
-        trk[et * kPitch + i] = rk[i];
-        trs[et * kPitch + i] = rs[i];
+        trk[i * kPitch + et] = rk[i];
+        trs[i * kPitch + et] = rs[i];
       }
-      bm[et] = badmask;
       __syncwarp();
       if (lane == 0) mbar_arrive(red_full);
       if (!mbar_wait(red_full, 0)) {
         report_timeout(p.err);
       } else {
-        constexpr int kTpc = kPrecN == 32 ? 4 : 2;             // threads per column
-        constexpr int kSpan = 128 / kTpc;                      // partials each thread reads
         const int col = et / kTpc, part = et % kTpc;
         const bool active = col < kPrecN;
         const int ccol = active ? col : 0;
-        const int t0 = part * kSpan;
+        const float4* rk4 = reinterpret_cast<const float4*>(trk + ccol * kPitch) + part;
+        const float4* rs4 = reinterpret_cast<const float4*>(trs + ccol * kPitch) + part;
         // pass 1: the column's reference = the largest of the 128 references
         float kmax = -INFINITY;
-        int bad = 0;
-#pragma unroll 8
-        for (int t = 0; t < kSpan; ++t) {
-          kmax = fmaxf(kmax, trk[(t0 + t) * kPitch + ccol]);
-          bad |= static_cast<int>((bm[t0 + t] >> ccol) & 1ull);
+#pragma unroll
+        for (int j = 0; j < kVecs; ++j) {
+          const float4 r = rk4[j * kTpc];
+          kmax = fmaxf(kmax, fmaxf(fmaxf(r.x, r.y), fmaxf(r.z, r.w)));
         }
 #pragma unroll
-        for (int off = 1; off < kTpc; off <<= 1) {
-          kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
-          bad |= __shfl_xor_sync(0xffffffffu, bad, off);
-        }
+        for (int off = 1; off < kTpc; off <<= 1) kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
         // pass 2: exact power-of-two scaling to that reference, compensated
         // sum in four independent chains
         float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
         if (kmax != -INFINITY) {
-#pragma unroll 4
-          for (int t = 0; t < kSpan; ++t) {
-            const int idx = (t0 + t) * kPitch + ccol;
-            ff_accumulate(sh[t & 3], sl[t & 3], trs[idx] * pow2_int(trk[idx] - kmax));
+#pragma unroll
+          for (int j = 0; j < kVecs; ++j) {
+            const float4 r = rk4[j * kTpc];
+            const float4 s = rs4[j * kTpc];
+            ff_accumulate(sh[0], sl[0], s.x * pow2_nonpos(r.x - kmax));
+            ff_accumulate(sh[1], sl[1], s.y * pow2_nonpos(r.y - kmax));
+            ff_accumulate(sh[2], sl[2], s.z * pow2_nonpos(r.z - kmax));
+            ff_accumulate(sh[3], sl[3], s.w * pow2_nonpos(r.w - kmax));
           }
         }
         ff sum = ff_norm(sh[0], sl[0]);
@@ -753,7 +762,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         Partial acc;
         acc.k = kmax;
         acc.s = sum;
-        acc.bad = bad;
+        // a non-finite logit made its thread's sum NaN (or the reference +inf)
+        acc.bad = !isfinite(sum.hi) || kmax == INFINITY;
         if (part == 0 && col < kPrecN && col < p.M)
           store_part(&p.tpart[static_cast<size_t>(col) * p.tparts + blockIdx.x], acc);
       }

@@ -4,7 +4,7 @@
 // exp(z/T) is evaluated as 2^(z*c) with c = log2(e)/T carried as a pair of
 // floats, so z*c is exact to ~1e-14 and no rounded temperature or log2(e)
 // scales every exponent the same way.  A partial sum is kept against an
-// integer reference k (the ceiling of its largest exponent): bringing
+// integer reference k (at or a few units above its largest exponent): bringing
 // partials to a common reference is then an exact power of two.  Sums are
 // compensated (TwoSum), so the normalisers carry no systematic error larger
 // than ~1e-12; the only per-token error left is the f32 rounding of one
@@ -59,6 +59,28 @@ __device__ __forceinline__ bool ff_gt(ff a, ff b) { return a.hi > b.hi || (a.hi 
 // and for e = -inf).
 __device__ __forceinline__ float pow2_int(float e) {
   return e >= -126.f ? __int_as_float((static_cast<int>(e) + 127) << 23) : 0.f;
+}
+
+// The same for an integer-valued e <= 0 (0 at or below -127, also for -inf
+// and NaN) without a float-to-int conversion, which issues ~12x slower than
+// a float add on sm_103: adding 1.5 * 2^23 leaves the integer in the low
+// mantissa bits, from which the exponent field is built.
+__device__ __forceinline__ float pow2_nonpos(float e) {
+  const float c = __fadd_rn(fmaxf(e, -127.f), 12582912.f);
+  return __int_as_float((__float_as_int(c) - (0x4B400000 - 127)) << 23);
+}
+
+// An integer-valued reference k with h <= k <= h + 4 for any finite h, from
+// float adds only (ceilf issues ~12x slower than an add on sm_103).  Adding
+// and removing m = +-1.5 * 2^23 (the sign of h) rounds to an integer: the
+// nearest one for |h| < 2^22, so k = rint(h) + 1 in [h + 1/2, h + 3/2]; one
+// within 1 of h for 2^22 <= |h| < 2^23; beyond that h itself is an integer
+// and the max and min keep k within [h, h + 4] (h + 2 may round up by 2).
+// NaN and infinities pass through (as NaN or infinity).
+__device__ __forceinline__ float ref_above(float h) {
+  const float m = __int_as_float((__float_as_int(h) & 0x80000000) | 0x4B400000);  // copysign(1.5 * 2^23, h)
+  const float r = __fadd_rn(__fadd_rn(h, m), -m);
+  return fminf(fmaxf(__fadd_rn(r, 1.f), h), __fadd_rn(h, 2.f));
 }
 
 // a * 2^e, exact (barring underflow).

@@ -232,7 +232,12 @@ def test_determinism_bits():
 
 # ---------------------------------------------------------------- whole step, small
 @pytest.mark.parametrize("B,K,d,V,T", [(3, 3, 256, 5000, 0.8), (1, 5, 512, 32000, 1.0), (5, 0, 128, 1000, 1.0),
-                                       (12, 8, 384, 4099, 1.0)])
+                                       (12, 8, 384, 4099, 1.0),
+                                       (9, 4, 384, 2000, 0.7),      # M = 45: 48 columns, last chunk partial
+                                       (13, 3, 256, 3001, 1.1),     # M = 52: 64 columns
+                                       (8, 7, 512, 7000, 0.9),      # M = 64: every column used
+                                       (2, 3, 256, 3000, 1e-6),     # |z / T| in log2 units around 2^22
+                                       (2, 3, 256, 3000, 1e-8)])    # ... and beyond 2^24
 def test_spec_verify_small(B, K, d, V, T):
     w = synth.custom("small", B=B, K=K, d=d, V=V, temperature=T, seed=B + K + d + V)
     inp, tok, n, logits, dbg = _run_head_case(w)
@@ -297,6 +302,28 @@ def test_nonfinite_logit_marks_the_sequence():
     t3, n3 = sv.spec_verify_from_logits(zp2, zq, x, u, 0.0, workspace=torch.empty(
         sv.workspace_bytes(B, K, V, 0.0), dtype=torch.uint8, device="cuda"))
     assert np_int(n3)[1] == -1
+
+
+def test_nonfinite_hidden_marks_the_sequence():
+    """A NaN or infinite hidden state makes its position's logits non-finite
+    inside the LM head's fused statistics: that sequence is flagged, the
+    others are unaffected."""
+    w = synth.custom("nf_head", B=3, K=2, d=256, V=3000, temperature=1.0, seed=21)
+    inp = synth.make_inputs(w, device="cuda")
+    B, K, V, T = w.B, w.K, w.V, w.temperature
+    ref = oracle.spec_verify(np64(inp["hidden"]), np64(inp["W"]), np64(inp["draft_logits"]),
+                             np_int(inp["draft_tokens"]), np64(inp["uniforms"]), t32(T), B, K)
+    for bad in (float("nan"), float("inf"), float("-inf")):
+        h = inp["hidden"].clone()
+        h[1 * (K + 1) + 2, 5] = bad
+        ws = torch.empty(sv.workspace_bytes(B, K, V, T), dtype=torch.uint8, device="cuda")
+        tok, n = sv.spec_verify(h, inp["W"], inp["draft_logits"], inp["draft_tokens"], inp["uniforms"], T,
+                                workspace=ws)
+        assert sv.read_error(ws) & sv.DEVERR_NONFINITE, bad
+        n, tok = np_int(n), np_int(tok)
+        assert n[1] == -1 and (tok[1] == -1).all(), bad
+        keep = [0, 2]
+        compare_sampling(tok[keep], n[keep], {k: v[keep] for k, v in ref.items() if k != "target_logits"}, K)
 
 
 def test_all_accept_and_first_reject_extremes():
