@@ -53,6 +53,9 @@ constexpr int kThreads = 256;  // 8 warps: producer, MMA, 4 epilogue, 2 draft st
 constexpr uint32_t kABytes = kHeadTileV * kHeadTileK * 2;  // 16 KB W tile per stage
 constexpr uint32_t kBarrierBytes = 512;
 constexpr uint32_t kReduceBytes = 4 * 4 * 256 * 4;         // per-column scratch of the 4 epilogue warps
+constexpr int kArgPitch = 36;                              // floats per row of a warp's 32x32 transpose block
+constexpr uint32_t kArgmaxSmallBytes = 2 * 4 * 256 * 4;    // greedy scratch: [4 warps][256] values and indices
+constexpr uint32_t kArgmaxBytes = kArgmaxSmallBytes + 4 * 32 * kArgPitch * 4;  // + the 4 transpose blocks
 constexpr int kSlotsPrecise = 4;
 constexpr int kGroupPrecise = 4;  // hidden blocks accumulated per TMEM slot (precise scheme)
 
@@ -127,6 +130,86 @@ __device__ __forceinline__ bool work_next(const HeadParams& p, WorkCursor& c, in
   return true;
 }
 
+// Greedy partials of the kCols (16 or 32) columns [c0, c0 + kCols) over the
+// warp's 32 rows, by warp collectives (the small-batch scheme, whose epilogue
+// has time to spare): per column the largest value and the lowest row
+// holding it.
+// Values map to order-preserving unsigned keys (-0 taken as +0 first, so
+// that equal floats give equal keys); one warp max reduction finds the
+// largest key and a ballot the lowest lane with it (the lowest token id).
+// Rows past V and non-finite values take key 0, below every finite value's
+// key; a non-finite value marks the column (index -2).  Lane l keeps column
+// c0 + l's result, so the warp writes the scratch once per array.
+template <int kCols>
+__device__ __forceinline__ void argmax_redux(const HeadParams& p, const float* val, int c0, int v, int q, int lane,
+                                            float* scr) {
+  float* red_val = scr;
+  int* red_idx = reinterpret_cast<int*>(scr + 1024);
+  const bool in = v < p.V;
+  const int v0 = v - lane;  // the warp's first row
+  float my_val = -INFINITY;
+  int my_idx = 0x7fffffff;
+#pragma unroll
+  for (int i = 0; i < kCols; ++i) {
+    const float x = val[i] + 0.f;
+    const bool bad = in && !isfinite(x);
+    const uint32_t u = __float_as_uint(x);
+    const uint32_t key = (in && !bad) ? ((u & 0x80000000u) ? ~u : (u | 0x80000000u)) : 0u;
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+    const uint32_t win = __ballot_sync(0xffffffffu, key == kmax);
+    const bool any_bad = __any_sync(0xffffffffu, bad);
+    if (lane == i) {
+      my_val = kmax == 0u ? -INFINITY : __uint_as_float((kmax & 0x80000000u) ? (kmax & 0x7fffffffu) : ~kmax);
+      my_idx = any_bad ? -2 : (kmax == 0u ? 0x7fffffff : v0 + __ffs(win) - 1);
+    }
+  }
+  if (lane < kCols) {
+    red_val[q * 256 + c0 + lane] = my_val;
+    red_idx[q * 256 + c0 + lane] = my_idx;
+  }
+}
+
+// The same partials for the large-batch scheme, where the epilogue of a
+// 128 x 256 tile must keep pace with its MMAs: the warp's 32 rows x kCols
+// block goes through a per-warp transpose in shared memory (each lane stores
+// its row with 128-bit stores; a pitch of 36 floats keeps every quarter-warp
+// phase and every column read conflict-free), then lane c scans column c0 + c
+// row by row, keeping the first (lowest-id) row of the largest finite value.
+// A few plain instructions per value instead of a chain of warp collectives
+// per column (measured ~49 issued instructions a column with those).
+template <int kCols>
+__device__ __forceinline__ void argmax_transpose(const HeadParams& p, const float* val, int c0, int v, int q,
+                                                 int lane, float* scr) {
+  float* red_val = scr;
+  int* red_idx = reinterpret_cast<int*>(scr + 1024);
+  float* tb = scr + 2048 + q * (32 * kArgPitch);
+  __syncwarp();  // every lane's reads of the previous block are done
+#pragma unroll
+  for (int j = 0; j < kCols; j += 4)
+    *reinterpret_cast<float4*>(tb + lane * kArgPitch + j) = make_float4(val[j], val[j + 1], val[j + 2], val[j + 3]);
+  __syncwarp();
+  const int v0 = v - lane;                // the warp's first row
+  const int rows = min(32, p.V - v0);     // of which inside the vocabulary (may be <= 0)
+  if (lane < kCols) {
+    float best = -INFINITY;
+    int br = -1;
+    bool bad = false;
+#pragma unroll 8
+    for (int r = 0; r < 32; ++r) {
+      const float x = tb[r * kArgPitch + lane];
+      const bool use = r < rows;
+      const bool fin = isfinite(x);
+      bad |= use && !fin;
+      if (use && fin && x > best) {
+        best = x;
+        br = r;
+      }
+    }
+    red_val[q * 256 + c0 + lane] = best;
+    red_idx[q * 256 + c0 + lane] = bad ? -2 : (br < 0 ? 0x7fffffff : v0 + br);
+  }
+}
+
 // Output of 16 columns [c0, c0+16) of this thread's vocabulary row v.
 // Scratch layout (per lane quadrant q and column): argmax uses [0] value,
 // [1] index; statistics use [0] reference k, [1] sum hi, [2] sum lo, [3] bad.
@@ -142,34 +225,7 @@ __device__ __forceinline__ void emit16(const HeadParams& p, const float (&val)[1
       }
     }
   }
-  if (kMode == kModeArgmax) {
-    float* red_val = scr;
-    int* red_idx = reinterpret_cast<int*>(scr + 1024);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      float bv = val[i];
-      int bi = v;
-      const bool bad = (v < p.V) && !isfinite(bv);
-      if (v >= p.V || bad) {
-        bv = -INFINITY;
-        bi = 0x7fffffff;
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-        if (ov > bv || (ov == bv && oi < bi)) {
-          bv = ov;
-          bi = oi;
-        }
-      }
-      const bool any_bad = __any_sync(0xffffffffu, bad);
-      if (lane == 0) {
-        red_val[q * 256 + c0 + i] = bv;
-        red_idx[q * 256 + c0 + i] = any_bad ? -2 : bi;
-      }
-    }
-  }
+  if (kMode == kModeArgmax) argmax_redux<16>(p, val, c0, v, q, lane, scr);
   if (kMode == kModeStats) {
     const Expo c{p.c_hi, p.c_lo};
 #pragma unroll
@@ -675,10 +731,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         wait_prev();
         const uint32_t t_row = t_lane + static_cast<uint32_t>(slot * N);
-        for (int c0 = 0; c0 < N; c0 += 16) {
+        // 32 columns per TMEM load (one wait for two emits), 16 for the tail
+        int c0 = 0;
+        for (; c0 + 32 <= N; c0 += 32) {
+          float v32[32];
+          tmem_load_32(t_row + c0, v32);
+          if constexpr (kMode == kModeArgmax) {
+            argmax_transpose<32>(p, v32, c0, v, q, lane, scr);
+          } else {
+            float lo[16], hi[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              lo[i] = v32[i];
+              hi[i] = v32[16 + i];
+            }
+            emit16<kMode>(p, lo, c0, m0, v, q, lane, scr);
+            emit16<kMode>(p, hi, c0 + 16, m0, v, q, lane, scr);
+          }
+        }
+        if (c0 < N) {
           float val[16];
           tmem_load_16(t_row + c0, val);
-          emit16<kMode>(p, val, c0, m0, v, q, lane, scr);
+          if constexpr (kMode == kModeArgmax)
+            argmax_transpose<16>(p, val, c0, v, q, lane, scr);
+          else
+            emit16<kMode>(p, val, c0, m0, v, q, lane, scr);
         }
         tc_fence_before_sync();
         __syncwarp();
@@ -891,8 +968,10 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
   const size_t stage = kABytes + static_cast<size_t>(h.N) * 128;
   // the cross-quadrant scratch is used by the greedy epilogue and by the
   // per-tile statistics of the standard scheme only
-  const bool scratch = mode == HeadOut::kArgmax || (!h.precise && mode == HeadOut::kStats);
-  const size_t fixed = 1024 + kBarrierBytes + (scratch ? kReduceBytes : 0);
+  size_t scratch = 0;
+  if (mode == HeadOut::kArgmax) scratch = h.precise ? kArgmaxSmallBytes : kArgmaxBytes;
+  if (mode == HeadOut::kStats && !h.precise) scratch = kReduceBytes;
+  const size_t fixed = 1024 + kBarrierBytes + scratch;
   const size_t budget = static_cast<size_t>(dev.max_smem_optin);
   int stages = static_cast<int>((budget - fixed) / stage);
   stages = std::min(12, std::max(2, stages));
