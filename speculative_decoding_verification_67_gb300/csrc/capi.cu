@@ -79,10 +79,11 @@ Layout make_layout(int B, int K, int V, bool greedy, bool logits_in_ws, bool fro
     off += round_up(sv::kFixupBytes);
   }
   if (!greedy) {
-    // the LM head writes one partial per tile, or one per CTA (precise)
+    // the LM head writes one partial per CTA (at most kMaxHeadGrid CTAs) or,
+    // with more than a few position chunks, one per vocabulary tile
     L.tpart = off;
     const size_t parts = from_logits ? static_cast<size_t>(L.CA)
-                                     : std::max(num_vt, static_cast<size_t>(precise_head ? sv::kMaxHeadGrid : 0));
+                                     : std::max(num_vt, static_cast<size_t>(sv::kMaxHeadGrid));
     off += round_up(sizeof(sv::StatPart) * M * parts);
     L.dpart = off;
     off += round_up(sizeof(sv::StatPart) * static_cast<size_t>(B) * K * L.CA);
@@ -260,23 +261,22 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
   hs.dpart = reinterpret_cast<sv::StatPart*>(ws + L.dpart);
   hs.tickets = reinterpret_cast<unsigned*>(reinterpret_cast<int*>(ws) + kCtrlTickets);
   hs.n_tickets = dims.B;
-  int Pt;
-  if (plan.precise) {
-    // small batch: the LM head's epilogue and side warps produce the statistics
-    e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kStats, logits, nullptr, nullptr, &hs, err,
-                        true, dev, s, &enc_fail, ldz, L.fix ? ws + L.fix : nullptr);
-    if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
-    Pt = plan.target_parts;
-  } else {
-    // large batch (compute-bound head): logits, then one statistics pass
-    e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kLogits, logits, nullptr, nullptr, nullptr,
-                        err, true, dev, s, &enc_fail, ldz);
-    if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
-    e = sv::launch_row_stats(logits, draft_logits, M, dims.B * dims.K, dims.V, hs.c_hi, hs.c_lo, hs.tpart, hs.dpart,
-                             nullptr, hs.tickets, hs.n_tickets, s, ldz);
+  // The LM head's epilogue produces the target statistics as it writes the
+  // logits (per CTA in the small-batch scheme, per vocabulary tile in the
+  // large-batch one).  The draft statistics come from the head's side warps
+  // in the small-batch scheme, whose weight stream leaves the SM idle; next
+  // to the large-batch head's tensor-bound MMAs that work slowed them by
+  // ~30 % (B=64, K=8, V=152064), so there a separate streaming pass follows.
+  if (!plan.precise) hs.draft_rows = 0;
+  e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kStats, logits, nullptr, nullptr, &hs, err, true,
+                      dev, s, &enc_fail, ldz, L.fix ? ws + L.fix : nullptr);
+  if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
+  if (!plan.precise) {
+    e = sv::launch_row_stats(nullptr, draft_logits, 0, dims.B * dims.K, dims.V, hs.c_hi, hs.c_lo, nullptr, hs.dpart,
+                             nullptr, nullptr, 0, s, dims.V);
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
-    Pt = L.CA;
   }
+  const int Pt = plan.target_parts;
   if (!mark(1)) return SPEC_ERR_CUDA;
   sv::VerifyArgs a = sampling_args(L, dims, temperature, logits, draft_logits, draft_tokens, uniforms,
                                    out_tokens, out_num_accepted, out_debug, ws, Pt);

@@ -52,7 +52,9 @@ namespace {
 constexpr int kThreads = 256;  // 8 warps: producer, MMA, 4 epilogue, 2 draft statistics
 constexpr uint32_t kABytes = kHeadTileV * kHeadTileK * 2;  // 16 KB W tile per stage
 constexpr uint32_t kBarrierBytes = 512;
-constexpr uint32_t kReduceBytes = 4 * 4 * 256 * 4;         // per-column scratch of the 4 epilogue warps
+constexpr int kRunChunks = 4;                              // position chunks whose partials a CTA keeps running
+constexpr int kStatPitch = 20;                             // floats per row of a warp's 32x16 transpose block
+constexpr uint32_t kStatsBytes = (3 * 4 * 256 + 4 * 32 * kStatPitch) * 4;  // k, sum hi, sum lo [4][256] + blocks
 constexpr int kArgPitch = 36;                              // floats per row of a warp's 32x32 transpose block
 constexpr uint32_t kArgmaxSmallBytes = 2 * 4 * 256 * 4;    // greedy scratch: [4 warps][256] values and indices
 constexpr uint32_t kArgmaxBytes = kArgmaxSmallBytes + 4 * 32 * kArgPitch * 4;  // + the 4 transpose blocks
@@ -210,9 +212,10 @@ __device__ __forceinline__ void argmax_transpose(const HeadParams& p, const floa
   }
 }
 
-// Output of 16 columns [c0, c0+16) of this thread's vocabulary row v.
-// Scratch layout (per lane quadrant q and column): argmax uses [0] value,
-// [1] index; statistics use [0] reference k, [1] sum hi, [2] sum lo, [3] bad.
+// Output of 16 columns [c0, c0+16) of this thread's vocabulary row v: the
+// logits, or the greedy partials of the small-batch scheme.  Scratch layout
+// (per lane quadrant q and column): argmax uses [0] value, [1] index;
+// statistics use [0] reference k, [1] sum hi, [2] sum lo.
 template <int kMode>
 __device__ __forceinline__ void emit16(const HeadParams& p, const float (&val)[16], int c0, int m0, int v, int q,
                                        int lane, float* scr) {
@@ -226,29 +229,55 @@ __device__ __forceinline__ void emit16(const HeadParams& p, const float (&val)[1
     }
   }
   if (kMode == kModeArgmax) argmax_redux<16>(p, val, c0, v, q, lane, scr);
-  if (kMode == kModeStats) {
-    const Expo c{p.c_hi, p.c_lo};
+}
+
+// Softmax partials of the 16 columns [c0, c0 + 16) over the warp's 32 rows
+// (large-batch scheme): the warp's 32 x 16 block goes through a per-warp
+// transpose in shared memory (128-bit stores, pitch kStatPitch); lane
+// (c, h) = (lane & 15, lane >> 4) takes column c0 + c over rows 16h .. 16h+15,
+// the two halves exchange their largest exponent so that both use the same
+// integer reference k = ceil(max z c), and their compensated sums meet in one
+// shuffle.  Written to the scratch as [q][col] k, sum hi, sum lo (NaN sum hi
+// for a column with a non-finite value).
+__device__ __forceinline__ void stats_transpose16(const HeadParams& p, const float* val, int c0, int v, int q,
+                                                  int lane, float* scr) {
+  float* tb = scr + 3072 + q * (32 * kStatPitch);
+  __syncwarp();  // every lane's reads of the previous block are done
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int col = c0 + i;
-      if (m0 + col >= p.M) break;  // uniform across the warp
-      const float z = val[i];
-      const bool in = v < p.V;
-      const float h = expo_hi(z, c);
-      const bool bad = in && !isfinite(h);
-      const float hv = (in && !bad) ? h : -INFINITY;
-      const float hm = warp_max_f(hv);
-      const float kw = (hm == -INFINITY) ? -INFINITY : ceilf(hm);
-      const float t = (hv != -INFINITY) ? exp2f((h - kw) + expo_lo(z, h, c)) : 0.f;
-      const ff sum = warp_sum_ff({t, 0.f});
-      const bool any_bad = __any_sync(0xffffffffu, bad);
-      if (lane == 0) {
-        scr[q * 256 + col] = kw;
-        scr[1024 + q * 256 + col] = sum.hi;
-        scr[2048 + q * 256 + col] = sum.lo;
-        reinterpret_cast<int*>(scr)[3072 + q * 256 + col] = any_bad ? 1 : 0;
-      }
-    }
+  for (int j = 0; j < 16; j += 4)
+    *reinterpret_cast<float4*>(tb + lane * kStatPitch + j) = make_float4(val[j], val[j + 1], val[j + 2], val[j + 3]);
+  __syncwarp();
+  const Expo ce{p.c_hi, p.c_lo};
+  const int c = lane & 15, h = lane >> 4;
+  const int rows = min(32, p.V - (v - lane)) - 16 * h;  // of this lane's 16 rows, inside the vocabulary
+  float z[16], e[16];
+  float hm = -INFINITY;
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    z[i] = tb[(16 * h + i) * kStatPitch + c];
+    e[i] = expo_hi(z[i], ce);
+    const bool use = i < rows;
+    const bool fin = isfinite(e[i]);
+    bad |= use && !fin;
+    if (!(use && fin)) e[i] = -INFINITY;
+    hm = fmaxf(hm, e[i]);
+  }
+  hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 16));
+  bad = (__shfl_xor_sync(0xffffffffu, bad ? 1 : 0, 16) != 0) || bad;
+  const float k = hm == -INFINITY ? -INFINITY : ceilf(hm);
+  float sh = 0.f, sl = 0.f;
+  if (k != -INFINITY) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (e[i] != -INFINITY) ff_accumulate(sh, sl, exp2f((e[i] - k) + expo_lo(z[i], e[i], ce)));
+  }
+  ff sum = ff_norm(sh, sl);
+  sum = ff_add(sum, shfl_xor_ff(sum, 16));
+  if (h == 0) {
+    scr[q * 256 + c0 + c] = k;
+    scr[1024 + q * 256 + c0 + c] = bad ? __int_as_float(0x7fc00000) : sum.hi;
+    scr[2048 + q * 256 + c0 + c] = sum.lo;
   }
 }
 
@@ -264,7 +293,8 @@ __device__ __forceinline__ void store_part(StatPart* dst, const Partial& a) {
 // Softmax partials of one tile's columns: merge the four lane quadrants;
 // fold into the CTA's running partials (one per CTA) or store per tile.
 __device__ __forceinline__ void stats_finish(const HeadParams& p, int N, int vt, int m0, int et, const float* scr,
-                                             Partial (&run)[2]) {
+                                             Partial (&run)[2 * kRunChunks]) {
+  const int pc = m0 / N;  // the tile's position chunk
   int r = 0;
   for (int c = et; c < N; c += 128, ++r) {
     const int m = m0 + c;
@@ -275,11 +305,12 @@ __device__ __forceinline__ void stats_finish(const HeadParams& p, int N, int vt,
       Partial pq;
       pq.k = scr[qq * 256 + c];
       pq.s = {scr[1024 + qq * 256 + c], scr[2048 + qq * 256 + c]};
-      pq.bad = reinterpret_cast<const int*>(scr)[3072 + qq * 256 + c];
+      pq.bad = isnan(pq.s.hi) ? 1 : 0;
+      if (pq.bad) pq.s = {0.f, 0.f};
       acc = partial_merge(acc, pq);
     }
     if (p.per_cta)
-      run[r] = partial_merge(run[r], acc);
+      run[pc * 2 + r] = partial_merge(run[pc * 2 + r], acc);
     else
       store_part(&p.tpart[static_cast<size_t>(m) * p.tparts + vt], acc);
   }
@@ -585,7 +616,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool run_stats = kPrecise && kMode == kModeStats;
     constexpr bool reduce = kMode != kModeLogits && !run_stats;  // cross-quadrant scratch per tile
     constexpr int kRun = run_stats ? kPrecN : 1;
-    Partial run[2] = {partial_empty(), partial_empty()};
+    Partial run[2 * kRunChunks];  // [chunk][column / 128]: running partials of the standard scheme
+#pragma unroll
+    for (int i = 0; i < 2 * kRunChunks; ++i) run[i] = partial_empty();
     float rk[kRun], rs[kRun];
 #pragma unroll
     for (int i = 0; i < kRun; ++i) {
@@ -745,17 +778,23 @@ __global__ void __launch_bounds__(kThreads, 1)
               lo[i] = v32[i];
               hi[i] = v32[16 + i];
             }
-            emit16<kMode>(p, lo, c0, m0, v, q, lane, scr);
-            emit16<kMode>(p, hi, c0 + 16, m0, v, q, lane, scr);
+            emit16<kModeLogits>(p, lo, c0, m0, v, q, lane, scr);
+            emit16<kModeLogits>(p, hi, c0 + 16, m0, v, q, lane, scr);
+            if constexpr (kMode == kModeStats) {
+              stats_transpose16(p, lo, c0, v, q, lane, scr);
+              stats_transpose16(p, hi, c0 + 16, v, q, lane, scr);
+            }
           }
         }
         if (c0 < N) {
           float val[16];
           tmem_load_16(t_row + c0, val);
-          if constexpr (kMode == kModeArgmax)
+          if constexpr (kMode == kModeArgmax) {
             argmax_transpose<16>(p, val, c0, v, q, lane, scr);
-          else
-            emit16<kMode>(p, val, c0, m0, v, q, lane, scr);
+          } else {
+            emit16<kModeLogits>(p, val, c0, m0, v, q, lane, scr);
+            if constexpr (kMode == kModeStats) stats_transpose16(p, val, c0, v, q, lane, scr);
+          }
         }
         tc_fence_before_sync();
         __syncwarp();
@@ -845,9 +884,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           store_part(&p.tpart[static_cast<size_t>(col) * p.tparts + blockIdx.x], acc);
       }
     } else if (kMode == kModeStats && p.per_cta) {
-      int r = 0;
-      for (int c = et; c < N; c += 128, ++r)
-        if (c < p.M) store_part(&p.tpart[static_cast<size_t>(c) * p.tparts + blockIdx.x], run[r]);
+      for (int pc = 0; pc < p.num_chunks; ++pc) {
+        int r = 0;
+        for (int c = et; c < N; c += 128, ++r) {
+          const int m = pc * N + c;
+          if (m < p.M) store_part(&p.tpart[static_cast<size_t>(m) * p.tparts + blockIdx.x], run[pc * 2 + r]);
+        }
+      }
     }
   } else if (kMode == kModeStats) {
     // ------------------------------------------------------------ draft statistics
@@ -970,7 +1013,7 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
   // per-tile statistics of the standard scheme only
   size_t scratch = 0;
   if (mode == HeadOut::kArgmax) scratch = h.precise ? kArgmaxSmallBytes : kArgmaxBytes;
-  if (mode == HeadOut::kStats && !h.precise) scratch = kReduceBytes;
+  if (mode == HeadOut::kStats && !h.precise) scratch = kStatsBytes;
   const size_t fixed = 1024 + kBarrierBytes + scratch;
   const size_t budget = static_cast<size_t>(dev.max_smem_optin);
   int stages = static_cast<int>((budget - fixed) / stage);
@@ -981,7 +1024,10 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
   h.groups = h.precise ? (h.num_kb + kGroupPrecise - 1) / kGroupPrecise : 1;
   const long long units = h.streamk ? static_cast<long long>(h.num_tiles) * h.groups : h.num_tiles;
   h.grid = static_cast<int>(std::min<long long>(units, std::min(dev.sm_count, kMaxHeadGrid)));
-  h.per_cta_partials = h.num_chunks == 1;
+  // one running partial per CTA and target row while a thread's share of
+  // the columns fits in registers (up to kRunChunks position chunks), else
+  // one per vocabulary tile
+  h.per_cta_partials = h.num_chunks <= kRunChunks;
   h.target_parts = h.per_cta_partials ? h.grid : h.num_vt;
   return h;
 }

@@ -30,6 +30,7 @@
 // (max, lowest argmax) partials; greedy_finish_kernel reduces them and
 // compares the drafts with the argmax left to right (section "Một vòng
 // speculative decoding", Bước 3).
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 
@@ -126,61 +127,125 @@ __device__ __forceinline__ void load16(const float* __restrict__ row, int e0, in
 }
 
 // ---------------------------------------------------------------- statistics
-// Softmax partial of one (row, chunk) of given logits; thread partials are
-// merged across the block (exact rescaling), no barrier before the merge.
+constexpr int kStatThreads = 128;  // the per-row statistics pass: 4 warps a block, several blocks an SM
+
+// 32 consecutive values per lane of a 1024-token block [base, base + 1024) of
+// a row, in eight 128-bit loads per lane (lane l holds tokens base + 4(32j + l)
+// .. +3 for j = 0..7, so every load instruction covers 512 contiguous bytes);
+// bit t of `valid` tells whether value t exists.
 template <bool kVec>
-__global__ void __launch_bounds__(kThreads) row_stats_kernel(const float* __restrict__ zp,
-                                                             const float* __restrict__ zq, int M, int V,
-                                                             long long ldp, Expo c, StatPart* tpart, StatPart* dpart,
-                                                             int P, int* err, unsigned* tickets, int n_tickets) {
-  __shared__ Partial sm[kWarps];
-  const int row = blockIdx.x, chunk = blockIdx.y;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (row == 0 && chunk == 0) {
-    if (err && threadIdx.x == 0) *err = 0;
-    for (int i = threadIdx.x; i < n_tickets; i += kThreads) tickets[i] = 0u;
-  }
-  const bool target = row < M;
-  const float* z = target ? zp + static_cast<size_t>(row) * ldp : zq + static_cast<size_t>(row - M) * V;
-  float v[kPer];
-  unsigned valid;
-  load16<kVec>(z, chunk * kChunk + threadIdx.x * kPer, V, v, valid);
-  Partial tp = partial_empty();
-  float hm = -INFINITY;
+__device__ __forceinline__ void load_block32(const float* __restrict__ z, int base, int V, int lane, float (&v)[32],
+                                             unsigned& valid) {
+  valid = 0;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    if (!((valid >> i) & 1u)) continue;
-    const float h = expo_hi(v[i], c);
-    if (!isfinite(h)) {
-      tp.bad = 1;
-      valid &= ~(1u << i);
+  for (int j = 0; j < 8; ++j) {
+    const int e = base + (j * 32 + lane) * 4;
+    if (kVec && e + 3 < V) {
+      const float4 f = __ldg(reinterpret_cast<const float4*>(z + e));
+      v[4 * j] = f.x;
+      v[4 * j + 1] = f.y;
+      v[4 * j + 2] = f.z;
+      v[4 * j + 3] = f.w;
+      valid |= 0xfu << (4 * j);
     } else {
-      hm = fmaxf(hm, h);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const bool in = e + t < V;
+        v[4 * j + t] = in ? z[e + t] : 0.f;
+        valid |= in ? (1u << (4 * j + t)) : 0u;
+      }
     }
   }
-  if (hm != -INFINITY) {
-    tp.k = ceilf(hm);
-    float sh = 0.f, sl = 0.f;
+}
+
+// Folds one lane's 32 values into its running partial: the block reference
+// ceil(max z c) raises the partial's (exact power-of-two rescale), then a
+// compensated sum in two independent chains.  Missing and non-finite values
+// add nothing; a non-finite one marks the partial.
+__device__ __forceinline__ void fold_block32(const float (&v)[32], unsigned valid, Expo c, Partial& lp) {
+  float hm = -INFINITY;
+  unsigned use = 0;  // bit t: value t exists and z c is finite
 #pragma unroll
-    for (int i = 0; i < kPer; ++i)
-      if ((valid >> i) & 1u) ff_accumulate(sh, sl, pow2_rel(v[i], c, tp.k));
-    tp.s = ff_norm(sh, sl);
+  for (int t = 0; t < 32; ++t) {
+    const float h = expo_hi(v[t], c);
+    const bool in = (valid >> t) & 1u;
+    const bool fin = isfinite(h);
+    lp.bad |= (in && !fin) ? 1 : 0;
+    use |= (in && fin) ? (1u << t) : 0u;
+    hm = fmaxf(hm, (in && fin) ? h : -INFINITY);
   }
-  tp = warp_merge(tp);
-  if (lane == 0) sm[warp] = tp;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    Partial acc = sm[0];
-    for (int w = 1; w < kWarps; ++w) acc = partial_merge(acc, sm[w]);
-    StatPart out;
-    out.k = acc.k;
-    out.s_hi = acc.s.hi;
-    out.s_lo = acc.s.lo;
-    out.bad = acc.bad;
-    if (target)
-      tpart[static_cast<size_t>(row) * P + chunk] = out;
-    else
-      dpart[static_cast<size_t>(row - M) * P + chunk] = out;
+  if (hm == -INFINITY) return;
+  const float kn = ceilf(hm);
+  if (lp.k == -INFINITY) {
+    lp.k = kn;
+  } else if (kn > lp.k) {
+    const float sc = pow2_nonpos(lp.k - kn);
+    lp.s = {lp.s.hi * sc, lp.s.lo * sc};
+    lp.k = kn;
+  }
+  float sh0 = lp.s.hi, sl0 = lp.s.lo, sh1 = 0.f, sl1 = 0.f;
+#pragma unroll
+  for (int t = 0; t < 32; t += 2) {
+    const float ha = expo_hi(v[t], c), hb = expo_hi(v[t + 1], c);
+    const float a = exp2f((ha - lp.k) + expo_lo(v[t], ha, c));
+    const float b = exp2f((hb - lp.k) + expo_lo(v[t + 1], hb, c));
+    ff_accumulate(sh0, sl0, ((use >> t) & 1u) ? a : 0.f);
+    ff_accumulate(sh1, sl1, ((use >> (t + 1)) & 1u) ? b : 0.f);
+  }
+  lp.s = ff_add(ff_norm(sh0, sl0), ff_norm(sh1, sl1));
+}
+
+// Softmax partials of given logits, one per (row, 4096-token chunk) unit;
+// rows [0, M) are target rows (stride ldp), the rest draft rows (stride V).
+// Each warp takes whole units (warp-strided over the grid) and streams a
+// unit in four 1024-token blocks, loading the next block before folding the
+// current one, then merges its lanes: no block barrier and no serial merge
+// per unit (one unit per block with a block merge reached ~1.7 TB/s).
+template <bool kVec>
+__global__ void __launch_bounds__(kStatThreads, 3) row_stats_kernel(const float* __restrict__ zp,
+                                                             const float* __restrict__ zq, int M, int V,
+                                                             long long ldp, Expo c, StatPart* tpart, StatPart* dpart,
+                                                             int P, long long units, int* err, unsigned* tickets,
+                                                             int n_tickets) {
+  const int lane = threadIdx.x & 31;
+  if (blockIdx.x == 0) {
+    if (err && threadIdx.x == 0) *err = 0;
+    for (int i = threadIdx.x; i < n_tickets; i += kStatThreads) tickets[i] = 0u;
+  }
+  constexpr int kStatWarps = kStatThreads / 32;
+  const long long nw = static_cast<long long>(gridDim.x) * kStatWarps;
+  for (long long u = static_cast<long long>(blockIdx.x) * kStatWarps + (threadIdx.x >> 5); u < units; u += nw) {
+    const int row = static_cast<int>(u / P), chunk = static_cast<int>(u % P);
+    const float* z = row < M ? zp + static_cast<size_t>(row) * ldp : zq + static_cast<size_t>(row - M) * V;
+    const int base = chunk * kChunk;
+    Partial lp = partial_empty();
+    float cur[32];
+    unsigned cv;
+    load_block32<kVec>(z, base, V, lane, cur, cv);
+#pragma unroll 1
+    for (int blk = 0; blk < kChunk / 1024; ++blk) {
+      float nxt[32];
+      unsigned nv = 0;
+      if (blk + 1 < kChunk / 1024) load_block32<kVec>(z, base + (blk + 1) * 1024, V, lane, nxt, nv);
+      fold_block32(cur, cv, c, lp);
+      if (blk + 1 < kChunk / 1024) {
+#pragma unroll
+        for (int t = 0; t < 32; ++t) cur[t] = nxt[t];
+        cv = nv;
+      }
+    }
+    const Partial wp = warp_merge(lp);
+    if (lane == 0) {
+      StatPart out;
+      out.k = wp.k;
+      out.s_hi = wp.s.hi;
+      out.s_lo = wp.s.lo;
+      out.bad = wp.bad;
+      if (row < M)
+        tpart[static_cast<size_t>(row) * P + chunk] = out;
+      else
+        dpart[static_cast<size_t>(row - M) * P + chunk] = out;
+    }
   }
 }
 
@@ -775,16 +840,27 @@ cudaError_t launch_row_stats(const float* zp, const float* zq, int M, int draft_
                              StatPart* tpart, StatPart* dpart, int* err, unsigned* tickets, int n_tickets,
                              cudaStream_t stream, long long ldp) {
   const int P = (V + kChunk - 1) / kChunk;
-  const dim3 g(M + draft_rows, P);
+  const long long units = static_cast<long long>(M + draft_rows) * P;
+  if (units == 0) return cudaSuccess;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // warps take whole units; as many blocks as fit on the SMs at once
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, row_stats_kernel<true>, kStatThreads, 0);
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(
+      std::min<long long>((units + kStatThreads / 32 - 1) / (kStatThreads / 32), static_cast<long long>(std::max(per_sm, 1)) * sms));
   const Expo c{c_hi, c_lo};
   if (ldp <= 0) ldp = V;
   if (V % 4 == 0 && ldp % 4 == 0 && (reinterpret_cast<uintptr_t>(zp) & 15u) == 0 &&
       (reinterpret_cast<uintptr_t>(zq) & 15u) == 0)
-    row_stats_kernel<true><<<g, kThreads, 0, stream>>>(zp, zq, M, V, ldp, c, tpart, dpart, P, err, tickets,
-                                                       n_tickets);
+    row_stats_kernel<true><<<grid, kStatThreads, 0, stream>>>(zp, zq, M, V, ldp, c, tpart, dpart, P, units, err,
+                                                              tickets, n_tickets);
   else
-    row_stats_kernel<false><<<g, kThreads, 0, stream>>>(zp, zq, M, V, ldp, c, tpart, dpart, P, err, tickets,
-                                                        n_tickets);
+    row_stats_kernel<false><<<grid, kStatThreads, 0, stream>>>(zp, zq, M, V, ldp, c, tpart, dpart, P, units, err,
+                                                               tickets, n_tickets);
   return cudaGetLastError();
 }
 

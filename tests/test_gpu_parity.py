@@ -237,7 +237,9 @@ def test_determinism_bits():
                                        (13, 3, 256, 3001, 1.1),     # M = 52: 64 columns
                                        (8, 7, 512, 7000, 0.9),      # M = 64: every column used
                                        (2, 3, 256, 3000, 1e-6),     # |z / T| in log2 units around 2^22
-                                       (2, 3, 256, 3000, 1e-8)])    # ... and beyond 2^24
+                                       (2, 3, 256, 3000, 1e-8),     # ... and beyond 2^24
+                                       (40, 7, 256, 3001, 0.9),     # M = 320: two position chunks of 160
+                                       (20, 12, 128, 1500, 1.3)])   # M = 260: chunks of 144 and 116 rows
 def test_spec_verify_small(B, K, d, V, T):
     w = synth.custom("small", B=B, K=K, d=d, V=V, temperature=T, seed=B + K + d + V)
     inp, tok, n, logits, dbg = _run_head_case(w)
@@ -304,11 +306,12 @@ def test_nonfinite_logit_marks_the_sequence():
     assert np_int(n3)[1] == -1
 
 
-def test_nonfinite_hidden_marks_the_sequence():
+@pytest.mark.parametrize("B,K", [(3, 2), (24, 4)])   # small-batch and large-batch LM-head schemes
+def test_nonfinite_hidden_marks_the_sequence(B, K):
     """A NaN or infinite hidden state makes its position's logits non-finite
     inside the LM head's fused statistics: that sequence is flagged, the
     others are unaffected."""
-    w = synth.custom("nf_head", B=3, K=2, d=256, V=3000, temperature=1.0, seed=21)
+    w = synth.custom("nf_head", B=B, K=K, d=256, V=3000, temperature=1.0, seed=21 + B)
     inp = synth.make_inputs(w, device="cuda")
     B, K, V, T = w.B, w.K, w.V, w.temperature
     ref = oracle.spec_verify(np64(inp["hidden"]), np64(inp["W"]), np64(inp["draft_logits"]),
@@ -322,7 +325,7 @@ def test_nonfinite_hidden_marks_the_sequence():
         assert sv.read_error(ws) & sv.DEVERR_NONFINITE, bad
         n, tok = np_int(n), np_int(tok)
         assert n[1] == -1 and (tok[1] == -1).all(), bad
-        keep = [0, 2]
+        keep = [b for b in range(B) if b != 1]
         compare_sampling(tok[keep], n[keep], {k: v[keep] for k, v in ref.items() if k != "target_logits"}, K)
 
 
