@@ -159,8 +159,8 @@ __device__ __forceinline__ void load_block32(const float* __restrict__ z, int ba
 }
 
 // Folds one lane's 32 values into its running partial: the block reference
-// ceil(max z c) raises the partial's (exact power-of-two rescale), then a
-// compensated sum in two independent chains.  Missing and non-finite values
+// ceil(max z c) raises the partial's (exact power-of-two rescale), then the
+// block's terms are added.  Missing and non-finite values
 // add nothing; a non-finite one marks the partial.
 __device__ __forceinline__ void fold_block32(const float (&v)[32], unsigned valid, Expo c, Partial& lp) {
   float hm = -INFINITY;
@@ -183,16 +183,21 @@ __device__ __forceinline__ void fold_block32(const float (&v)[32], unsigned vali
     lp.s = {lp.s.hi * sc, lp.s.lo * sc};
     lp.k = kn;
   }
-  float sh0 = lp.s.hi, sl0 = lp.s.lo, sh1 = 0.f, sl1 = 0.f;
+  // the 32 terms (each <= 1) summed pairwise (rounding error <= 5 half-ulps
+  // of the block sum, below the terms' own exp2f error), then added to the
+  // running partial with a compensated add
+  float t[32];
 #pragma unroll
-  for (int t = 0; t < 32; t += 2) {
-    const float ha = expo_hi(v[t], c), hb = expo_hi(v[t + 1], c);
-    const float a = exp2f((ha - lp.k) + expo_lo(v[t], ha, c));
-    const float b = exp2f((hb - lp.k) + expo_lo(v[t + 1], hb, c));
-    ff_accumulate(sh0, sl0, ((use >> t) & 1u) ? a : 0.f);
-    ff_accumulate(sh1, sl1, ((use >> (t + 1)) & 1u) ? b : 0.f);
+  for (int i = 0; i < 32; ++i) {
+    const float h = expo_hi(v[i], c);
+    const float e = exp2f((h - lp.k) + expo_lo(v[i], h, c));
+    t[i] = ((use >> i) & 1u) ? e : 0.f;
   }
-  lp.s = ff_add(ff_norm(sh0, sl0), ff_norm(sh1, sl1));
+#pragma unroll
+  for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) t[i] += t[i + w];
+  lp.s = ff_add_f(lp.s, t[0]);
 }
 
 // Softmax partials of given logits, one per (row, 4096-token chunk) unit;
