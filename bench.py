@@ -882,7 +882,9 @@ def main():
     head_ms = statistics.mean(t[0].elapsed_time(t[1]) for t in evs)
     finish_ms = statistics.mean(t[1].elapsed_time(t[2]) for t in evs)
     nb = step_bytes(w)
-    head_bytes = nb["head"] if w.greedy else nb["step"]  # the fused head also reads the draft logits
+    # the timed interval also covers the draft logits' read (by the head's side
+    # warps at M <= 64, by the statistics pass after the head above that)
+    head_bytes = nb["head"] if w.greedy else nb["step"]
     gbs = head_bytes / (head_ms * 1e-3) / 1e9
     tflops = nb["flops"] / (head_ms * 1e-3) / 1e12
     hbm_time, tc_time = head_bytes / (peak_gbs * 1e9), nb["flops"] / (peak_tf * 1e12)
@@ -891,10 +893,13 @@ def main():
     else:
         roofline = {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s", "frac": tflops / peak_tf}
     roofline.update({"traffic": NCU_TRAFFIC.get(w.name), "peak_kind": peak_kind, "launch_ms": head_ms,
-                     "kernel": "head_kernel (LM head" + ("" if w.greedy else " + fused softmax statistics") + ")",
+                     "kernel": ("head_kernel (LM head)" if w.greedy else
+                                "head_kernel (LM head + fused softmax statistics)" if w.M <= 64 else
+                                "head_kernel (LM head + fused target statistics) + row_stats_kernel (draft statistics)"),
                      "bytes_per_launch": head_bytes, "flops_per_launch": nb["flops"],
                      "finish_kernel_ms": finish_ms})
-    if w.greedy:
+    # the whole step against whichever of the step's bytes or flops binds
+    if nb["step"] / (peak_gbs * 1e9) < nb["flops"] / (peak_tf * 1e12):
         tf = nb["flops"] / (ms_per_step * 1e-3) / 1e12
         roofline_step = {"bound": "tensor", "achieved_tflops": tf, "peak_tflops": peak_tf, "frac": tf / peak_tf}
     else:
