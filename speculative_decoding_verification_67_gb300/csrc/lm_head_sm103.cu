@@ -413,7 +413,7 @@ __device__ __forceinline__ void argmax_finish(const HeadParams& p, int N, int vt
   }
 }
 
-// kPrecN == 0: standard accumulation; kPrecN == 32 or 64: precise
+// kPrecN == 0: standard accumulation; kPrecN == 16, 32, 48 or 64: precise
 // accumulation with N == kPrecN.  kMode: HeadOut as int.
 template <int kPrecN, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -681,7 +681,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after_sync();
-          if constexpr (kPrecN == 48) {
+          if constexpr (kPrecN == 16) {
+            float val[16];
+            tmem_load_16(t_lane + static_cast<uint32_t>(slot * kPrecN), val);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] += val[i];
+          } else if constexpr (kPrecN == 48) {
             float val[48];
             tmem_load_48(t_lane + static_cast<uint32_t>(slot * kPrecN), val);
 #pragma unroll
@@ -827,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // reader takes every kTpc-th float4 of its column, and the pitch of
       // 128 + 4 kTpc words puts the 8 float4 reads of each quarter-warp
       // phase in distinct banks.
-      constexpr int kTpc = kPrecN == 32 ? 4 : 2;               // threads per column
+      constexpr int kTpc = kPrecN == 16 ? 8 : (kPrecN == 32 ? 4 : 2);  // threads per column
       constexpr int kPitch = 128 + 4 * kTpc;
       constexpr int kVecs = 128 / 4 / kTpc;                    // float4 reads per thread and array
       float* trk = reinterpret_cast<float*>(smem);             // references
@@ -990,7 +995,7 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
   HeadPlan h;
   if (M <= 64) {
     h.precise = true;
-    h.N = M <= 32 ? 32 : (M <= 48 ? 48 : 64);
+    h.N = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 48 ? 48 : 64));
     h.num_chunks = 1;
     // tcgen05.alloc takes a power of two >= 32 columns
     uint32_t cols = 32;
@@ -1084,6 +1089,7 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
     p.n_tickets = stats->n_tickets;
   }
   if (!h.precise) return launch_mode<0>(mode, map_w, map_h, p, h, dev, stream);
+  if (h.N == 16) return launch_mode<16>(mode, map_w, map_h, p, h, dev, stream);
   if (h.N == 32) return launch_mode<32>(mode, map_w, map_h, p, h, dev, stream);
   if (h.N == 48) return launch_mode<48>(mode, map_w, map_h, p, h, dev, stream);
   return launch_mode<64>(mode, map_w, map_h, p, h, dev, stream);
