@@ -79,6 +79,31 @@ def test_lm_head_is_deterministic():
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("B,K,T", [(2, 3, 0.9),      # 16-column precise head, stream-K split tiles
+                                   (8, 4, 0.8),      # 48 columns
+                                   (40, 7, 1.1),     # large-batch scheme, two position chunks, fused statistics
+                                   (40, 7, 0.0)])    # large-batch greedy (transposed argmax epilogue)
+def test_whole_step_is_deterministic(B, K, T):
+    """The same inputs twice through the whole step (LM head, statistics,
+    decision, draw): identical logits, tokens, counts and debug fields.  The
+    schedules fix every summation order (stream-K splits, per-CTA running
+    partials, the merges), so nothing may depend on timing."""
+    w = synth.custom("det_step", B=B, K=K, d=512, V=7001, temperature=T, seed=B + K)
+    inp = synth.make_inputs(w, device="cuda")
+    outs = []
+    for _ in range(2):
+        logits = torch.empty((B * (K + 1), w.V), dtype=torch.float32, device="cuda") if T > 0 else None
+        dbg = torch.zeros((B, K + 1, sv.SPEC_DEBUG_FIELDS), dtype=torch.float32, device="cuda")
+        tok, n = sv.spec_verify(inp["hidden"], inp["W"], inp["draft_logits"], inp["draft_tokens"], inp["uniforms"], T,
+                                out_target_logits=logits, out_debug=dbg)
+        torch.cuda.synchronize()
+        outs.append((tok.clone(), n.clone(), dbg.clone(), None if logits is None else logits.clone()))
+    (t1, n1, d1, z1), (t2, n2, d2, z2) = outs
+    assert torch.equal(t1, t2) and torch.equal(n1, n2) and torch.equal(d1, d2)
+    if z1 is not None:
+        assert torch.equal(z1, z2)
+
+
 # ---------------------------------------------------------------- sampling from logits
 def _from_logits_case(B, K, V, T, seed, std=2.0, noise=0.5):
     g = torch.Generator(device="cuda").manual_seed(seed)
@@ -252,7 +277,8 @@ def test_spec_verify_small(B, K, d, V, T):
     print(f"\nspec_verify small {B},{K},{d},{V},{T}: logits {err} {st}")
 
 
-@pytest.mark.parametrize("B,K,d,V", [(4, 4, 256, 3000), (40, 3, 512, 1001), (100, 4, 128, 20000)])
+@pytest.mark.parametrize("B,K,d,V", [(4, 4, 256, 3000), (40, 3, 512, 1001), (100, 4, 128, 20000),
+                                     (16, 4, 256, 4097)])   # M = 80: a 16-column tail in the large-batch epilogue
 def test_greedy_small(B, K, d, V):
     w = synth.custom("greedy", B=B, K=K, d=d, V=V, temperature=0.0, noise=0.2, seed=B * K + V)
     inp, tok, n, _, dbg = _run_head_case(w)
@@ -289,6 +315,32 @@ def test_invalid_draft_token_marks_the_sequence():
     keep = [0, 1, 3]
     sub = {k: v[keep] for k, v in ref.items()}
     compare_sampling(tok[keep], n[keep], sub, K)
+
+
+@pytest.mark.parametrize("M_seq", [1, 16])                 # small-batch and large-batch LM-head schemes
+@pytest.mark.parametrize("lo,hi", [(31, 32), (95, 96), (127, 128), (5, 900), (0, 999)])
+def test_greedy_exact_ties_pick_the_lowest_id(M_seq, lo, hi):
+    """Two identical weight rows that dominate every position's logits give
+    exact ties (same bf16 operands, same accumulation order) across a warp
+    boundary (31/32), a lane-quadrant boundary (95/96), a vocabulary-tile
+    boundary (127/128) and far apart; the greedy target token is the lower
+    id, as in the oracle, and drafts equal to it are all accepted."""
+    B, K, d, V = M_seq, 4, 128, 1000
+    g = torch.Generator(device="cuda").manual_seed(lo * 1000 + hi)
+    base = torch.randn(d, generator=g, device="cuda")
+    hidden = (base + 0.05 * torch.randn((B * (K + 1), d), generator=g, device="cuda")).to(torch.bfloat16)
+    W = 0.01 * torch.randn((V, d), generator=g, device="cuda")
+    W[lo] = 3.0 * base / base.norm()
+    W[hi] = W[lo]
+    W = W.to(torch.bfloat16)
+    x = torch.full((B, K), lo, dtype=torch.int32, device="cuda")
+    tok, n = sv.spec_verify(hidden, W, None, x, None, 0.0)
+    torch.cuda.synchronize()
+    ref = oracle.spec_verify(np64(hidden), np64(W), None, np_int(x), None, 0.0, B, K)
+    assert (ref["argmax"] == lo).all()
+    np.testing.assert_array_equal(np_int(tok), ref["tokens"])
+    np.testing.assert_array_equal(np_int(n), ref["num_accepted"])
+    assert (np_int(n) == K).all()
 
 
 def test_nonfinite_logit_marks_the_sequence():
