@@ -264,7 +264,9 @@ def test_determinism_bits():
                                        (2, 3, 256, 3000, 1e-6),     # |z / T| in log2 units around 2^22
                                        (2, 3, 256, 3000, 1e-8),     # ... and beyond 2^24
                                        (40, 7, 256, 3001, 0.9),     # M = 320: two position chunks of 160
-                                       (20, 12, 128, 1500, 1.3)])   # M = 260: chunks of 144 and 116 rows
+                                       (20, 12, 128, 1500, 1.3),    # M = 260: chunks of 144 and 116 rows
+                                       (100, 10, 128, 2000, 1.0),   # M = 1100: 5 chunks, per-tile partials
+                                       (80, 0, 128, 1000, 1.0)])    # large-batch scheme, bonus draws only
 def test_spec_verify_small(B, K, d, V, T):
     w = synth.custom("small", B=B, K=K, d=d, V=V, temperature=T, seed=B + K + d + V)
     inp, tok, n, logits, dbg = _run_head_case(w)
