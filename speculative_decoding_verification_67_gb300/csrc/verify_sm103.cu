@@ -484,13 +484,9 @@ __device__ __forceinline__ float segment_total(const float (&r)[kPer]) {
 // The smallest token of `chunk` whose cumulative mass base + (prefix through
 // it) exceeds t, or INT_MAX; and the chunk's last token with positive mass
 // (or -1) for the rounding fallback.
-template <bool kVec>
-__device__ void locate_in_chunk(const ResRow& R, int chunk, ff base, ff t, int& y, int& last_pos, ff* sm_ff,
-                                int* sm_i) {
+__device__ void locate_from_terms(const float (&r)[kPer], int e0, ff base, ff t, int& y, int& last_pos, ff* sm_ff,
+                                  int* sm_i) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int e0 = chunk * kChunk + threadIdx.x * kPer;
-  float r[kPer];
-  residual_segment<kVec>(R, e0, r);
   ff excl, total;
   block_excl_scan_ff({segment_total(r), 0.f}, excl, total, sm_ff);
   const ff tb = ff_add(base, excl);
@@ -516,6 +512,15 @@ __device__ void locate_in_chunk(const ResRow& R, int chunk, ff base, ff t, int& 
     last_pos = max(last_pos, sm_i[kWarps + w]);
   }
   __syncthreads();
+}
+
+template <bool kVec>
+__device__ void locate_in_chunk(const ResRow& R, int chunk, ff base, ff t, int& y, int& last_pos, ff* sm_ff,
+                                int* sm_i) {
+  const int e0 = chunk * kChunk + threadIdx.x * kPer;
+  float r[kPer];
+  residual_segment<kVec>(R, e0, r);
+  locate_from_terms(r, e0, base, t, y, last_pos, sm_ff, sm_i);
 }
 
 // grid (sequences) x (chunks of 4096 tokens): the decision (redundantly per
@@ -657,6 +662,129 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyArgs a) {
   __syncthreads();
   int y, last_pos;
   locate_in_chunk<kVec>(R, s_chunk, s_base, s_t, y, last_pos, sm_ff, sm_i);
+  if (threadIdx.x == 0) {
+    if (y == INT_MAX) y = last_pos >= 0 ? last_pos : 0;
+    a.out_tokens[b * (K + 1) + n] = y;
+    if (a.out_debug) {
+      const ff mass = R.rej ? ff_div(s_S, d.S_p) : ff{1.f, 0.f};
+      a.out_debug[static_cast<size_t>(b * (K + 1) + n) * 6 + 5] = mass.hi;
+    }
+  }
+}
+
+// Rows of at most kMaxClusterChunks chunks (V <= 32768): one cluster per
+// sequence with one CTA per chunk.  The chunk masses meet through distributed
+// shared memory after one cluster barrier instead of a global array and a
+// last-CTA ticket, every CTA finds the chunk holding t = u * S, and the CTA
+// owning it locates the token from the residual terms it still holds in
+// registers (no second read of the row pair).  Arithmetic identical to
+// finish_kernel: the same chunk masses in the same order, the same search.
+constexpr int kMaxClusterChunks = 8;
+
+// The cluster's chunk masses of exchange `round` (warp 0): total S, the
+// chunk holding t = S * u, the mass before it, and t.
+__device__ void cluster_chunk_search(float4* s_mass, int round, int C, float u, ff& S, int& cs, ff& base, ff& t) {
+  const int lane = threadIdx.x & 31;
+  ff v{0.f, 0.f};
+  if (lane < C) {
+    const float4 f = ld_cluster_f4(cluster_map(&s_mass[round], static_cast<uint32_t>(lane)));
+    v = {f.x, f.y};
+  }
+  // the same sequential order as the chunk-sum search of finish_kernel: a
+  // warp inclusive scan, lane j holding chunks 0..j
+  ff incl = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    ff o{__shfl_up_sync(0xffffffffu, incl.hi, off), __shfl_up_sync(0xffffffffu, incl.lo, off)};
+    if (lane >= off) incl = ff_add(o, incl);
+  }
+  ff ex{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+  if (lane == 0) ex = {0.f, 0.f};
+  // S as finish_kernel forms it: the warp sum of the chunk masses
+  S = warp_sum_ff(v);
+  t = ff_mul_f(S, u);
+  const unsigned hit = __ballot_sync(0xffffffffu, lane < C && ff_gt(incl, t));
+  const unsigned pos = __ballot_sync(0xffffffffu, lane < C && v.hi > 0.f);
+  if (hit) {
+    cs = __ffs(hit) - 1;
+  } else {  // rounding left t at the very end: the last chunk with mass
+    cs = pos ? 31 - __clz(pos) : 0;
+  }
+  base = {__shfl_sync(0xffffffffu, ex.hi, cs), __shfl_sync(0xffffffffu, ex.lo, cs)};
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kThreads) finish_cluster_kernel(const VerifyArgs a) {
+  __shared__ DecideSmem ds;
+  __shared__ ff sm_ff[kWarps];
+  __shared__ int sm_i[2 * kWarps];
+  __shared__ float4 s_mass[2];  // this CTA's chunk mass, per exchange round (hi, lo)
+  __shared__ ff s_base, s_t, s_S;
+  __shared__ int s_chunk;
+  const int C = a.CB;  // CTAs per cluster = chunks per row
+  const int b = blockIdx.x / C;
+  const int chunk = static_cast<int>(cluster_ctarank());
+  const int lane = threadIdx.x & 31;
+  load_inputs(a, b, ds);
+  __syncthreads();  // the drafts in shared memory are read by other warps below
+  griddep_wait();
+  griddep_launch_dependents();  // the next kernel may start; the LM head grid is complete
+  decide(a, b, ds);
+  if (chunk == 0) write_prefix(a, b, ds);
+  const Decision& d = ds.d;
+  if (d.bad) return;  // every CTA of the cluster decided the same: none waits at a barrier below
+  const int K = a.K;
+  const int n = d.n;
+  ResRow R;
+  R.rej = n < K;
+  R.zp = a.zp + static_cast<size_t>(b * (K + 1) + n) * a.ldp;
+  R.zq = R.rej ? a.zq + static_cast<size_t>(b * K + n) * a.V : nullptr;
+  R.c = {a.c_hi, a.c_lo};
+  R.k_p = d.k_p;
+  R.k_q = d.k_q;
+  R.kh = d.kappa.hi;
+  R.kl = d.kappa.lo;
+  R.V = a.V;
+  const float u = ds.uj[K];
+  const int e0 = chunk * kChunk + threadIdx.x * kPer;
+  float r[kPer];
+  auto chunk_mass = [&](int round) {
+    residual_segment<kVec>(R, e0, r);
+    const ff ws = warp_sum_ff({segment_total(r), 0.f});
+    if (lane == 0) sm_ff[threadIdx.x >> 5] = ws;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      ff total = sm_ff[0];
+      for (int w = 1; w < kWarps; ++w) total = ff_add(total, sm_ff[w]);
+      s_mass[round] = make_float4(total.hi, total.lo, 0.f, 0.f);
+    }
+    cluster_sync();  // every CTA's mass of this round is readable
+    if (threadIdx.x < 32) {
+      ff S, base, t;
+      int cs;
+      cluster_chunk_search(s_mass, round, C, u, S, cs, base, t);
+      if (lane == 0) {
+        s_S = S;
+        s_chunk = cs;
+        s_base = base;
+        s_t = t;
+      }
+    }
+    __syncthreads();
+  };
+  chunk_mass(0);
+  if (!(s_S.hi > 0.f) && R.rej) {
+    // A rejection whose residual has no mass in f32 (impossible in exact
+    // arithmetic): draw from p at that position instead.
+    R.rej = false;
+    R.zq = nullptr;
+    chunk_mass(1);
+  }
+  const int owner = s_chunk;
+  cluster_sync();  // every CTA has read the others' masses: none leaves before
+  if (chunk != owner) return;
+  int y, last_pos;
+  locate_from_terms(r, e0, s_base, s_t, y, last_pos, sm_ff, sm_i);
   if (threadIdx.x == 0) {
     if (y == INT_MAX) y = last_pos >= 0 ? last_pos : 0;
     a.out_tokens[b * (K + 1) + n] = y;
@@ -870,9 +998,28 @@ cudaError_t launch_row_stats(const float* zp, const float* zq, int M, int draft_
 }
 
 cudaError_t launch_verify_sampling(const VerifyArgs& a, cudaStream_t stream) {
-  const dim3 g(a.B, a.CB);
   // 16-byte loads need every target row 16-byte aligned
   const bool vec = a.V % 4 == 0 && a.ldp % 4 == 0 && (reinterpret_cast<uintptr_t>(a.zp) & 15u) == 0;
+  if (a.CB <= kMaxClusterChunks) {
+    // one cluster of CB CTAs per sequence, a programmatic dependent of the head
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.B) * static_cast<unsigned>(a.CB));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(a.CB);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (vec) return cudaLaunchKernelEx(&cfg, finish_cluster_kernel<true>, a);
+    return cudaLaunchKernelEx(&cfg, finish_cluster_kernel<false>, a);
+  }
+  const dim3 g(a.B, a.CB);
   if (vec) return launch_dependent(finish_kernel<true>, g, dim3(kThreads), stream, a);
   return launch_dependent(finish_kernel<false>, g, dim3(kThreads), stream, a);
 }
