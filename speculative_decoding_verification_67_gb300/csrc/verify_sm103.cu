@@ -22,6 +22,11 @@
 //     smallest token whose cumulative mass exceeds u*S (inverse CDF,
 //     ascending token id).
 //
+// Rows of at most 8 chunks (V <= 32768) take finish_cluster_kernel instead:
+// one cluster per sequence, the chunk masses exchanged through distributed
+// shared memory, and the CTA owning the drawn chunk scanning it from the
+// terms it still holds in registers; the same arithmetic, the same tokens.
+//
 // Arithmetic: see verify_math.cuh (exact power-of-two rescaling of
 // partials, float-float sums, exponent map z * log2(e)/T as a float pair);
 // nothing here uses f64 (slow on this part).
