@@ -23,8 +23,10 @@
 //    the greedy path, or the logits plus the softmax(z/T) normaliser
 //    partials of every target row for the sampling path (the epilogue holds
 //    each logit in a register already, so the statistics cost no extra
-//    pass over the logits); in that mode warps 6-7 reduce the draft logits
-//    to the same partials meanwhile, hidden under the weight stream;
+//    pass over the logits); in that mode, in the small-batch scheme, warps 6-7
+//    reduce the draft logits to the same partials meanwhile, hidden under the
+//    weight stream (beside the large-batch scheme's tensor-bound MMAs that
+//    work slowed them, so the caller passes no draft rows there);
 //  * two accumulation schemes.  Standard (any N): one TMEM accumulator per
 //    tile over the whole hidden size, double-buffered so the epilogue of a
 //    tile overlaps the next tile's MMAs.  Precise (N <= 64, the small-batch
