@@ -168,6 +168,39 @@ __device__ __forceinline__ void load_block32(const float* __restrict__ z, int ba
 // block's terms are added.  Missing and non-finite values
 // add nothing; a non-finite one marks the partial.
 __device__ __forceinline__ void fold_block32(const float (&v)[32], unsigned valid, Expo c, Partial& lp) {
+  if (valid == 0xffffffffu) {
+    // Full block: the largest exponent from the largest logit (z -> z c is
+    // monotone, c > 0), the terms without per-value masks.  A non-finite
+    // value makes the block sum non-finite; only then does the block take
+    // the masked path below (same arithmetic otherwise, same result).
+    float zm = v[0];
+#pragma unroll
+    for (int t = 1; t < 32; ++t) zm = fmaxf(zm, v[t]);
+    const float hm = expo_hi(zm, c);
+    if (isfinite(hm)) {
+      const float kn = ceilf(hm);
+      const float k = lp.k == -INFINITY ? kn : fmaxf(lp.k, kn);
+      float t[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float h = expo_hi(v[i], c);
+        t[i] = exp2f((h - k) + expo_lo(v[i], h, c));
+      }
+#pragma unroll
+      for (int w = 16; w > 0; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) t[i] += t[i + w];
+      if (isfinite(t[0])) {
+        if (lp.k != -INFINITY && kn > lp.k) {
+          const float sc = pow2_nonpos(lp.k - kn);
+          lp.s = {lp.s.hi * sc, lp.s.lo * sc};
+        }
+        lp.k = k;
+        lp.s = ff_add_f(lp.s, t[0]);
+        return;
+      }
+    }
+  }
   float hm = -INFINITY;
   unsigned use = 0;  // bit t: value t exists and z c is finite
 #pragma unroll
