@@ -22,10 +22,12 @@
 //     smallest token whose cumulative mass exceeds u*S (inverse CDF,
 //     ascending token id).
 //
-// Rows of at most 8 chunks (V <= 32768) take finish_cluster_kernel instead:
-// one cluster per sequence, the chunk masses exchanged through distributed
-// shared memory, and the CTA owning the drawn chunk scanning it from the
-// terms it still holds in registers; the same arithmetic, the same tokens.
+// Rows of at most 32 chunks (V <= 131072) take finish_cluster_kernel
+// instead: one cluster per sequence (one chunk per CTA up to 8 chunks, two
+// above, so at most 16 CTAs), the chunk masses exchanged through
+// distributed shared memory, and the warps owning the drawn chunk scanning
+// it from the terms they still hold in registers; the same arithmetic, the
+// same tokens.
 //
 // Arithmetic: see verify_math.cuh (exact power-of-two rescaling of
 // partials, float-float sums, exponent map z * log2(e)/T as a float pair);
@@ -36,6 +38,7 @@
 // compares the drafts with the argmax left to right (section "Một vòng
 // speculative decoding", Bước 3).
 #include <algorithm>
+#include <atomic>
 #include <cfloat>
 #include <climits>
 
@@ -51,6 +54,13 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kPer = kChunk / kThreads;  // 16 tokens per thread
 static_assert(kPer == 16, "load16 handles 16 tokens per thread");
 
+// The kThreads threads that hold one chunk: the whole block of finish_kernel,
+// one chunk's warps of a finish_cluster_kernel block (chunk h owns warps
+// h*kWarps .. h*kWarps+kWarps-1).  Named barrier 1 over them alone, and a
+// warp's index among them.
+__device__ __forceinline__ void chunk_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+__device__ __forceinline__ int chunk_warp() { return (threadIdx.x >> 5) % kWarps; }
+
 // ------------------------------------------------------------ block helpers
 __device__ __forceinline__ int warp_max_i(int v) {
 #pragma unroll
@@ -64,10 +74,10 @@ __device__ __forceinline__ int warp_min_i(int v) {
   return v;
 }
 
-// Exclusive prefix sum (thread order) of a float-float value over the block,
-// and the block total.  sm: kWarps pairs.
+// Exclusive prefix sum (thread order) of a float-float value over one
+// chunk's threads, and their total.  sm: kWarps pairs.
 __device__ void block_excl_scan_ff(ff v, ff& excl, ff& total, ff* sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = chunk_warp();
   ff incl = v;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -77,14 +87,14 @@ __device__ void block_excl_scan_ff(ff v, ff& excl, ff& total, ff* sm) {
   ff ex{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
   if (lane == 0) ex = {0.f, 0.f};
   if (lane == 31) sm[warp] = incl;
-  __syncthreads();
+  chunk_sync();
   ff off{0.f, 0.f}, tot{0.f, 0.f};
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) {
     if (w == warp) off = tot;
     tot = ff_add(tot, sm[w]);
   }
-  __syncthreads();
+  chunk_sync();
   excl = ff_add(off, ex);
   total = tot;
 }
@@ -329,20 +339,22 @@ __device__ void load_inputs(const VerifyArgs& a, int b, DecideSmem& ds) {
   for (int j = lane; j <= K; j += 32) ds.uj[j] = a.u[b * (K + 1) + j];
 }
 
-// Merge the partials of every row of sequence b (one warp per row, two
-// passes: the row's largest reference, then the exact-scaled compensated
-// sum), then warp 0 decides.  Ends with a __syncthreads.
+// Merge the partials of every row of sequence b (one warp per row over all
+// the block's warps, two passes: the row's largest reference, then the
+// exact-scaled compensated sum), then warp 0 decides.  Ends with a
+// __syncthreads.
 __device__ void decide(const VerifyArgs& a, int b, DecideSmem& ds) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = static_cast<int>(blockDim.x >> 5);
   const int K = a.K;
   const int nrows = 2 * K + 1;
   // the target logit at each draft, issued now so its latency overlaps the merge
   float zpx = 0.f;
-  if (warp == kWarps - 1 && lane < K) {
+  if (warp == nw - 1 && lane < K) {
     const int xj = ds.xj[lane];
     if (xj >= 0 && xj < a.V) zpx = __ldcg(&a.zp[static_cast<size_t>(b * (K + 1) + lane) * a.ldp + xj]);
   }
-  for (int r = warp; r < nrows; r += kWarps) {
+  for (int r = warp; r < nrows; r += nw) {
     const StatPart* pp = r <= K ? a.tpart + static_cast<size_t>(b * (K + 1) + r) * a.Pt
                                 : a.dpart + static_cast<size_t>(b * K + (r - K - 1)) * a.Pd;
     const int np = r <= K ? a.Pt : a.Pd;
@@ -393,7 +405,7 @@ __device__ void decide(const VerifyArgs& a, int b, DecideSmem& ds) {
       ds.rbad[r] = bad || !(s.hi > 0.f) || !isfinite(s.hi) || !isfinite(kmax);
     }
   }
-  if (warp == kWarps - 1 && lane < K) ds.zpx[lane] = zpx;
+  if (warp == nw - 1 && lane < K) ds.zpx[lane] = zpx;
   __syncthreads();
   if (warp == 0) {
     const Expo c{a.c_hi, a.c_lo};
@@ -524,7 +536,7 @@ __device__ __forceinline__ float segment_total(const float (&r)[kPer]) {
 // (or -1) for the rounding fallback.
 __device__ void locate_from_terms(const float (&r)[kPer], int e0, ff base, ff t, int& y, int& last_pos, ff* sm_ff,
                                   int* sm_i) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, warp = chunk_warp();
   ff excl, total;
   block_excl_scan_ff({segment_total(r), 0.f}, excl, total, sm_ff);
   const ff tb = ff_add(base, excl);
@@ -542,14 +554,14 @@ __device__ void locate_from_terms(const float (&r)[kPer], int e0, ff base, ff t,
     sm_i[warp] = found;
     sm_i[kWarps + warp] = lastp;
   }
-  __syncthreads();
+  chunk_sync();
   y = sm_i[0];
   last_pos = sm_i[kWarps];
   for (int w = 1; w < kWarps; ++w) {
     y = min(y, sm_i[w]);
     last_pos = max(last_pos, sm_i[kWarps + w]);
   }
-  __syncthreads();
+  chunk_sync();
 }
 
 template <bool kVec>
@@ -710,22 +722,29 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyArgs a) {
   }
 }
 
-// Rows of at most kMaxClusterChunks chunks (V <= 32768): one cluster per
-// sequence with one CTA per chunk.  The chunk masses meet through distributed
-// shared memory after one cluster barrier instead of a global array and a
-// last-CTA ticket, every CTA finds the chunk holding t = u * S, and the CTA
-// owning it locates the token from the residual terms it still holds in
-// registers (no second read of the row pair).  Arithmetic identical to
-// finish_kernel: the same chunk masses in the same order, the same search.
-constexpr int kMaxClusterChunks = 8;
+// Rows of at most kMaxClusterChunks chunks (V <= 131072): one cluster per
+// sequence, kCPC chunks per CTA (kCPC * kThreads threads; chunk h of a CTA
+// owns warps h*kWarps .. h*kWarps+kWarps-1).  The chunk masses meet through
+// distributed shared memory after one cluster barrier instead of a global
+// array and a last-CTA ticket, every CTA finds the chunk holding t = u * S,
+// and the warps owning it locate the token from the residual terms they
+// still hold in registers (no second read of the row pair).  Arithmetic
+// identical to finish_kernel: the same chunk masses in the same order, the
+// same search.  Clusters above 8 CTAs are a non-portable size; the launch
+// checks that one fits and otherwise takes finish_kernel.
+constexpr int kMaxClusterCtas = 16;
+constexpr int kMaxClusterChunks = 2 * kMaxClusterCtas;
+static_assert(kMaxClusterChunks <= 32, "one lane per chunk in the chunk search");
 
 // The cluster's chunk masses of exchange `round` (warp 0): total S, the
-// chunk holding t = S * u, the mass before it, and t.
+// chunk holding t = S * u, the mass before it, and t.  Chunk j's mass is
+// slot round*kCPC + j%kCPC of CTA j/kCPC.
+template <int kCPC>
 __device__ void cluster_chunk_search(float4* s_mass, int round, int C, float u, ff& S, int& cs, ff& base, ff& t) {
   const int lane = threadIdx.x & 31;
   ff v{0.f, 0.f};
   if (lane < C) {
-    const float4 f = ld_cluster_f4(cluster_map(&s_mass[round], static_cast<uint32_t>(lane)));
+    const float4 f = ld_cluster_f4(cluster_map(&s_mass[round * kCPC + lane % kCPC], static_cast<uint32_t>(lane / kCPC)));
     v = {f.x, f.y};
   }
   // the same sequential order as the chunk-sum search of finish_kernel: a
@@ -751,24 +770,26 @@ __device__ void cluster_chunk_search(float4* s_mass, int round, int C, float u, 
   base = {__shfl_sync(0xffffffffu, ex.hi, cs), __shfl_sync(0xffffffffu, ex.lo, cs)};
 }
 
-template <bool kVec>
-__global__ void __launch_bounds__(kThreads) finish_cluster_kernel(const VerifyArgs a) {
+template <bool kVec, int kCPC>
+__global__ void __launch_bounds__(kThreads * kCPC, 2) finish_cluster_kernel(const VerifyArgs a) {
   __shared__ DecideSmem ds;
-  __shared__ ff sm_ff[kWarps];
+  __shared__ ff sm_ff[kWarps * kCPC];
   __shared__ int sm_i[2 * kWarps];
-  __shared__ float4 s_mass[2];  // this CTA's chunk mass, per exchange round (hi, lo)
+  __shared__ float4 s_mass[2 * kCPC];  // this CTA's chunk masses, per exchange round (hi, lo)
   __shared__ ff s_base, s_t, s_S;
   __shared__ int s_chunk;
-  const int C = a.CB;  // CTAs per cluster = chunks per row
-  const int b = blockIdx.x / C;
-  const int chunk = static_cast<int>(cluster_ctarank());
-  const int lane = threadIdx.x & 31;
+  const int C = a.CB;                         // chunks per row
+  const int ctas = (C + kCPC - 1) / kCPC;     // CTAs per cluster
+  const int b = blockIdx.x / ctas;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int chunk = rank * kCPC + warp / kWarps;  // C itself (no tokens) in the second half of an odd row's last CTA
   load_inputs(a, b, ds);
   __syncthreads();  // the drafts in shared memory are read by other warps below
   griddep_wait();
   griddep_launch_dependents();  // the next kernel may start; the LM head grid is complete
   decide(a, b, ds);
-  if (chunk == 0) write_prefix(a, b, ds);
+  if (rank == 0) write_prefix(a, b, ds);
   const Decision& d = ds.d;
   if (d.bad) return;  // every CTA of the cluster decided the same: none waits at a barrier below
   const int K = a.K;
@@ -784,23 +805,24 @@ __global__ void __launch_bounds__(kThreads) finish_cluster_kernel(const VerifyAr
   R.kl = d.kappa.lo;
   R.V = a.V;
   const float u = ds.uj[K];
-  const int e0 = chunk * kChunk + threadIdx.x * kPer;
+  const int e0 = chunk * kChunk + (threadIdx.x % kThreads) * kPer;
   float r[kPer];
   auto chunk_mass = [&](int round) {
     residual_segment<kVec>(R, e0, r);
     const ff ws = warp_sum_ff({segment_total(r), 0.f});
-    if (lane == 0) sm_ff[threadIdx.x >> 5] = ws;
+    if (lane == 0) sm_ff[warp] = ws;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      ff total = sm_ff[0];
-      for (int w = 1; w < kWarps; ++w) total = ff_add(total, sm_ff[w]);
-      s_mass[round] = make_float4(total.hi, total.lo, 0.f, 0.f);
+    if (threadIdx.x < kCPC) {
+      const ff* w8 = sm_ff + threadIdx.x * kWarps;
+      ff total = w8[0];
+      for (int w = 1; w < kWarps; ++w) total = ff_add(total, w8[w]);
+      s_mass[round * kCPC + threadIdx.x] = make_float4(total.hi, total.lo, 0.f, 0.f);
     }
-    cluster_sync();  // every CTA's mass of this round is readable
+    cluster_sync();  // every CTA's masses of this round are readable
     if (threadIdx.x < 32) {
       ff S, base, t;
       int cs;
-      cluster_chunk_search(s_mass, round, C, u, S, cs, base, t);
+      cluster_chunk_search<kCPC>(s_mass, round, C, u, S, cs, base, t);
       if (lane == 0) {
         s_S = S;
         s_chunk = cs;
@@ -821,9 +843,10 @@ __global__ void __launch_bounds__(kThreads) finish_cluster_kernel(const VerifyAr
   const int owner = s_chunk;
   cluster_sync();  // every CTA has read the others' masses: none leaves before
   if (chunk != owner) return;
+  // the owning chunk's kThreads threads alone from here (named barrier 1)
   int y, last_pos;
   locate_from_terms(r, e0, s_base, s_t, y, last_pos, sm_ff, sm_i);
-  if (threadIdx.x == 0) {
+  if (threadIdx.x % kThreads == 0) {
     if (y == INT_MAX) y = last_pos >= 0 ? last_pos : 0;
     a.out_tokens[b * (K + 1) + n] = y;
     if (a.out_debug) {
@@ -1035,27 +1058,79 @@ cudaError_t launch_row_stats(const float* zp, const float* zq, int M, int draft_
   return cudaGetLastError();
 }
 
+namespace {
+
+// One cluster of `ctas` CTAs of finish_cluster_kernel<kVec, kCPC> per
+// sequence, a programmatic dependent of the preceding kernel.  `probe`
+// asks instead whether such a cluster can be resident at all (1 yes, 0 no).
+template <bool kVec, int kCPC>
+cudaError_t cluster_finish(const VerifyArgs& a, int ctas, cudaStream_t stream, int* probe) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(a.B) * static_cast<unsigned>(ctas));
+  cfg.blockDim = dim3(kThreads * kCPC);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(ctas);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (probe) {
+    if (ctas > 8) {
+      cudaError_t e = cudaFuncSetAttribute(finish_cluster_kernel<kVec, kCPC>,
+                                           cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        *probe = 0;
+        return cudaSuccess;
+      }
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, finish_cluster_kernel<kVec, kCPC>, &cfg);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    *probe = (e == cudaSuccess && clusters > 0) ? 1 : 0;
+    return cudaSuccess;
+  }
+  return cudaLaunchKernelEx(&cfg, finish_cluster_kernel<kVec, kCPC>, a);
+}
+
+template <int kCPC>
+cudaError_t cluster_finish_any(const VerifyArgs& a, bool vec, int ctas, cudaStream_t stream, int* probe) {
+  return vec ? cluster_finish<true, kCPC>(a, ctas, stream, probe) : cluster_finish<false, kCPC>(a, ctas, stream, probe);
+}
+
+// Whether clusters of `ctas` CTAs (kCPC = 2 when above 8) fit on this
+// device, probed once per (size, load width) and process: 0 unknown, 1 yes, 2 no.
+std::atomic<int> g_cluster_fits[kMaxClusterCtas + 1][2];
+
+}  // namespace
+
 cudaError_t launch_verify_sampling(const VerifyArgs& a, cudaStream_t stream) {
   // 16-byte loads need every target row 16-byte aligned
   const bool vec = a.V % 4 == 0 && a.ldp % 4 == 0 && (reinterpret_cast<uintptr_t>(a.zp) & 15u) == 0;
   if (a.CB <= kMaxClusterChunks) {
-    // one cluster of CB CTAs per sequence, a programmatic dependent of the head
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.B) * static_cast<unsigned>(a.CB));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(a.CB);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    if (vec) return cudaLaunchKernelEx(&cfg, finish_cluster_kernel<true>, a);
-    return cudaLaunchKernelEx(&cfg, finish_cluster_kernel<false>, a);
+    // up to 8 chunks: one CTA per chunk; above: two chunks per CTA
+    const bool two = a.CB > kMaxClusterChunks / 4;
+    const int ctas = two ? (a.CB + 1) / 2 : a.CB;
+    std::atomic<int>& fits = g_cluster_fits[ctas][vec ? 1 : 0];
+    int f = fits.load(std::memory_order_relaxed);
+    if (f == 0) {
+      int ok = 0;
+      if (two) cluster_finish_any<2>(a, vec, ctas, stream, &ok);
+      else cluster_finish_any<1>(a, vec, ctas, stream, &ok);
+      f = ok ? 1 : 2;
+      fits.store(f, std::memory_order_relaxed);
+    }
+    if (f == 1) {
+      if (two) return cluster_finish_any<2>(a, vec, ctas, stream, nullptr);
+      return cluster_finish_any<1>(a, vec, ctas, stream, nullptr);
+    }
   }
   const dim3 g(a.B, a.CB);
   if (vec) return launch_dependent(finish_kernel<true>, g, dim3(kThreads), stream, a);

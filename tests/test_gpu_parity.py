@@ -116,7 +116,11 @@ def _from_logits_case(B, K, V, T, seed, std=2.0, noise=0.5):
 
 
 @pytest.mark.parametrize("B,K,V,T", [(1, 4, 1000, 1.0), (64, 4, 1000, 1.0), (33, 7, 8193, 0.8),
-                                     (16, 0, 5000, 1.0), (8, 32, 3000, 1.3), (200, 3, 1001, 0.7)])
+                                     (16, 0, 5000, 1.0), (8, 32, 3000, 1.3), (200, 3, 1001, 0.7),
+                                     # rows of 4096-token chunks: 9 chunks on 5 CTAs (the last CTA's
+                                     # second chunk empty), 25 on 13, 32 on 16, and 35 (no cluster)
+                                     (3, 4, 36000, 0.9), (3, 3, 100000, 1.0), (2, 4, 131072, 0.8),
+                                     (2, 3, 140000, 1.0)])
 def test_verify_from_logits_matches_oracle(B, K, V, T):
     zp, zq, x, u = _from_logits_case(B, K, V, T, seed=B * 131 + K * 7 + V)
     dbg = torch.zeros((B, K + 1, sv.SPEC_DEBUG_FIELDS), device="cuda")
@@ -174,6 +178,27 @@ def test_degenerate_distributions(kind, T):
     if kind in ("v1", "uniform", "p_equals_q"):
         assert (np_int(n) == K).all()
     if kind == "spikes":
+        spike = np.argmax(np64(zp).reshape(B, K + 1, V)[:, 0], axis=1)
+        same = np_int(x)[:, 0] == spike
+        assert (np_int(n)[~same] == 0).all() and (np_int(tok)[~same, 0] == spike[~same]).all()
+
+
+@pytest.mark.parametrize("V", [36000, 100000, 131072, 140000])
+@pytest.mark.parametrize("kind", ["spikes", "p_equals_q"])
+def test_degenerate_distributions_large_vocabulary(kind, V):
+    """The degenerate rows over many 4096-token chunks: each rejected
+    sequence draws exactly the target's spike wherever it lies (any chunk of
+    any CTA of the row); with p = q every draft passes and the bonus comes
+    from p_K."""
+    zp, zq, x, u, V = _degenerate_case(kind, B=6, K=3, V=V, T=1.0, seed=V + len(kind))
+    B, K = x.shape
+    tok, n = sv.spec_verify_from_logits(zp, zq, x, u, 1.0)
+    torch.cuda.synchronize()
+    ref = oracle.verify_sampling(np64(zp).reshape(B, K + 1, V), np64(zq).reshape(B, K, V), np_int(x), np64(u), t32(1.0))
+    compare_sampling(np_int(tok), np_int(n), ref, K)
+    if kind == "p_equals_q":
+        assert (np_int(n) == K).all()
+    else:
         spike = np.argmax(np64(zp).reshape(B, K + 1, V)[:, 0], axis=1)
         same = np_int(x)[:, 0] == spike
         assert (np_int(n)[~same] == 0).all() and (np_int(tok)[~same, 0] == spike[~same]).all()
