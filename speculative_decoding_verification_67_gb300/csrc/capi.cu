@@ -158,6 +158,7 @@ sv::VerifyArgs sampling_args(const Layout& L, const spec_dims& d, float T, const
   a.Pt = Pt;
   a.Pd = L.CA;
   a.res_sums = reinterpret_cast<float2*>(ws + L.res);
+  a.G = 1;
   a.CB = L.CA;
   return a;
 }

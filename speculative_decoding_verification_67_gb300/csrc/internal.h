@@ -122,6 +122,7 @@ struct VerifyArgs {
   int Pt, Pd;
   float2* res_sums;         // [B][CB]
   int CB;
+  int G;                    // chunks per CTA of the grid finishing kernel (set at launch)
 };
 
 // log2(e) / T split into a float pair.

@@ -509,10 +509,12 @@ __device__ __forceinline__ float residual_term(float zp, float zq, const ResRow&
   return fmaxf(0.f, ep - fmaf(R.kh, eq, R.kl * eq));
 }
 
+// The row pair's 16 logits of tokens e0 .. e0+15 (the draft row only at a
+// rejection), and their residual terms.
 template <bool kVec>
-__device__ __forceinline__ void residual_segment(const ResRow& R, int e0, float (&r)[kPer]) {
-  float zp[kPer], zq[kPer];
-  unsigned valid, vq;
+__device__ __forceinline__ void load_pair(const ResRow& R, int e0, float (&zp)[kPer], float (&zq)[kPer],
+                                          unsigned& valid) {
+  unsigned vq;
   load16<kVec>(R.zp, e0, R.V, zp, valid);
   if (R.rej) {
     load16<kVec>(R.zq, e0, R.V, zq, vq);
@@ -520,8 +522,20 @@ __device__ __forceinline__ void residual_segment(const ResRow& R, int e0, float 
 #pragma unroll
     for (int i = 0; i < kPer; ++i) zq[i] = 0.f;
   }
+}
+
+__device__ __forceinline__ void pair_terms(const ResRow& R, const float (&zp)[kPer], const float (&zq)[kPer],
+                                           unsigned valid, float (&r)[kPer]) {
 #pragma unroll
   for (int i = 0; i < kPer; ++i) r[i] = ((valid >> i) & 1u) ? residual_term(zp[i], zq[i], R) : 0.f;
+}
+
+template <bool kVec>
+__device__ __forceinline__ void residual_segment(const ResRow& R, int e0, float (&r)[kPer]) {
+  float zp[kPer], zq[kPer];
+  unsigned valid;
+  load_pair<kVec>(R, e0, zp, zq, valid);
+  pair_terms(R, zp, zq, valid, r);
 }
 
 __device__ __forceinline__ float segment_total(const float (&r)[kPer]) {
@@ -573,25 +587,28 @@ __device__ void locate_in_chunk(const ResRow& R, int chunk, ff base, ff t, int& 
   locate_from_terms(r, e0, base, t, y, last_pos, sm_ff, sm_i);
 }
 
-// grid (sequences) x (chunks of 4096 tokens): the decision (redundantly per
-// CTA), the residual mass of the row pair at the first rejection (or of
-// the bonus row) per chunk, and, in the last CTA of the sequence, the
-// inverse-CDF draw.
+// grid (sequences) x (groups of a.G consecutive chunks of 4096 tokens, G
+// sized at launch so that the grid fits the SMs at once): the decision
+// (redundantly per CTA), the residual mass of the row pair at the first
+// rejection (or of the bonus row) per chunk, and, in the last CTA of the
+// sequence, the inverse-CDF draw.
 template <bool kVec>
 __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyArgs a) {
   __shared__ DecideSmem ds;
   __shared__ ff sm_ff[kWarps];
+  __shared__ ff sm_w[2][kWarps];  // per-chunk warp masses, alternating buffers
   __shared__ int sm_i[2 * kWarps];
   __shared__ ff s_base, s_t, s_S;
   __shared__ int s_chunk;
-  const int b = blockIdx.x, chunk = blockIdx.y;
-  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x, grp = blockIdx.y;
+  const int c0 = grp * a.G, c1 = min(a.CB, c0 + a.G);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   load_inputs(a, b, ds);
   __syncthreads();  // the drafts in shared memory are read by other warps below
   griddep_wait();
   griddep_launch_dependents();  // the next kernel may start; the LM head grid is complete
   decide(a, b, ds);
-  if (chunk == 0) write_prefix(a, b, ds);
+  if (grp == 0) write_prefix(a, b, ds);
   const Decision& d = ds.d;
   if (d.bad) return;
   const int K = a.K;
@@ -608,18 +625,28 @@ __global__ void __launch_bounds__(kThreads) finish_kernel(const VerifyArgs a) {
   R.V = a.V;
 
   {
-    float r[kPer];
-    residual_segment<kVec>(R, chunk * kChunk + threadIdx.x * kPer, r);
-    const ff ws = warp_sum_ff({segment_total(r), 0.f});
-    if (lane == 0) sm_ff[threadIdx.x >> 5] = ws;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      ff total = sm_ff[0];
-      for (int w = 1; w < kWarps; ++w) total = ff_add(total, sm_ff[w]);
-      a.res_sums[static_cast<size_t>(b) * a.CB + chunk] = make_float2(total.hi, total.lo);
+    // chunk by chunk; the next chunk's loads are in flight while this
+    // chunk's terms are reduced
+    const int t0 = threadIdx.x * kPer;
+    float zp[kPer], zq[kPer];
+    unsigned valid;
+    load_pair<kVec>(R, c0 * kChunk + t0, zp, zq, valid);
+    for (int c = c0; c < c1; ++c) {
+      float r[kPer];
+      pair_terms(R, zp, zq, valid, r);
+      if (c + 1 < c1) load_pair<kVec>(R, (c + 1) * kChunk + t0, zp, zq, valid);
+      const ff ws = warp_sum_ff({segment_total(r), 0.f});
+      ff* sw = sm_w[(c - c0) & 1];
+      if (lane == 0) sw[warp] = ws;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        ff total = sw[0];
+        for (int w = 1; w < kWarps; ++w) total = ff_add(total, sw[w]);
+        a.res_sums[static_cast<size_t>(b) * a.CB + c] = make_float2(total.hi, total.lo);
+      }
     }
   }
-  if (!last_block_ticket(&a.tickets[b], static_cast<unsigned>(a.CB), sm_i)) return;
+  if (!last_block_ticket(&a.tickets[b], gridDim.y, sm_i)) return;
 
   const float2* sums = a.res_sums + static_cast<size_t>(b) * a.CB;
   const float u = ds.uj[K];
@@ -1109,6 +1136,9 @@ cudaError_t cluster_finish_any(const VerifyArgs& a, bool vec, int ctas, cudaStre
 // device, probed once per (size, load width) and process: 0 unknown, 1 yes, 2 no.
 std::atomic<int> g_cluster_fits[kMaxClusterCtas + 1][2];
 
+// CTAs of finish_kernel<kVec> resident on the device at once (0 unknown).
+std::atomic<int> g_finish_resident[2];
+
 }  // namespace
 
 cudaError_t launch_verify_sampling(const VerifyArgs& a, cudaStream_t stream) {
@@ -1132,9 +1162,26 @@ cudaError_t launch_verify_sampling(const VerifyArgs& a, cudaStream_t stream) {
       return cluster_finish_any<1>(a, vec, ctas, stream, nullptr);
     }
   }
-  const dim3 g(a.B, a.CB);
-  if (vec) return launch_dependent(finish_kernel<true>, g, dim3(kThreads), stream, a);
-  return launch_dependent(finish_kernel<false>, g, dim3(kThreads), stream, a);
+  // chunks per CTA: as few as let the whole grid be resident at once
+  std::atomic<int>& resident = g_finish_resident[vec ? 1 : 0];
+  int res = resident.load(std::memory_order_relaxed);
+  if (res == 0) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+      e = vec ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, finish_kernel<true>, kThreads, 0)
+              : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, finish_kernel<false>, kThreads, 0);
+    if (e != cudaSuccess) return e;
+    res = std::max(1, per_sm * sms);
+    resident.store(res, std::memory_order_relaxed);
+  }
+  VerifyArgs g_args = a;
+  const long long units = static_cast<long long>(a.B) * a.CB;
+  g_args.G = static_cast<int>(std::min<long long>(a.CB, std::max<long long>(1, (units + res - 1) / res)));
+  const dim3 g(a.B, (a.CB + g_args.G - 1) / g_args.G);
+  if (vec) return launch_dependent(finish_kernel<true>, g, dim3(kThreads), stream, g_args);
+  return launch_dependent(finish_kernel<false>, g, dim3(kThreads), stream, g_args);
 }
 
 cudaError_t launch_greedy_finish(const GreedyArgs& a, cudaStream_t stream) {
