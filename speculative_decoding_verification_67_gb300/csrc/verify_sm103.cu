@@ -1178,8 +1178,10 @@ cudaError_t launch_verify_sampling(const VerifyArgs& a, cudaStream_t stream) {
   }
   VerifyArgs g_args = a;
   const long long units = static_cast<long long>(a.B) * a.CB;
-  g_args.G = static_cast<int>(std::min<long long>(a.CB, std::max<long long>(1, (units + res - 1) / res)));
-  const dim3 g(a.B, (a.CB + g_args.G - 1) / g_args.G);
+  int G = static_cast<int>(std::min<long long>(a.CB, std::max<long long>(1, (units + res - 1) / res)));
+  while (G < a.CB && static_cast<long long>(a.B) * ((a.CB + G - 1) / G) > res) ++G;  // whole groups per row
+  g_args.G = G;
+  const dim3 g(a.B, (a.CB + G - 1) / G);
   if (vec) return launch_dependent(finish_kernel<true>, g, dim3(kThreads), stream, g_args);
   return launch_dependent(finish_kernel<false>, g, dim3(kThreads), stream, g_args);
 }

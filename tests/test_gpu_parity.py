@@ -121,8 +121,9 @@ def _from_logits_case(B, K, V, T, seed, std=2.0, noise=0.5):
                                      # second chunk empty), 25 on 13, 32 on 16, and 35 (no cluster)
                                      (3, 4, 36000, 0.9), (3, 3, 100000, 1.0), (2, 4, 131072, 0.8),
                                      (2, 3, 140000, 1.0),
-                                     # 16 x 35 chunks exceed the resident CTAs: two chunks per CTA
-                                     (16, 2, 140000, 0.9)])
+                                     # 40 x 35 chunks exceed any residency (8 CTAs x 152 SMs): several
+                                     # chunks per CTA, the last group of a row shorter
+                                     (40, 1, 140000, 0.9)])
 def test_verify_from_logits_matches_oracle(B, K, V, T):
     zp, zq, x, u = _from_logits_case(B, K, V, T, seed=B * 131 + K * 7 + V)
     dbg = torch.zeros((B, K + 1, sv.SPEC_DEBUG_FIELDS), device="cuda")
