@@ -4,7 +4,9 @@
 // target row and draft row come from the LM-head kernel (its epilogue and
 // two side warps) or, on given logits, from row_stats_kernel.  Then one
 // launch, chained with programmatic dependent launch: finish_kernel, grid
-// (sequences) x (chunks of 4096 tokens).  Every CTA of a sequence
+// (sequences) x (groups of consecutive chunks of 4096 tokens, as few
+// chunks per CTA as let the grid be resident at once).  Every CTA of a
+// sequence
 //
 //  1. merges the partials of the sequence's 2K+1 rows into their
 //     normalisers (page "quochung.cyou" A.I article, section "Forward pass":
@@ -14,7 +16,7 @@
 //     accepted prefix with one warp ballot (section "Áp dụng thuật toán":
 //     left to right, stop at the first rejection) -- the same arithmetic in
 //     every CTA, so the same decision, with no exchange between CTAs;
-//  2. reduces its chunk of the row pair at the first rejection n_b to the
+//  2. reduces its chunks of the row pair at the first rejection n_b to the
 //     mass of max(0, p - q) (section "Khi reject thì lấy token từ đâu?"), or
 //     of p_K for the bonus token when n_b = K.  The last CTA of the
 //     sequence (atomic ticket; no CTA ever waits for another) finds the
