@@ -2,13 +2,15 @@
 // Token Draft secara Paralel", section "Sampling eksak memerlukan aturan
 // koreksi").  Declared in include/spec_tree.h.
 //
-// Sampling: one thread-block cluster of kTC CTAs per sequence.  CTA r owns
+// Sampling: one thread-block cluster of kC CTAs per sequence: 16 or 12 (a
+// non-portable size) when that many clusters of all B trees are resident at
+// once, else 8.  CTA r owns
 // the vocabulary slice [r*S, (r+1)*S) and keeps the current node's target and
 // draft rows of that slice in shared memory, as probabilities.  Every
 // reduction of the walk -- a node's two softmax normalisers, the residual
 // mass after a rejection, the slice masses of the final draw -- is a block
 // reduction followed by an exchange of one value per CTA through distributed
-// shared memory; every CTA merges the kTC values in rank order, so all of
+// shared memory; every CTA merges the kC values in rank order, so all of
 // them reach the same decisions and walk the tree in lockstep.  A rejection
 // costs one pass over shared memory and one cluster barrier; the rows of a
 // node are read from HBM / L2 once, when the walk reaches it.
@@ -23,6 +25,7 @@
 #include <climits>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 
 #include "internal.h"
 #include "sm103_ptx.cuh"
@@ -32,7 +35,8 @@
 namespace sv {
 namespace {
 
-constexpr int kTC = 8;            // CTAs per cluster (one cluster per sequence)
+constexpr int kTC = 8;            // CTAs per cluster (one cluster per sequence): the portable size
+constexpr int kTCMax = 16;        // the largest (non-portable) size
 constexpr int kTT = 512;          // threads per CTA
 constexpr int kTW = kTT / 32;
 constexpr int kMaxSlice = 24576;  // vocabulary entries per CTA
@@ -66,8 +70,8 @@ struct TreeShared {
   int si[2 * kTW];
   float4 res;  // broadcast of a block or cluster reduction
   int res_i;
-  ff pre[kTC + 1];
-  float zs[kTC];
+  ff pre[kTCMax + 1];
+  float zs[kTCMax];
   int flag;
   uint64_t bar;  // completion of the node-row bulk copies
 };
@@ -116,11 +120,12 @@ __device__ __forceinline__ float4 fetch(TreeShared& sh, int ph, int which, int r
   return ld_cluster_f4(cluster_map(&sh.ex[ph][which], static_cast<uint32_t>(rank)));
 }
 
+template <int kC>
 __device__ ff cluster_sum_ff(TreeShared& sh, int ph) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp == 0) {
     ff v = {0.f, 0.f};
-    if (lane < kTC) {
+    if (lane < kC) {
       const float4 f = fetch(sh, ph, 0, lane);
       v = ff{f.x, f.y};
     }
@@ -136,25 +141,26 @@ __device__ ff cluster_sum_ff(TreeShared& sh, int ph) {
 // Inclusive prefix over ranks of the pass's published float pairs (x, y of
 // value 0); lane r of warp 0 holds rank r's.  Returns the prefix ending at
 // `rank` in pre_end and the total.
-__device__ void cluster_scan_ff(TreeShared& sh, int ph, ff* pre /*[kTC + 1]*/, float* zs /*[kTC]*/) {
+template <int kC>
+__device__ void cluster_scan_ff(TreeShared& sh, int ph, ff* pre /*[kC + 1]*/, float* zs /*[kC]*/) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp == 0) {
-    float4 v = lane < kTC ? fetch(sh, ph, 0, lane) : make_float4(0.f, 0.f, -1.f, 0.f);
+    float4 v = lane < kC ? fetch(sh, ph, 0, lane) : make_float4(0.f, 0.f, -1.f, 0.f);
     ff incl = {v.x, v.y};
 #pragma unroll
-    for (int off = 1; off < kTC; off <<= 1) {
+    for (int off = 1; off < kC; off <<= 1) {
       const ff o{__shfl_up_sync(0xffffffffu, incl.hi, off), __shfl_up_sync(0xffffffffu, incl.lo, off)};
       if (lane >= off) incl = ff_add(o, incl);
     }
-    if (lane < kTC) {
+    if (lane < kC) {
       sh.pre[lane + 1] = incl;
       sh.zs[lane] = v.z;
     }
     if (lane == 0) sh.pre[0] = ff{0.f, 0.f};
   }
   __syncthreads();
-  for (int r = 0; r <= kTC; ++r) pre[r] = sh.pre[r];
-  for (int r = 0; r < kTC; ++r) zs[r] = sh.zs[r];
+  for (int r = 0; r <= kC; ++r) pre[r] = sh.pre[r];
+  for (int r = 0; r < kC; ++r) zs[r] = sh.zs[r];
   __syncthreads();
 }
 
@@ -165,10 +171,11 @@ struct NodeStats {
 
 // Cluster-wide max of two values (and OR of two flags) published as
 // (mx_p, mx_q, bad_p, bad_q) by every CTA.
+template <int kC>
 __device__ float4 cluster_max2(TreeShared& sh, int ph) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp == 0) {
-    float4 v = lane < kTC ? fetch(sh, ph, 0, lane) : make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
+    float4 v = lane < kC ? fetch(sh, ph, 0, lane) : make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       v.x = fmaxf(v.x, __shfl_xor_sync(0xffffffffu, v.x, off));
@@ -200,10 +207,11 @@ __device__ float block_max_f(float v, TreeShared& sh, int slot) {
 
 // Sum of two ff values per thread over the cluster (after block sums):
 // returns (sum_a, sum_b).
+template <int kC>
 __device__ void cluster_sum2(TreeShared& sh, int ph, ff& a, ff& b) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp == 0) {
-    float4 f = lane < kTC ? fetch(sh, ph, 0, lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 f = lane < kC ? fetch(sh, ph, 0, lane) : make_float4(0.f, 0.f, 0.f, 0.f);
     ff x = {f.x, f.y}, y = {f.z, f.w};
     x = warp_sum_ff(x);
     y = warp_sum_ff(y);
@@ -219,6 +227,7 @@ __device__ void cluster_sum2(TreeShared& sh, int ph, ff& a, ff& b) {
 // slice into shared memory as 2^(z*c - k) against the cluster-wide reference
 // k of the row (p_v = sp[v] * inv_p); a non-finite logit, or a row without
 // mass, marks the node bad in every CTA.
+template <int kC>
 __device__ NodeStats load_node(const TreeArgs& a, TreeShared& sh, float* sp, float* sq, int b, int node, bool need_q,
                                int rank, int& ph, uint32_t& bar_phase, Expo c) {
   const int base = rank * a.S;
@@ -279,7 +288,7 @@ __device__ NodeStats load_node(const TreeArgs& a, TreeShared& sh, float* sp, flo
   mq = block_max_f(mq, sh, 1);
   const int bp = __syncthreads_or(bad_p), bq = __syncthreads_or(bad_q);
   publish(sh, ph, make_float4(mp, mq, static_cast<float>(bp), static_cast<float>(bq)), make_float4(0.f, 0.f, 0.f, 0.f));
-  const float4 gm = cluster_max2(sh, ph);
+  const float4 gm = cluster_max2<kC>(sh, ph);
   ph ^= 1;
   NodeStats st;
   st.bad = gm.z != 0.f || gm.x == -INFINITY || (need_q && (gm.w != 0.f || gm.y == -INFINITY));
@@ -324,7 +333,7 @@ __device__ NodeStats load_node(const TreeArgs& a, TreeShared& sh, float* sp, flo
   const ff sq_sum = block_sum(ff_norm(qh, ql), sh);
   publish(sh, ph, make_float4(sp_sum.hi, sp_sum.lo, sq_sum.hi, sq_sum.lo), make_float4(0.f, 0.f, 0.f, 0.f));
   ff Sp, Sq;
-  cluster_sum2(sh, ph, Sp, Sq);
+  cluster_sum2<kC>(sh, ph, Sp, Sq);
   ph ^= 1;
   st.inv_p = 1.f / (Sp.hi + Sp.lo);
   st.inv_q = need_q ? 1.f / (Sq.hi + Sq.lo) : 0.f;
@@ -337,6 +346,7 @@ __device__ __forceinline__ float rval(float e_p, float e_q, float ip, float iq, 
 }
 
 // Mass of max(0, p - lam q) over the whole row.
+template <int kC>
 __device__ ff residual_mass(const TreeArgs& a, TreeShared& sh, const float* sp, const float* sq, const NodeStats& st,
                             float lam, int rank, int& ph) {
   const int cnt = max(0, min(a.S, a.V - rank * a.S));
@@ -351,13 +361,14 @@ __device__ ff residual_mass(const TreeArgs& a, TreeShared& sh, const float* sp, 
   for (int i = 4 * c4 + threadIdx.x; i < cnt; i += kTT) ff_accumulate(hi, lo, rval(sp[i], sq[i], st.inv_p, st.inv_q, lam));
   const ff s = block_sum(ff_norm(hi, lo), sh);
   publish(sh, ph, make_float4(s.hi, s.lo, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f));
-  const ff tot = cluster_sum_ff(sh, ph);
+  const ff tot = cluster_sum_ff<kC>(sh, ph);
   ph ^= 1;
   return tot;
 }
 
 // Inverse-CDF draw over max(0, p - lam q) (lam = 0: over p) with uniform u.
 // Returns y in every CTA.
+template <int kC>
 __device__ int draw(const TreeArgs& a, TreeShared& sh, const float* sp, const float* sq, const NodeStats& st,
                     float lam, float u, int rank, int& ph) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -384,15 +395,15 @@ __device__ int draw(const TreeArgs& a, TreeShared& sh, const float* sp, const fl
   for (int w = 0; w < kTW; ++w) cta = ff_add(cta, sh.scan[w]);
   lastp = block_max_i(lastp, sh);
   publish(sh, ph, make_float4(cta.hi, cta.lo, static_cast<float>(lastp), 0.f), make_float4(0.f, 0.f, 0.f, 0.f));
-  ff pre[kTC + 1];
-  float zs[kTC];
-  cluster_scan_ff(sh, ph, pre, zs);
+  ff pre[kC + 1];
+  float zs[kC];
+  cluster_scan_ff<kC>(sh, ph, pre, zs);
   int last_all = -1;
-  for (int r = 0; r < kTC; ++r) last_all = max(last_all, static_cast<int>(zs[r]));
+  for (int r = 0; r < kC; ++r) last_all = max(last_all, static_cast<int>(zs[r]));
   ph ^= 1;
-  const ff t = ff_mul_f(pre[kTC], u);
+  const ff t = ff_mul_f(pre[kC], u);
   int owner = -1;
-  for (int r = 0; r < kTC && owner < 0; ++r)
+  for (int r = 0; r < kC && owner < 0; ++r)
     if (ff_gt(pre[r + 1], t)) owner = r;
   int y = -1;
   if (owner == rank) {
@@ -438,13 +449,14 @@ __device__ int draw(const TreeArgs& a, TreeShared& sh, const float* sp, const fl
   return yy;
 }
 
+template <int kC>
 __global__ void __launch_bounds__(kTT, 1) tree_sample_kernel(const TreeArgs a) {
   __shared__ TreeShared sh;
   extern __shared__ float4 dyn[];
   float* sp = reinterpret_cast<float*>(dyn);
   float* sq = sp + a.S;
   const int rank = static_cast<int>(cluster_ctarank());
-  const int b = blockIdx.x / kTC;
+  const int b = blockIdx.x / kC;
   const Expo c{a.c_hi, a.c_lo};
   griddep_wait();
   // tree structure and validity
@@ -474,7 +486,7 @@ __global__ void __launch_bounds__(kTT, 1) tree_sample_kernel(const TreeArgs a) {
   };
   while (!bad) {
     const int first = next_child(cur, 0);
-    const NodeStats st = load_node(a, sh, sp, sq, b, cur, first >= 0, rank, ph, bar_phase, c);
+    const NodeStats st = load_node<kC>(a, sh, sp, sq, b, cur, first >= 0, rank, ph, bar_phase, c);
     if (st.bad) {
       bad = kErrNonFinite;
       break;
@@ -494,7 +506,7 @@ __global__ void __launch_bounds__(kTT, 1) tree_sample_kernel(const TreeArgs a) {
         break;
       }
       const float lam_new = lam > 0.f ? lam + (sres.hi + sres.lo) : 1.f;
-      const ff s_new = residual_mass(a, sh, sp, sq, st, lam_new, rank, ph);
+      const ff s_new = residual_mass<kC>(a, sh, sp, sq, st, lam_new, rank, ph);
       if (s_new.hi > 0.f) {
         lam = lam_new;
         sres = s_new;
@@ -502,18 +514,18 @@ __global__ void __launch_bounds__(kTT, 1) tree_sample_kernel(const TreeArgs a) {
     }
     const float u0 = __ldcg(a.u + static_cast<size_t>(b) * a.N);
     if (accepted < 0) {
-      y = draw(a, sh, sp, sq, st, lam, u0, rank, ph);
+      y = draw<kC>(a, sh, sp, sq, st, lam, u0, rank, ph);
       break;
     }
     sh.path[n++] = accepted;  // every thread writes the same value
     cur = accepted;
     if (next_child(cur, 0) < 0) {
-      const NodeStats sb = load_node(a, sh, sp, sq, b, cur, false, rank, ph, bar_phase, c);
+      const NodeStats sb = load_node<kC>(a, sh, sp, sq, b, cur, false, rank, ph, bar_phase, c);
       if (sb.bad) {
         bad = kErrNonFinite;
         break;
       }
-      y = draw(a, sh, sp, sq, sb, 0.f, u0, rank, ph);
+      y = draw<kC>(a, sh, sp, sq, sb, 0.f, u0, rank, ph);
       break;
     }
   }
@@ -717,31 +729,76 @@ TreeArgs tree_args(const spec_tree_dims& d, float T, const float* zp, const floa
   return a;
 }
 
-cudaError_t launch_tree_sample(const TreeArgs& a, const DeviceInfo& dev, cudaStream_t s) {
-  static bool attr_done[64] = {false};
+// One cluster of kC CTAs per tree, a programmatic dependent of the LM head;
+// `probe` asks instead how many such clusters can be resident at once.
+template <int kC>
+cudaError_t tree_sample_launch(TreeArgs a, cudaStream_t s, int* probe) {
+  a.S = ((a.V + kC - 1) / kC + 3) / 4 * 4;  // slice per CTA, whole 16-byte units
   const size_t smem = 2u * sizeof(float) * static_cast<size_t>(a.S);
-  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev.device]) {
-    const cudaError_t e = cudaFuncSetAttribute(tree_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               2 * static_cast<int>(sizeof(float)) * kMaxSlice);
-    if (e != cudaSuccess) return e;
-    attr_done[dev.device] = true;
-  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.B * kTC);
+  cfg.gridDim = dim3(a.B * kC);
   cfg.blockDim = dim3(kTT);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kTC;
+  attr[0].val.clusterDim.x = kC;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, tree_sample_kernel, a);
+  if (probe) {
+    *probe = 0;
+    const int max_smem = 2 * static_cast<int>(sizeof(float)) * kMaxSlice;
+    cudaError_t e = cudaFuncSetAttribute(tree_sample_kernel<kC>, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e == cudaSuccess && kC > 8)
+      e = cudaFuncSetAttribute(tree_sample_kernel<kC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return kC > 8 ? cudaSuccess : e;  // the portable size must work
+    }
+    cfg.gridDim = dim3(kC);
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, tree_sample_kernel<kC>, &cfg);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    *probe = e == cudaSuccess ? clusters : 0;
+    return cudaSuccess;
+  }
+  return cudaLaunchKernelEx(&cfg, tree_sample_kernel<kC>, a);
+}
+
+cudaError_t launch_tree_sample(const TreeArgs& a, const DeviceInfo& dev, cudaStream_t s) {
+  // per device: resident clusters of 16, 12 and 8 CTAs (probed once, at the
+  // largest slices any call asks for); ready[] set after the probe
+  static int fit[64][3];
+  static bool ready[64] = {false};
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  if (!ready[dev.device]) {
+    TreeArgs pa = a;
+    pa.V = kTC * kMaxSlice;
+    cudaError_t e = tree_sample_launch<16>(pa, s, &fit[dev.device][0]);
+    if (e == cudaSuccess) e = tree_sample_launch<12>(pa, s, &fit[dev.device][1]);
+    if (e == cudaSuccess) e = tree_sample_launch<kTC>(pa, s, &fit[dev.device][2]);
+    if (e != cudaSuccess) return e;
+    ready[dev.device] = true;
+  }
+  // SPEC_TREE_CLUSTER_CTAS = 8, 12 or 16 forces that size where one such
+  // cluster fits (the tests run every size against the oracle this way)
+  if (const char* force = std::getenv("SPEC_TREE_CLUSTER_CTAS")) {
+    const int f = std::atoi(force);
+    if (f == 16 && fit[dev.device][0] > 0) return tree_sample_launch<16>(a, s, nullptr);
+    if (f == 12 && fit[dev.device][1] > 0) return tree_sample_launch<12>(a, s, nullptr);
+    if (f == 8) return tree_sample_launch<kTC>(a, s, nullptr);
+  }
+  // the largest cluster of which all B trees are resident at once (a tree
+  // that waits for another tree's walk to end costs a whole walk); the
+  // portable 8 otherwise
+  if (a.B <= fit[dev.device][0]) return tree_sample_launch<16>(a, s, nullptr);
+  if (a.B <= fit[dev.device][1]) return tree_sample_launch<12>(a, s, nullptr);
+  return tree_sample_launch<kTC>(a, s, nullptr);
 }
 
 }  // namespace

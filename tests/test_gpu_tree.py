@@ -91,6 +91,34 @@ def test_sampling_random_trees(N, V, T):
     compare_tree(np_(t), np_(p), np_(n), ref)
 
 
+@pytest.mark.parametrize("B,N,V,T", [(12, 9, 32000, 1.0),   # more than 9 trees: 8-CTA clusters
+                                     (12, 33, 1000, 0.7),
+                                     (9, 17, 131072, 0.9),  # 9 trees of 16 CTAs, slices of 8192
+                                     (3, 5, 196608, 1.0)])  # the largest vocabulary, slices of 12288
+def test_sampling_random_trees_cluster_sizes(B, N, V, T):
+    """A walk runs on 16-CTA clusters while B*16 CTAs fit the SMs and on
+    8-CTA clusters otherwise; both against the oracle, at slice sizes up to
+    the largest vocabulary."""
+    rng = np.random.default_rng(B * 7919 + N * 31 + V)
+    zp, zq, tok, par, u = random_tree(rng, B, N, V, T)
+    t, p, n = gpu_tree(zp, zq, tok, par, u, T)
+    ref = tv.verify_tree(zp, zq, tok, par, u, t32(T))
+    compare_tree(np_(t), np_(p), np_(n), ref)
+
+
+@pytest.mark.parametrize("ctas", ["8", "12", "16"])
+@pytest.mark.parametrize("B,N,V,T", [(5, 9, 32000, 1.0), (3, 33, 128256, 0.8), (2, 5, 196608, 1.0), (4, 9, 7, 1.0)])
+def test_sampling_every_cluster_size(ctas, B, N, V, T, monkeypatch):
+    """Each cluster size of the walk (forced where it fits) against the
+    oracle: slices of 4 to 24576 tokens, empty slices at V = 7."""
+    monkeypatch.setenv("SPEC_TREE_CLUSTER_CTAS", ctas)
+    rng = np.random.default_rng(B * 104729 + N * 13 + V)
+    zp, zq, tok, par, u = random_tree(rng, B, N, V, T)
+    t, p, n = gpu_tree(zp, zq, tok, par, u, T)
+    ref = tv.verify_tree(zp, zq, tok, par, u, t32(T))
+    compare_tree(np_(t), np_(p), np_(n), ref)
+
+
 def test_sampling_deep_and_wide_trees():
     """A chain of depth 40 (high acceptance) and a star of 60 children."""
     rng = np.random.default_rng(17)
