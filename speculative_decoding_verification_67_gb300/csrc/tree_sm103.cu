@@ -61,167 +61,100 @@ struct TreeArgs {
 };
 
 struct TreeShared {
-  float4 ex[2][2];  // cluster exchange slots [pass parity][value]
+  float4 ex[2][kTW];  // cluster exchange: one value per warp [pass parity][warp]
   int par[kMaxNodes];
   int tok[kMaxNodes];
   int path[kMaxNodes];
-  float wk[kTW], wsh[kTW];
-  ff scan[kTW];
-  int si[2 * kTW];
-  float4 res;  // broadcast of a block or cluster reduction
-  int res_i;
-  ff pre[kTCMax + 1];
-  float zs[kTCMax];
+  float4 res;         // a cluster reduction's result, broadcast to the block
+  int res_slot, res_last;
   int flag;
   uint64_t bar;  // completion of the node-row bulk copies
 };
 
-__device__ ff block_sum(ff v, TreeShared& sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_sum_ff(v);
-  if (lane == 0) sh.scan[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    ff w = lane < kTW ? sh.scan[lane] : ff{0.f, 0.f};
-    w = warp_sum_ff(w);
-    if (lane == 0) sh.res = make_float4(w.hi, w.lo, 0.f, 0.f);
-  }
-  __syncthreads();
-  return ff{sh.res.x, sh.res.y};
-}
-
-__device__ int block_max_i(int v, TreeShared& sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, off));
-  if (lane == 0) sh.si[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < kTW ? sh.si[lane] : INT_MIN;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) w = max(w, __shfl_xor_sync(0xffffffffu, w, off));
-    if (lane == 0) sh.res_i = w;
-  }
-  __syncthreads();
-  return sh.res_i;
-}
-
-// Publishes two values of this CTA for the current pass; after the cluster
-// barrier every CTA's values of the pass are readable.
-__device__ __forceinline__ void publish(TreeShared& sh, int ph, float4 a, float4 b) {
-  if (threadIdx.x == 0) {
-    sh.ex[ph][0] = a;
-    sh.ex[ph][1] = b;
-  }
+// Every cluster reduction of the walk: lane 0 of each warp publishes its
+// warp's value in exchange slot [ph][warp], one cluster barrier makes every
+// slot of every CTA readable, and warp 0 of each CTA reads all kC * kTW
+// values, lane l the consecutive slots l*kPL .. l*kPL + kPL - 1 in (rank,
+// warp) order, and merges them in that fixed order: every CTA computes the
+// same result.  The barrier of the next reduction (the other parity)
+// orders the reuse of the slots and of sh.res.
+__device__ __forceinline__ void publish_warp(TreeShared& sh, int ph, float4 v) {
+  if ((threadIdx.x & 31) == 0) sh.ex[ph][threadIdx.x >> 5] = v;
   cluster_sync();
 }
 
-__device__ __forceinline__ float4 fetch(TreeShared& sh, int ph, int which, int rank) {
-  return ld_cluster_f4(cluster_map(&sh.ex[ph][which], static_cast<uint32_t>(rank)));
-}
-
 template <int kC>
-__device__ ff cluster_sum_ff(TreeShared& sh, int ph) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp == 0) {
-    ff v = {0.f, 0.f};
-    if (lane < kC) {
-      const float4 f = fetch(sh, ph, 0, lane);
-      v = ff{f.x, f.y};
-    }
-    v = warp_sum_ff(v);
-    if (lane == 0) sh.res = make_float4(v.hi, v.lo, 0.f, 0.f);
-  }
-  __syncthreads();
-  const ff r = {sh.res.x, sh.res.y};
-  __syncthreads();
-  return r;
-}
-
-// Inclusive prefix over ranks of the pass's published float pairs (x, y of
-// value 0); lane r of warp 0 holds rank r's.  Returns the prefix ending at
-// `rank` in pre_end and the total.
-template <int kC>
-__device__ void cluster_scan_ff(TreeShared& sh, int ph, ff* pre /*[kC + 1]*/, float* zs /*[kC]*/) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp == 0) {
-    float4 v = lane < kC ? fetch(sh, ph, 0, lane) : make_float4(0.f, 0.f, -1.f, 0.f);
-    ff incl = {v.x, v.y};
+__device__ __forceinline__ void fetch_lane_slots(TreeShared& sh, int ph, float4 (&f)[kC * kTW / 32]) {
+  constexpr int kPL = kC * kTW / 32;
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int off = 1; off < kC; off <<= 1) {
-      const ff o{__shfl_up_sync(0xffffffffu, incl.hi, off), __shfl_up_sync(0xffffffffu, incl.lo, off)};
-      if (lane >= off) incl = ff_add(o, incl);
-    }
-    if (lane < kC) {
-      sh.pre[lane + 1] = incl;
-      sh.zs[lane] = v.z;
-    }
-    if (lane == 0) sh.pre[0] = ff{0.f, 0.f};
+  for (int j = 0; j < kPL; ++j) {
+    const int i = lane * kPL + j;
+    f[j] = ld_cluster_f4(cluster_map(&sh.ex[ph][i % kTW], static_cast<uint32_t>(i / kTW)));
+  }
+}
+
+__device__ __forceinline__ float4 max4(float4 a, float4 b) {
+  return make_float4(fmaxf(a.x, b.x), fmaxf(a.y, b.y), fmaxf(a.z, b.z), fmaxf(a.w, b.w));
+}
+
+__device__ __forceinline__ float4 warp_max4(float4 v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float4 o{__shfl_xor_sync(0xffffffffu, v.x, off), __shfl_xor_sync(0xffffffffu, v.y, off),
+                   __shfl_xor_sync(0xffffffffu, v.z, off), __shfl_xor_sync(0xffffffffu, v.w, off)};
+    v = max4(v, o);
+  }
+  return v;
+}
+
+// Cluster-wide componentwise maximum of one float4 per thread.
+template <int kC>
+__device__ float4 cluster_max4(TreeShared& sh, int ph, float4 v) {
+  publish_warp(sh, ph, warp_max4(v));
+  if (threadIdx.x < 32) {
+    constexpr int kPL = kC * kTW / 32;
+    float4 f[kPL];
+    fetch_lane_slots<kC>(sh, ph, f);
+    float4 m = f[0];
+#pragma unroll
+    for (int j = 1; j < kPL; ++j) m = max4(m, f[j]);
+    m = warp_max4(m);
+    if (threadIdx.x == 0) sh.res = m;
   }
   __syncthreads();
-  for (int r = 0; r <= kC; ++r) pre[r] = sh.pre[r];
-  for (int r = 0; r < kC; ++r) zs[r] = sh.zs[r];
+  return sh.res;
+}
+
+// Cluster-wide float-float sums of two values per thread: (sum a, sum b).
+template <int kC>
+__device__ void cluster_sum2(TreeShared& sh, int ph, ff& a, ff& b) {
+  a = warp_sum_ff(a);
+  b = warp_sum_ff(b);
+  publish_warp(sh, ph, make_float4(a.hi, a.lo, b.hi, b.lo));
+  if (threadIdx.x < 32) {
+    constexpr int kPL = kC * kTW / 32;
+    float4 f[kPL];
+    fetch_lane_slots<kC>(sh, ph, f);
+    ff x{f[0].x, f[0].y}, y{f[0].z, f[0].w};
+#pragma unroll
+    for (int j = 1; j < kPL; ++j) {
+      x = ff_add(x, ff{f[j].x, f[j].y});
+      y = ff_add(y, ff{f[j].z, f[j].w});
+    }
+    x = warp_sum_ff(x);
+    y = warp_sum_ff(y);
+    if (threadIdx.x == 0) sh.res = make_float4(x.hi, x.lo, y.hi, y.lo);
+  }
   __syncthreads();
+  a = ff{sh.res.x, sh.res.y};
+  b = ff{sh.res.z, sh.res.w};
 }
 
 struct NodeStats {
   float kp, inv_p, kq, inv_q;
   int bad;
 };
-
-// Cluster-wide max of two values (and OR of two flags) published as
-// (mx_p, mx_q, bad_p, bad_q) by every CTA.
-template <int kC>
-__device__ float4 cluster_max2(TreeShared& sh, int ph) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp == 0) {
-    float4 v = lane < kC ? fetch(sh, ph, 0, lane) : make_float4(-INFINITY, -INFINITY, 0.f, 0.f);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      v.x = fmaxf(v.x, __shfl_xor_sync(0xffffffffu, v.x, off));
-      v.y = fmaxf(v.y, __shfl_xor_sync(0xffffffffu, v.y, off));
-      v.z = fmaxf(v.z, __shfl_xor_sync(0xffffffffu, v.z, off));
-      v.w = fmaxf(v.w, __shfl_xor_sync(0xffffffffu, v.w, off));
-    }
-    if (lane == 0) sh.res = v;
-  }
-  __syncthreads();
-  const float4 r = sh.res;
-  __syncthreads();
-  return r;
-}
-
-__device__ float block_max_f(float v, TreeShared& sh, int slot) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_max_f(v);
-  if (lane == 0) sh.wk[warp] = v;
-  __syncthreads();
-  if (warp == 0) {
-    float w = lane < kTW ? sh.wk[lane] : -INFINITY;
-    w = warp_max_f(w);
-    if (lane == 0) sh.wsh[slot] = w;
-  }
-  __syncthreads();
-  return sh.wsh[slot];
-}
-
-// Sum of two ff values per thread over the cluster (after block sums):
-// returns (sum_a, sum_b).
-template <int kC>
-__device__ void cluster_sum2(TreeShared& sh, int ph, ff& a, ff& b) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp == 0) {
-    float4 f = lane < kC ? fetch(sh, ph, 0, lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-    ff x = {f.x, f.y}, y = {f.z, f.w};
-    x = warp_sum_ff(x);
-    y = warp_sum_ff(y);
-    if (lane == 0) sh.res = make_float4(x.hi, x.lo, y.hi, y.lo);
-  }
-  __syncthreads();
-  a = ff{sh.res.x, sh.res.y};
-  b = ff{sh.res.z, sh.res.w};
-  __syncthreads();
-}
 
 // Loads node `node`'s target row (and draft row if need_q) of this CTA's
 // slice into shared memory as 2^(z*c - k) against the cluster-wide reference
@@ -284,11 +217,7 @@ __device__ NodeStats load_node(const TreeArgs& a, TreeShared& sh, float* sp, flo
       }
     }
   }
-  mp = block_max_f(mp, sh, 0);
-  mq = block_max_f(mq, sh, 1);
-  const int bp = __syncthreads_or(bad_p), bq = __syncthreads_or(bad_q);
-  publish(sh, ph, make_float4(mp, mq, static_cast<float>(bp), static_cast<float>(bq)), make_float4(0.f, 0.f, 0.f, 0.f));
-  const float4 gm = cluster_max2<kC>(sh, ph);
+  const float4 gm = cluster_max4<kC>(sh, ph, make_float4(mp, mq, bad_p ? 1.f : 0.f, bad_q ? 1.f : 0.f));
   ph ^= 1;
   NodeStats st;
   st.bad = gm.z != 0.f || gm.x == -INFINITY || (need_q && (gm.w != 0.f || gm.y == -INFINITY));
@@ -329,10 +258,7 @@ __device__ NodeStats load_node(const TreeArgs& a, TreeShared& sh, float* sp, flo
       }
     }
   }
-  const ff sp_sum = block_sum(ff_norm(ph_, pl), sh);
-  const ff sq_sum = block_sum(ff_norm(qh, ql), sh);
-  publish(sh, ph, make_float4(sp_sum.hi, sp_sum.lo, sq_sum.hi, sq_sum.lo), make_float4(0.f, 0.f, 0.f, 0.f));
-  ff Sp, Sq;
+  ff Sp = ff_norm(ph_, pl), Sq = ff_norm(qh, ql);
   cluster_sum2<kC>(sh, ph, Sp, Sq);
   ph ^= 1;
   st.inv_p = 1.f / (Sp.hi + Sp.lo);
@@ -359,24 +285,31 @@ __device__ ff residual_mass(const TreeArgs& a, TreeShared& sh, const float* sp, 
                               (rval(e.z, f.z, st.inv_p, st.inv_q, lam) + rval(e.w, f.w, st.inv_p, st.inv_q, lam)));
   }
   for (int i = 4 * c4 + threadIdx.x; i < cnt; i += kTT) ff_accumulate(hi, lo, rval(sp[i], sq[i], st.inv_p, st.inv_q, lam));
-  const ff s = block_sum(ff_norm(hi, lo), sh);
-  publish(sh, ph, make_float4(s.hi, s.lo, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f));
-  const ff tot = cluster_sum_ff<kC>(sh, ph);
+  ff tot = ff_norm(hi, lo), none{0.f, 0.f};
+  cluster_sum2<kC>(sh, ph, tot, none);
   ph ^= 1;
   return tot;
 }
 
-// Inverse-CDF draw over max(0, p - lam q) (lam = 0: over p) with uniform u.
-// Returns y in every CTA.
+__device__ __forceinline__ int warp_max_i(int v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+// Inverse-CDF draw over max(0, p - lam q) (lam = 0: over p) with uniform u,
+// written to out_tok[b][pos] by the warp that finds it.  Warp w of each CTA
+// covers the contiguous block [w*blk, (w+1)*blk) of its slice, so the
+// (rank, warp) block masses in that order are coarse steps of the CDF: one
+// cluster reduction scans them for the block holding t = u*S, and the warp
+// owning that block scans it 32 tokens at a time.
 template <int kC>
-__device__ int draw(const TreeArgs& a, TreeShared& sh, const float* sp, const float* sq, const NodeStats& st,
-                    float lam, float u, int rank, int& ph) {
+__device__ void draw(const TreeArgs& a, TreeShared& sh, const float* sp, const float* sq, const NodeStats& st,
+                     float lam, float u, int rank, int& ph, int b, int pos) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int base = rank * a.S;
   const int cnt = max(0, min(a.S, a.V - base));
   const float ip = st.inv_p, iq = st.inv_q;
-  // this CTA's slice mass and last token with mass; warp w covers the
-  // contiguous block [w*blk, (w+1)*blk) so that the owner can be found by warp
   const int blk = ((cnt + kTW - 1) / kTW + 31) / 32 * 32;
   const int w0 = min(cnt, warp * blk), w1 = min(cnt, w0 + blk);
   float hi = 0.f, lo = 0.f;
@@ -388,65 +321,86 @@ __device__ int draw(const TreeArgs& a, TreeShared& sh, const float* sp, const fl
       lastp = base + i;
     }
   }
-  const ff wsum = warp_sum_ff(ff_norm(hi, lo));  // this warp's block
-  if (lane == 0) sh.scan[warp] = wsum;
-  __syncthreads();
-  ff cta = {0.f, 0.f};
-  for (int w = 0; w < kTW; ++w) cta = ff_add(cta, sh.scan[w]);
-  lastp = block_max_i(lastp, sh);
-  publish(sh, ph, make_float4(cta.hi, cta.lo, static_cast<float>(lastp), 0.f), make_float4(0.f, 0.f, 0.f, 0.f));
-  ff pre[kC + 1];
-  float zs[kC];
-  cluster_scan_ff<kC>(sh, ph, pre, zs);
-  int last_all = -1;
-  for (int r = 0; r < kC; ++r) last_all = max(last_all, static_cast<int>(zs[r]));
-  ph ^= 1;
-  const ff t = ff_mul_f(pre[kC], u);
-  int owner = -1;
-  for (int r = 0; r < kC && owner < 0; ++r)
-    if (ff_gt(pre[r + 1], t)) owner = r;
-  int y = -1;
-  if (owner == rank) {
-    // the warp whose block holds t, then 32 tokens at a time with a warp scan
-    const ff tl = ff_add(t, ff{-pre[rank].hi, -pre[rank].lo});
-    ff run = {0.f, 0.f};
-    int ow = -1;
-    for (int w = 0; w < kTW; ++w) {
-      const ff nxt = ff_add(run, sh.scan[w]);
-      if (ow < 0 && ff_gt(nxt, tl)) ow = w;
-      if (ow < 0) run = nxt;
-    }
-    if (warp == ow) {
-      const int v0 = min(cnt, ow * blk), v1 = min(cnt, v0 + blk);
-      for (int i0 = v0; i0 < v1 && y < 0; i0 += 32) {
-        const int i = i0 + lane;
-        const float d = i < v1 ? rval(sp[i], lam > 0.f ? sq[i] : 0.f, ip, iq, lam) : 0.f;
-        ff incl = {d, 0.f};
+  const ff wsum = warp_sum_ff(ff_norm(hi, lo));
+  lastp = warp_max_i(lastp);
+  publish_warp(sh, ph, make_float4(wsum.hi, wsum.lo, __int_as_float(lastp), 0.f));
+  if (threadIdx.x < 32) {
+    constexpr int kPL = kC * kTW / 32;
+    float4 f[kPL];
+    fetch_lane_slots<kC>(sh, ph, f);
+    ff tot{0.f, 0.f};
+    int last = -1;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const ff o{__shfl_up_sync(0xffffffffu, incl.hi, off), __shfl_up_sync(0xffffffffu, incl.lo, off)};
-          if (lane >= off) incl = ff_add(o, incl);
-        }
-        const unsigned hit = __ballot_sync(0xffffffffu, i < v1 && ff_gt(ff_add(run, incl), tl));
-        if (hit) y = base + i0 + __ffs(hit) - 1;
-        const ff tot{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
-        run = ff_add(run, tot);
-      }
-      if (lane == 0) sh.res_i = y;
+    for (int j = 0; j < kPL; ++j) {
+      tot = ff_add(tot, ff{f[j].x, f[j].y});
+      last = max(last, __float_as_int(f[j].z));
     }
-    __syncthreads();
-    y = ow < 0 ? -1 : sh.res_i;
-    __syncthreads();
+    // exclusive prefix of the lanes' totals; S the total
+    ff incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const ff o{__shfl_up_sync(0xffffffffu, incl.hi, off), __shfl_up_sync(0xffffffffu, incl.lo, off)};
+      if (lane >= off) incl = ff_add(o, incl);
+    }
+    ff ex{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+    if (lane == 0) ex = {0.f, 0.f};
+    const ff S{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
+    const ff t = ff_mul_f(S, u);
+    // this lane's first slot whose inclusive prefix exceeds t, and the prefix before it
+    ff run = ex, pre{0.f, 0.f};
+    int hit = -1;
+#pragma unroll
+    for (int j = 0; j < kPL; ++j) {
+      const ff nxt = ff_add(run, ff{f[j].x, f[j].y});
+      if (hit < 0 && ff_gt(nxt, t)) {
+        hit = j;
+        pre = run;
+      }
+      run = nxt;
+    }
+    const unsigned hm = __ballot_sync(0xffffffffu, hit >= 0);
+    last = warp_max_i(last);
+    int slot = -1;
+    float4 r = make_float4(0.f, 0.f, t.hi, t.lo);
+    if (hm) {
+      const int src = __ffs(hm) - 1;
+      slot = src * kPL + __shfl_sync(0xffffffffu, hit, src);
+      r.x = __shfl_sync(0xffffffffu, pre.hi, src);
+      r.y = __shfl_sync(0xffffffffu, pre.lo, src);
+    }
+    if (lane == 0) {
+      sh.res_slot = slot;
+      sh.res_last = last;
+      sh.res = r;
+    }
   }
-  // the owner's y (or, when rounding left t past every slice or past the
-  // owner's last step, the last token with mass) to every CTA
-  const float yv = owner == rank ? static_cast<float>(y) : -2.f;
-  publish(sh, ph, make_float4(yv, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f));
-  int yy = -1;
-  if (owner >= 0) yy = static_cast<int>(fetch(sh, ph, 0, owner).x);
-  ph ^= 1;
-  if (owner < 0 || yy < 0) yy = last_all;
-  return yy;
+  __syncthreads();
+  int32_t* out = a.out_tok + static_cast<size_t>(b) * a.N + pos;
+  const int slot = sh.res_slot;
+  if (slot < 0) {  // rounding left t past every block: the last token with mass
+    if (rank == 0 && threadIdx.x == 0) *out = sh.res_last;
+    return;
+  }
+  if (rank != slot / kTW || warp != slot % kTW) return;
+  const ff tl = ff_add(ff{sh.res.z, sh.res.w}, ff{-sh.res.x, -sh.res.y});
+  ff run{0.f, 0.f};
+  int y = -1;
+  for (int i0 = w0; i0 < w1 && y < 0; i0 += 32) {
+    const int i = i0 + lane;
+    const float d = i < w1 ? rval(sp[i], lam > 0.f ? sq[i] : 0.f, ip, iq, lam) : 0.f;
+    ff incl{d, 0.f};
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const ff o{__shfl_up_sync(0xffffffffu, incl.hi, off), __shfl_up_sync(0xffffffffu, incl.lo, off)};
+      if (lane >= off) incl = ff_add(o, incl);
+    }
+    const unsigned h = __ballot_sync(0xffffffffu, i < w1 && ff_gt(ff_add(run, incl), tl));
+    if (h) y = base + i0 + __ffs(h) - 1;
+    const ff tot{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
+    run = ff_add(run, tot);
+  }
+  // (rounding left t past this block's last step: its last token with mass)
+  if (lane == 0) *out = y >= 0 ? y : lastp;
 }
 
 template <int kC>
@@ -478,7 +432,7 @@ __global__ void __launch_bounds__(kTT, 1) tree_sample_kernel(const TreeArgs a) {
   __syncthreads();
   int bad = sh.flag;
   int ph = 0;
-  int cur = 0, n = 0, y = -1;
+  int cur = 0, n = 0;
   auto next_child = [&](int node, int after) {
     for (int i = after + 1; i < a.N; ++i)
       if (sh.par[i] == node) return i;
@@ -514,7 +468,7 @@ __global__ void __launch_bounds__(kTT, 1) tree_sample_kernel(const TreeArgs a) {
     }
     const float u0 = __ldcg(a.u + static_cast<size_t>(b) * a.N);
     if (accepted < 0) {
-      y = draw<kC>(a, sh, sp, sq, st, lam, u0, rank, ph);
+      draw<kC>(a, sh, sp, sq, st, lam, u0, rank, ph, b, n);
       break;
     }
     sh.path[n++] = accepted;  // every thread writes the same value
@@ -525,7 +479,7 @@ __global__ void __launch_bounds__(kTT, 1) tree_sample_kernel(const TreeArgs a) {
         bad = kErrNonFinite;
         break;
       }
-      y = draw<kC>(a, sh, sp, sq, sb, 0.f, u0, rank, ph);
+      draw<kC>(a, sh, sp, sq, sb, 0.f, u0, rank, ph, b, n);
       break;
     }
   }
@@ -534,15 +488,11 @@ __global__ void __launch_bounds__(kTT, 1) tree_sample_kernel(const TreeArgs a) {
     const size_t o = static_cast<size_t>(b) * a.N;
     for (int i = threadIdx.x; i < a.N; i += kTT) {
       int tv = -1, pv = -1;
-      if (!bad) {
-        if (i < n) {
-          pv = sh.path[i];
-          tv = sh.tok[pv];
-        } else if (i == n) {
-          tv = y;
-        }
+      if (!bad && i < n) {
+        pv = sh.path[i];
+        tv = sh.tok[pv];
       }
-      a.out_tok[o + i] = tv;
+      if (bad || i != n) a.out_tok[o + i] = tv;  // position n: the drawn token, written by the warp that drew it
       a.out_path[o + i] = pv;
     }
     if (threadIdx.x == 0) {
@@ -779,7 +729,7 @@ cudaError_t launch_tree_sample(const TreeArgs& a, const DeviceInfo& dev, cudaStr
   if (!ready[dev.device]) {
     TreeArgs pa = a;
     pa.V = kTC * kMaxSlice;
-    cudaError_t e = tree_sample_launch<16>(pa, s, &fit[dev.device][0]);
+    cudaError_t e = tree_sample_launch<kTCMax>(pa, s, &fit[dev.device][0]);
     if (e == cudaSuccess) e = tree_sample_launch<12>(pa, s, &fit[dev.device][1]);
     if (e == cudaSuccess) e = tree_sample_launch<kTC>(pa, s, &fit[dev.device][2]);
     if (e != cudaSuccess) return e;
@@ -789,14 +739,14 @@ cudaError_t launch_tree_sample(const TreeArgs& a, const DeviceInfo& dev, cudaStr
   // cluster fits (the tests run every size against the oracle this way)
   if (const char* force = std::getenv("SPEC_TREE_CLUSTER_CTAS")) {
     const int f = std::atoi(force);
-    if (f == 16 && fit[dev.device][0] > 0) return tree_sample_launch<16>(a, s, nullptr);
+    if (f == 16 && fit[dev.device][0] > 0) return tree_sample_launch<kTCMax>(a, s, nullptr);
     if (f == 12 && fit[dev.device][1] > 0) return tree_sample_launch<12>(a, s, nullptr);
     if (f == 8) return tree_sample_launch<kTC>(a, s, nullptr);
   }
   // the largest cluster of which all B trees are resident at once (a tree
   // that waits for another tree's walk to end costs a whole walk); the
   // portable 8 otherwise
-  if (a.B <= fit[dev.device][0]) return tree_sample_launch<16>(a, s, nullptr);
+  if (a.B <= fit[dev.device][0]) return tree_sample_launch<kTCMax>(a, s, nullptr);
   if (a.B <= fit[dev.device][1]) return tree_sample_launch<12>(a, s, nullptr);
   return tree_sample_launch<kTC>(a, s, nullptr);
 }
