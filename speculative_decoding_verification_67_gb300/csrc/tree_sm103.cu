@@ -61,11 +61,12 @@ struct TreeArgs {
 };
 
 struct TreeShared {
-  float4 ex[2][kTW];  // cluster exchange: one value per warp [pass parity][warp]
+  float4 ex[2][2][kTW];  // cluster exchange: up to two values per warp [pass parity][value][warp]
   int par[kMaxNodes];
   int tok[kMaxNodes];
   int path[kMaxNodes];
-  float4 res;         // a cluster reduction's result, broadcast to the block
+  float czp[kMaxNodes], czq[kMaxNodes];  // target / draft logit of each child of the node being loaded
+  float4 res, res2;                      // a cluster reduction's result, broadcast to the block
   int res_slot, res_last;
   int flag;
   uint64_t bar;  // completion of the node-row bulk copies
@@ -79,19 +80,28 @@ struct TreeShared {
 // same result.  The barrier of the next reduction (the other parity)
 // orders the reuse of the slots and of sh.res.
 __device__ __forceinline__ void publish_warp(TreeShared& sh, int ph, float4 v) {
-  if ((threadIdx.x & 31) == 0) sh.ex[ph][threadIdx.x >> 5] = v;
+  if ((threadIdx.x & 31) == 0) sh.ex[ph][0][threadIdx.x >> 5] = v;
   cluster_sync();
 }
 
 template <int kC>
-__device__ __forceinline__ void fetch_lane_slots(TreeShared& sh, int ph, float4 (&f)[kC * kTW / 32]) {
+__device__ __forceinline__ void fetch_lane_slots(TreeShared& sh, int ph, float4 (&f)[kC * kTW / 32], int which = 0) {
   constexpr int kPL = kC * kTW / 32;
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int j = 0; j < kPL; ++j) {
     const int i = lane * kPL + j;
-    f[j] = ld_cluster_f4(cluster_map(&sh.ex[ph][i % kTW], static_cast<uint32_t>(i / kTW)));
+    f[j] = ld_cluster_f4(cluster_map(&sh.ex[ph][which][i % kTW], static_cast<uint32_t>(i / kTW)));
   }
+}
+
+// Warp w's contiguous block [w0, w1) of a slice of cnt entries: every pass
+// over a node's rows uses this mapping, so a warp's own scale factors apply
+// to everything it reads.
+__device__ __forceinline__ void warp_block(int cnt, int& w0, int& w1) {
+  const int blk = ((cnt + kTW - 1) / kTW + 31) / 32 * 32;
+  w0 = min(cnt, static_cast<int>(threadIdx.x >> 5) * blk);
+  w1 = min(cnt, w0 + blk);
 }
 
 __device__ __forceinline__ float4 max4(float4 a, float4 b) {
@@ -152,17 +162,21 @@ __device__ void cluster_sum2(TreeShared& sh, int ph, ff& a, ff& b) {
 }
 
 struct NodeStats {
-  float kp, inv_p, kq, inv_q;
+  float kp, inv_p, kq, inv_q;  // the row's reference exponents and 1 / normaliser (cluster-wide)
+  float ip_w, iq_w;            // this warp's factors: p_v = sp[v] * ip_w, q_v = sq[v] * iq_w
   int bad;
 };
 
 // Loads node `node`'s target row (and draft row if need_q) of this CTA's
-// slice into shared memory as 2^(z*c - k) against the cluster-wide reference
-// k of the row (p_v = sp[v] * inv_p); a non-finite logit, or a row without
-// mass, marks the node bad in every CTA.
+// slice into shared memory as 2^(z*c - k_w), k_w = ceil of the largest z*c
+// of warp w's block (no barrier: each warp reduces its own block), sums the
+// block, and merges the (k_w, sum_w) pairs of every warp of the cluster
+// into K = max k_w and S = sum of sum_w * 2^(k_w - K) (exact powers of two).
+// A non-finite logit, or a row without mass, marks the node bad in every CTA.
 template <int kC>
 __device__ NodeStats load_node(const TreeArgs& a, TreeShared& sh, float* sp, float* sq, int b, int node, bool need_q,
                                int rank, int& ph, uint32_t& bar_phase, Expo c) {
+  const int lane = threadIdx.x & 31;
   const int base = rank * a.S;
   const int cnt = max(0, min(a.S, a.V - base));
   const size_t row = (static_cast<size_t>(b) * a.N + node) * a.V + base;
@@ -192,23 +206,12 @@ __device__ NodeStats load_node(const TreeArgs& a, TreeShared& sh, float* sp, flo
     }
   }
   __syncthreads();
-  // pass 1: largest exponent of each row (cnt is a multiple of 4 with bulk rows)
+  int w0, w1;
+  warp_block(cnt, w0, w1);
+  // the block's largest exponent per row
   float mp = -INFINITY, mq = -INFINITY;
   if (!bad_p) {
-    const int c4 = a.bulk ? cnt / 4 : 0;
-    for (int i = threadIdx.x; i < c4; i += kTT) {
-      const float4 z = reinterpret_cast<const float4*>(sp)[i];
-      const float h0 = expo_hi(z.x, c), h1 = expo_hi(z.y, c), h2 = expo_hi(z.z, c), h3 = expo_hi(z.w, c);
-      if (!(isfinite(h0) && isfinite(h1) && isfinite(h2) && isfinite(h3))) bad_p = 1;
-      mp = fmaxf(mp, fmaxf(fmaxf(h0, h1), fmaxf(h2, h3)));
-      if (need_q) {
-        const float4 w = reinterpret_cast<const float4*>(sq)[i];
-        const float g0 = expo_hi(w.x, c), g1 = expo_hi(w.y, c), g2 = expo_hi(w.z, c), g3 = expo_hi(w.w, c);
-        if (!(isfinite(g0) && isfinite(g1) && isfinite(g2) && isfinite(g3))) bad_q = 1;
-        mq = fmaxf(mq, fmaxf(fmaxf(g0, g1), fmaxf(g2, g3)));
-      }
-    }
-    for (int i = 4 * c4 + threadIdx.x; i < cnt; i += kTT) {
+    for (int i = w0 + lane; i < w1; i += 32) {
       const float h = expo_hi(sp[i], c);
       if (!isfinite(h)) bad_p = 1; else mp = fmaxf(mp, h);
       if (need_q) {
@@ -217,52 +220,65 @@ __device__ NodeStats load_node(const TreeArgs& a, TreeShared& sh, float* sp, flo
       }
     }
   }
-  const float4 gm = cluster_max4<kC>(sh, ph, make_float4(mp, mq, bad_p ? 1.f : 0.f, bad_q ? 1.f : 0.f));
-  ph ^= 1;
-  NodeStats st;
-  st.bad = gm.z != 0.f || gm.x == -INFINITY || (need_q && (gm.w != 0.f || gm.y == -INFINITY));
-  st.kp = st.bad ? 0.f : ceilf(gm.x);
-  st.kq = (st.bad || !need_q) ? 0.f : ceilf(gm.y);
-  st.inv_p = st.inv_q = 0.f;
-  if (st.bad) return st;
-  // pass 2: 2^(z*c - k) in place and the slice sums
+  const float kp_w = ceilf(warp_max_f(mp)), kq_w = ceilf(warp_max_f(mq));
+  // 2^(z*c - k_w) in place and the block sums
   float ph_ = 0.f, pl = 0.f, qh = 0.f, ql = 0.f;
-  {
-    const int c4 = a.bulk ? cnt / 4 : 0;
-    for (int i = threadIdx.x; i < c4; i += kTT) {
-      float4 z = reinterpret_cast<const float4*>(sp)[i];
-      z.x = pow2_rel(z.x, c, st.kp);
-      z.y = pow2_rel(z.y, c, st.kp);
-      z.z = pow2_rel(z.z, c, st.kp);
-      z.w = pow2_rel(z.w, c, st.kp);
-      reinterpret_cast<float4*>(sp)[i] = z;
-      ff_accumulate(ph_, pl, (z.x + z.y) + (z.z + z.w));
-      if (need_q) {
-        float4 w = reinterpret_cast<const float4*>(sq)[i];
-        w.x = pow2_rel(w.x, c, st.kq);
-        w.y = pow2_rel(w.y, c, st.kq);
-        w.z = pow2_rel(w.z, c, st.kq);
-        w.w = pow2_rel(w.w, c, st.kq);
-        reinterpret_cast<float4*>(sq)[i] = w;
-        ff_accumulate(qh, ql, (w.x + w.y) + (w.z + w.w));
-      }
-    }
-    for (int i = 4 * c4 + threadIdx.x; i < cnt; i += kTT) {
-      const float e = pow2_rel(sp[i], c, st.kp);
+  if (kp_w != -INFINITY) {
+    for (int i = w0 + lane; i < w1; i += 32) {
+      const float e = pow2_rel(sp[i], c, kp_w);
       sp[i] = e;
       ff_accumulate(ph_, pl, e);
-      if (need_q) {
-        const float f = pow2_rel(sq[i], c, st.kq);
-        sq[i] = f;
-        ff_accumulate(qh, ql, f);
-      }
     }
   }
-  ff Sp = ff_norm(ph_, pl), Sq = ff_norm(qh, ql);
-  cluster_sum2<kC>(sh, ph, Sp, Sq);
+  if (need_q && kq_w != -INFINITY) {
+    for (int i = w0 + lane; i < w1; i += 32) {
+      const float f = pow2_rel(sq[i], c, kq_w);
+      sq[i] = f;
+      ff_accumulate(qh, ql, f);
+    }
+  }
+  const ff sp_w = warp_sum_ff(ff_norm(ph_, pl)), sq_w = warp_sum_ff(ff_norm(qh, ql));
+  const int bp = __any_sync(0xffffffffu, bad_p != 0), bq = __any_sync(0xffffffffu, bad_q != 0);
+  if (lane == 0) {
+    sh.ex[ph][0][threadIdx.x >> 5] = make_float4(kp_w, sp_w.hi, sp_w.lo, bp ? 1.f : 0.f);
+    sh.ex[ph][1][threadIdx.x >> 5] = make_float4(kq_w, sq_w.hi, sq_w.lo, bq ? 1.f : 0.f);
+  }
+  cluster_sync();
+  if (threadIdx.x < 32) {
+    constexpr int kPL = kC * kTW / 32;
+    float4 fp[kPL], fq[kPL];
+    fetch_lane_slots<kC>(sh, ph, fp, 0);
+    fetch_lane_slots<kC>(sh, ph, fq, 1);
+    float4 m = make_float4(fp[0].x, fq[0].x, fp[0].w, fq[0].w);
+#pragma unroll
+    for (int j = 1; j < kPL; ++j) m = max4(m, make_float4(fp[j].x, fq[j].x, fp[j].w, fq[j].w));
+    m = warp_max4(m);
+    ff Sp{0.f, 0.f}, Sq{0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < kPL; ++j) {
+      const float a_ = pow2_nonpos(fp[j].x - m.x), b_ = pow2_nonpos(fq[j].x - m.y);
+      Sp = ff_add(Sp, ff{fp[j].y * a_, fp[j].z * a_});
+      Sq = ff_add(Sq, ff{fq[j].y * b_, fq[j].z * b_});
+    }
+    Sp = warp_sum_ff(Sp);
+    Sq = warp_sum_ff(Sq);
+    if (threadIdx.x == 0) {
+      sh.res = m;
+      sh.res2 = make_float4(Sp.hi, Sp.lo, Sq.hi, Sq.lo);
+    }
+  }
+  __syncthreads();
   ph ^= 1;
-  st.inv_p = 1.f / (Sp.hi + Sp.lo);
-  st.inv_q = need_q ? 1.f / (Sq.hi + Sq.lo) : 0.f;
+  const float4 m = sh.res, S = sh.res2;
+  NodeStats st;
+  st.bad = m.z != 0.f || m.x == -INFINITY || !(S.x > 0.f) || !isfinite(S.x) ||
+           (need_q && (m.w != 0.f || m.y == -INFINITY || !(S.z > 0.f) || !isfinite(S.z)));
+  st.kp = m.x;
+  st.kq = need_q ? m.y : 0.f;
+  st.inv_p = st.bad ? 0.f : 1.f / (S.x + S.y);
+  st.inv_q = (st.bad || !need_q) ? 0.f : 1.f / (S.z + S.w);
+  st.ip_w = st.inv_p * pow2_nonpos(kp_w - st.kp);
+  st.iq_w = need_q ? st.inv_q * pow2_nonpos(kq_w - st.kq) : 0.f;
   return st;
 }
 
@@ -276,15 +292,11 @@ template <int kC>
 __device__ ff residual_mass(const TreeArgs& a, TreeShared& sh, const float* sp, const float* sq, const NodeStats& st,
                             float lam, int rank, int& ph) {
   const int cnt = max(0, min(a.S, a.V - rank * a.S));
+  int w0, w1;
+  warp_block(cnt, w0, w1);
   float hi = 0.f, lo = 0.f;
-  const int c4 = a.bulk ? cnt / 4 : 0;
-  for (int i = threadIdx.x; i < c4; i += kTT) {
-    const float4 e = reinterpret_cast<const float4*>(sp)[i];
-    const float4 f = reinterpret_cast<const float4*>(sq)[i];
-    ff_accumulate(hi, lo, (rval(e.x, f.x, st.inv_p, st.inv_q, lam) + rval(e.y, f.y, st.inv_p, st.inv_q, lam)) +
-                              (rval(e.z, f.z, st.inv_p, st.inv_q, lam) + rval(e.w, f.w, st.inv_p, st.inv_q, lam)));
-  }
-  for (int i = 4 * c4 + threadIdx.x; i < cnt; i += kTT) ff_accumulate(hi, lo, rval(sp[i], sq[i], st.inv_p, st.inv_q, lam));
+  for (int i = w0 + static_cast<int>(threadIdx.x & 31); i < w1; i += 32)
+    ff_accumulate(hi, lo, rval(sp[i], sq[i], st.ip_w, st.iq_w, lam));
   ff tot = ff_norm(hi, lo), none{0.f, 0.f};
   cluster_sum2<kC>(sh, ph, tot, none);
   ph ^= 1;
@@ -309,9 +321,9 @@ __device__ void draw(const TreeArgs& a, TreeShared& sh, const float* sp, const f
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int base = rank * a.S;
   const int cnt = max(0, min(a.S, a.V - base));
-  const float ip = st.inv_p, iq = st.inv_q;
-  const int blk = ((cnt + kTW - 1) / kTW + 31) / 32 * 32;
-  const int w0 = min(cnt, warp * blk), w1 = min(cnt, w0 + blk);
+  const float ip = st.ip_w, iq = st.iq_w;
+  int w0, w1;
+  warp_block(cnt, w0, w1);
   float hi = 0.f, lo = 0.f;
   int lastp = -1;
   for (int i = w0 + lane; i < w1; i += 32) {
@@ -440,6 +452,17 @@ __global__ void __launch_bounds__(kTT, 1) tree_sample_kernel(const TreeArgs a) {
   };
   while (!bad) {
     const int first = next_child(cur, 0);
+    {
+      // the children's logits for their acceptance tests, in flight while
+      // the node's rows arrive (load_node's barrier publishes them)
+      const size_t crow = (static_cast<size_t>(b) * a.N + cur) * a.V;
+      for (int i = threadIdx.x; i < a.N; i += kTT) {
+        if (sh.par[i] == cur) {
+          sh.czp[i] = __ldcg(a.zp + crow + sh.tok[i]);
+          sh.czq[i] = __ldcg(a.zq + crow + sh.tok[i]);
+        }
+      }
+    }
     const NodeStats st = load_node<kC>(a, sh, sp, sq, b, cur, first >= 0, rank, ph, bar_phase, c);
     if (st.bad) {
       bad = kErrNonFinite;
@@ -448,11 +471,9 @@ __global__ void __launch_bounds__(kTT, 1) tree_sample_kernel(const TreeArgs a) {
     float lam = 0.f;       // 0: r = p
     ff sres = {1.f, 0.f};  // mass of max(0, p - lam q) (1 for r = p)
     int accepted = -1;
-    const size_t row = (static_cast<size_t>(b) * a.N + cur) * a.V;
     for (int ch = first; ch >= 0; ch = next_child(cur, ch)) {
-      const int x = sh.tok[ch];
-      const float px = pow2_rel(__ldcg(a.zp + row + x), c, st.kp) * st.inv_p;
-      const float qx = pow2_rel(__ldcg(a.zq + row + x), c, st.kq) * st.inv_q;  // = the smem values' scale
+      const float px = pow2_rel(sh.czp[ch], c, st.kp) * st.inv_p;
+      const float qx = pow2_rel(sh.czq[ch], c, st.kq) * st.inv_q;
       const float rx = lam > 0.f ? fmaxf(0.f, px - lam * qx) / (sres.hi + sres.lo) : px;
       const float acc = qx > 0.f ? fminf(1.f, rx / qx) : (rx > 0.f ? 1.f : 0.f);
       if (__ldcg(a.u + static_cast<size_t>(b) * a.N + ch) < acc) {
