@@ -25,7 +25,8 @@
 //     ascending token id).
 //
 // Rows of at most 32 chunks (V <= 131072) take finish_cluster_kernel
-// instead: one cluster per sequence (one chunk per CTA up to 8 chunks, two
+// instead whenever every sequence's cluster is resident at once: one
+// cluster per sequence (one chunk per CTA up to 8 chunks, two
 // above, so at most 16 CTAs), the chunk masses exchanged through
 // distributed shared memory, and the warps owning the drawn chunk scanning
 // it from the terms they still hold in registers; the same arithmetic, the
@@ -1091,7 +1092,7 @@ namespace {
 
 // One cluster of `ctas` CTAs of finish_cluster_kernel<kVec, kCPC> per
 // sequence, a programmatic dependent of the preceding kernel.  `probe`
-// asks instead whether such a cluster can be resident at all (1 yes, 0 no).
+// asks instead how many such clusters can be resident at once.
 template <bool kVec, int kCPC>
 cudaError_t cluster_finish(const VerifyArgs& a, int ctas, cudaStream_t stream, int* probe) {
   cudaLaunchConfig_t cfg = {};
@@ -1123,7 +1124,7 @@ cudaError_t cluster_finish(const VerifyArgs& a, int ctas, cudaStream_t stream, i
     int clusters = 0;
     cudaError_t e = cudaOccupancyMaxActiveClusters(&clusters, finish_cluster_kernel<kVec, kCPC>, &cfg);
     if (e != cudaSuccess) (void)cudaGetLastError();
-    *probe = (e == cudaSuccess && clusters > 0) ? 1 : 0;
+    *probe = e == cudaSuccess ? clusters : 0;
     return cudaSuccess;
   }
   return cudaLaunchKernelEx(&cfg, finish_cluster_kernel<kVec, kCPC>, a);
@@ -1134,8 +1135,9 @@ cudaError_t cluster_finish_any(const VerifyArgs& a, bool vec, int ctas, cudaStre
   return vec ? cluster_finish<true, kCPC>(a, ctas, stream, probe) : cluster_finish<false, kCPC>(a, ctas, stream, probe);
 }
 
-// Whether clusters of `ctas` CTAs (kCPC = 2 when above 8) fit on this
-// device, probed once per (size, load width) and process: 0 unknown, 1 yes, 2 no.
+// How many clusters of `ctas` CTAs (kCPC = 2 when above 8) are resident on
+// this device at once, probed once per (size, load width) and process:
+// stored plus one (0 unknown).
 std::atomic<int> g_cluster_fits[kMaxClusterCtas + 1][2];
 
 // CTAs of finish_kernel<kVec> resident on the device at once (0 unknown).
@@ -1153,13 +1155,15 @@ cudaError_t launch_verify_sampling(const VerifyArgs& a, cudaStream_t stream) {
     std::atomic<int>& fits = g_cluster_fits[ctas][vec ? 1 : 0];
     int f = fits.load(std::memory_order_relaxed);
     if (f == 0) {
-      int ok = 0;
-      if (two) cluster_finish_any<2>(a, vec, ctas, stream, &ok);
-      else cluster_finish_any<1>(a, vec, ctas, stream, &ok);
-      f = ok ? 1 : 2;
+      int n = 0;
+      if (two) cluster_finish_any<2>(a, vec, ctas, stream, &n);
+      else cluster_finish_any<1>(a, vec, ctas, stream, &n);
+      f = n + 1;
       fits.store(f, std::memory_order_relaxed);
     }
-    if (f == 1) {
+    // only while every sequence's cluster is resident at once: clusters in
+    // waves cost more than the grid kernel's single wave
+    if (a.B <= f - 1) {
       if (two) return cluster_finish_any<2>(a, vec, ctas, stream, nullptr);
       return cluster_finish_any<1>(a, vec, ctas, stream, nullptr);
     }
