@@ -56,7 +56,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 // softmax statistics clears the tickets the finishing kernel counts on.
 struct Layout {
   size_t ctrl_bytes = 0;
-  size_t fix = 0;                                     // stream-K fixup of the precise LM head
+  size_t fix = 0;                                     // stream-K fixup of the precise LM head (M <= 64)
   size_t tpart = 0, dpart = 0, res = 0, logits = 0;  // sampling
   size_t pmax = 0, pidx = 0;                                   // greedy
   int CA = 0, P = 0;
@@ -73,7 +73,7 @@ Layout make_layout(int B, int K, int V, bool greedy, bool logits_in_ws, bool fro
   size_t off = round_up(sizeof(int) * (kCtrlTickets + static_cast<size_t>(B)));
   L.ctrl_bytes = off;
   L.CA = (V + sv::kChunk - 1) / sv::kChunk;
-  const bool precise_head = !from_logits && M <= static_cast<size_t>(sv::kPreciseMaxM);
+  const bool precise_head = !from_logits && M <= 64;
   if (precise_head) {
     L.fix = off;
     off += round_up(sv::kFixupBytes);

@@ -74,9 +74,6 @@ struct HeadPlan {
 
 // Upper bound of the LM head's grid (sizes the per-CTA workspace areas).
 constexpr int kMaxHeadGrid = 256;
-// Positions up to which the LM head takes the precise scheme (above it the
-// large-batch scheme, which measured faster from 64 positions).
-constexpr int kPreciseMaxM = 56;
 // Fixup area of the stream-K schedule: 128 x 64 floats per CTA, then 4
 // 64-bit flags per CTA.
 constexpr size_t kFixupFloatsPerCta = 128 * 64;

@@ -995,8 +995,7 @@ cudaError_t launch_mode(HeadOut mode, const CUtensorMap& map_w, const CUtensorMa
 
 HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, bool streamk) {
   HeadPlan h;
-  // (K = 0 draft step at B = 64: precise 201 us, large-batch scheme 193 us)
-  if (M <= kPreciseMaxM) {
+  if (M <= 64) {
     h.precise = true;
     h.N = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 48 ? 48 : 64));
     h.num_chunks = 1;

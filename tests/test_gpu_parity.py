@@ -288,8 +288,7 @@ def test_determinism_bits():
                                        (12, 8, 384, 4099, 1.0),
                                        (9, 4, 384, 2000, 0.7),      # M = 45: 48 columns, last chunk partial
                                        (13, 3, 256, 3001, 1.1),     # M = 52: 64 columns
-                                       (8, 6, 512, 7000, 0.9),      # M = 56: the largest precise batch
-                                       (8, 7, 512, 7000, 0.9),      # M = 64: the large-batch scheme
+                                       (8, 7, 512, 7000, 0.9),      # M = 64: every column used
                                        (2, 3, 256, 3000, 1e-6),     # |z / T| in log2 units around 2^22
                                        (2, 3, 256, 3000, 1e-8),     # ... and beyond 2^24
                                        (40, 7, 256, 3001, 0.9),     # M = 320: two position chunks of 160
