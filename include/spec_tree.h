@@ -42,6 +42,13 @@
  * == 0.  Ownership, asynchrony, alignment (16 bytes) and the error word
  * (spec_verify_read_error on the workspace) as in spec_verify.h; the
  * workspace needs no initialisation.
+ *
+ * Execution (T > 0): one thread-block cluster per tree walks it; the
+ * library takes clusters of 16, 12 or 8 CTAs, the largest of which all B
+ * trees are resident at once.  The environment variable
+ * SPEC_TREE_CLUSTER_CTAS = 8, 12 or 16 forces one of these sizes where such
+ * a cluster fits (read at every call; the tokens drawn are the same up to
+ * the draw band of the summation order).
  */
 #ifndef SPEC_TREE_H_
 #define SPEC_TREE_H_
