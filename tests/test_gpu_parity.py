@@ -16,7 +16,7 @@ import oracle
 import speculative_decoding_verification_67_gb300 as sv
 from speculative_decoding_verification_67_gb300 import synth
 
-from _helpers import (LOGIT_ATOL, compare_debug, compare_greedy, compare_sampling, logits_error, np64, np_int,
+from _helpers import (DRAW_BAND, LOGIT_ATOL, compare_debug, compare_greedy, compare_sampling, logits_error, np64, np_int,
                       t32)
 
 pytestmark = pytest.mark.gpu
@@ -483,6 +483,57 @@ def test_full_size_sampling_workload(name):
     print(f"\n{name}: logits {err}; decisions {st}; accepted {np_int(n).tolist()}")
     assert err["max_abs"] <= LOGIT_ATOL, err
     compare_debug(np64(dbg), ref, np_int(n), w.K, w.temperature, err["max_abs"])
+
+
+def _draws_moved_by_logit_error(z32, z64, T, seed, per_row=256):
+    """Fraction of inverse-CDF draws (fp64 arithmetic on both sides, fresh
+    uniforms per row) whose token changes when the fp64 logits are replaced
+    by the LM head's, outside the draw band."""
+    rng = np.random.default_rng(seed)
+    moved = draws = 0
+    for r in range(z64.shape[0]):
+        def cdf(z):
+            p = np.exp((z - z.max()) / T)
+            c = np.cumsum(p)
+            return c / c[-1], p / c[-1]
+        c64, p64 = cdf(z64[r])
+        c32, _ = cdf(z32[r])
+        u = rng.random(per_row)
+        y64 = np.minimum(np.searchsorted(c64, u, side="right"), len(c64) - 1)
+        y32 = np.minimum(np.searchsorted(c32, u, side="right"), len(c32) - 1)
+        lo = u - np.where(y64 > 0, c64[np.maximum(y64 - 1, 0)], 0.0)
+        hi = c64[y64] - u
+        near = np.minimum(lo, hi) < DRAW_BAND * p64[y64]
+        moved += int(((y64 != y32) & ~near).sum())
+        draws += len(u)
+    return moved / draws, draws
+
+
+def test_head_precision_keeps_draws_headline():
+    """The precise LM head's own logit error moves under 0.1 % of inverse-CDF
+    draws against the fp64 logits (40 rows of the headline workload)."""
+    w = synth.WORKLOADS["head_B8_K4_V128256"]
+    inp = synth.make_inputs(w, device="cuda")
+    z32 = np64(sv.spec_lm_head(inp["hidden"], inp["W"]))
+    z64 = oracle.lm_head(np64(inp["hidden"]), inp["W"].float().cpu().numpy())
+    rate, draws = _draws_moved_by_logit_error(z32, z64, t32(w.temperature), seed=5)
+    print(f"\nheadline: {rate * 100:.3f} % of {draws} draws moved by the LM head's error")
+    assert rate < 1e-3
+
+
+@pytest.mark.xfail(strict=True, reason="the large-batch LM head scheme (above 64 positions) moves ~0.24 % of "
+                                       "draws at d = 8192, above the 0.1 % budget")
+def test_head_precision_keeps_draws_large_batch():
+    """The same measure on 48 rows of the B=64, d=8192 workload, whose LM head
+    (576 positions) runs the large-batch scheme."""
+    w = synth.WORKLOADS["head_B64_K8_V152064"]
+    inp = synth.make_inputs(w, device="cuda")
+    rows = 48
+    z32 = np64(sv.spec_lm_head(inp["hidden"], inp["W"])[:rows])
+    z64 = oracle.lm_head(np64(inp["hidden"][:rows]), inp["W"].float().cpu().numpy())
+    rate, draws = _draws_moved_by_logit_error(z32, z64, t32(w.temperature), seed=6)
+    print(f"\nB64: {rate * 100:.3f} % of {draws} draws moved by the LM head's error")
+    assert rate < 1e-3
 
 
 def test_full_size_many_draws_b8_v128256():
