@@ -268,16 +268,30 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
   // in the small-batch scheme, whose weight stream leaves the SM idle; next
   // to the large-batch head's tensor-bound MMAs that work slowed them by
   // ~30 % (B=64, K=8, V=152064), so there a separate streaming pass follows.
-  if (!plan.precise) hs.draft_rows = 0;
-  e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kStats, logits, nullptr, nullptr, &hs, err, true,
-                      dev, s, &enc_fail, ldz, L.fix ? ws + L.fix : nullptr);
-  if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
-  if (!plan.precise) {
-    e = sv::launch_row_stats(nullptr, draft_logits, 0, dims.B * dims.K, dims.V, hs.c_hi, hs.c_lo, nullptr, hs.dpart,
-                             nullptr, nullptr, 0, s, dims.V);
+  int Pt = plan.target_parts;
+  if (plan.wide) {
+    // Above 64 positions the LM head accumulates in the wide precise scheme
+    // and only writes logits (its epilogue would otherwise hold up the
+    // tensor cores); one streaming pass then forms every target and draft
+    // row's partials, one per 4096-token chunk.
+    e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kLogits, logits, nullptr, nullptr, nullptr, err,
+                        true, dev, s, &enc_fail, ldz, nullptr);
+    if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
+    e = sv::launch_row_stats(logits, draft_logits, M, dims.B * dims.K, dims.V, hs.c_hi, hs.c_lo, hs.tpart, hs.dpart,
+                             err, hs.tickets, hs.n_tickets, s, ldz);
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
+    Pt = L.CA;
+  } else {
+    if (!plan.precise) hs.draft_rows = 0;
+    e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kStats, logits, nullptr, nullptr, &hs, err,
+                        true, dev, s, &enc_fail, ldz, L.fix ? ws + L.fix : nullptr);
+    if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
+    if (!plan.precise) {
+      e = sv::launch_row_stats(nullptr, draft_logits, 0, dims.B * dims.K, dims.V, hs.c_hi, hs.c_lo, nullptr,
+                               hs.dpart, nullptr, nullptr, 0, s, dims.V);
+      if (e != cudaSuccess) return SPEC_ERR_CUDA;
+    }
   }
-  const int Pt = plan.target_parts;
   if (!mark(1)) return SPEC_ERR_CUDA;
   sv::VerifyArgs a = sampling_args(L, dims, temperature, logits, draft_logits, draft_tokens, uniforms,
                                    out_tokens, out_num_accepted, out_debug, ws, Pt);

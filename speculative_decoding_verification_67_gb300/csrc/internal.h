@@ -53,7 +53,7 @@ constexpr int kHeadTileV = 128;   // vocabulary rows per tile (MMA M)
 constexpr int kHeadTileK = 64;    // hidden elements per pipeline stage (128-byte rows)
 
 struct HeadPlan {
-  bool precise = false; // per-hidden-block TMEM slots summed in registers (N = 32, 48 or 64)
+  bool precise = false; // groups of hidden blocks in rotating TMEM slots, summed in registers
   int N = 0;            // positions per tile (MMA N), multiple of 16, <= 256
   int num_chunks = 0;   // position chunks, ceil(M / N)
   int num_vt = 0;       // vocabulary tiles, ceil(V / 128)
@@ -70,6 +70,10 @@ struct HeadPlan {
   // equal contiguous range of the num_tiles * groups (tile, 4-block group) units
   bool streamk = false;
   int groups = 1;        // units per tile
+  // the wide precise scheme (above 64 positions, logits and statistics):
+  // 128-position chunks, four 128-column slots of gkb hidden blocks each
+  bool wide = false;
+  int gkb = 4;           // hidden blocks accumulated per TMEM slot (precise schemes)
 };
 
 // Upper bound of the LM head's grid (sizes the per-CTA workspace areas).

@@ -27,14 +27,20 @@
 //    reduce the draft logits to the same partials meanwhile, hidden under the
 //    weight stream (beside the large-batch scheme's tensor-bound MMAs that
 //    work slowed them, so the caller passes no draft rows there);
-//  * two accumulation schemes.  Standard (any N): one TMEM accumulator per
-//    tile over the whole hidden size, double-buffered so the epilogue of a
-//    tile overlaps the next tile's MMAs.  Precise (N <= 64, the small-batch
+//  * three accumulation schemes.  Precise (N <= 64, the small-batch
 //    regime): every four 64-wide hidden blocks are accumulated into a fresh
 //    TMEM slot (4 slots rotate) and the epilogue adds the slot results in
 //    f32 registers with round-to-nearest, so the tensor core's own
 //    accumulation only ever spans 256 products; this cuts the logits' error
-//    against exact arithmetic several-fold at no cost to the weight stream;
+//    against exact arithmetic several-fold at no cost to the weight stream.
+//    Wide precise (above 64 positions, logits and statistics): the same with
+//    128-position chunks and slots of 16 hidden blocks (1024 products), the
+//    sums emitted through the large-batch scheme's epilogue blocks; an
+//    accumulator over the whole hidden size would move ~0.24 % of the
+//    sampling step's inverse-CDF draws at d = 8192, this keeps it ~0.01 %.
+//    Standard (greedy above 64 positions, any N <= 256): one TMEM
+//    accumulator per tile over the whole hidden size, double-buffered so the
+//    epilogue of a tile overlaps the next tile's MMAs;
 //  * every wait is bounded; a timeout sets the error word, drains the copies
 //    in flight and frees TMEM before returning.
 #include <cudaTypedefs.h>
@@ -54,7 +60,7 @@ namespace {
 constexpr int kThreads = 256;  // 8 warps: producer, MMA, 4 epilogue, 2 draft statistics
 constexpr uint32_t kABytes = kHeadTileV * kHeadTileK * 2;  // 16 KB W tile per stage
 constexpr uint32_t kBarrierBytes = 512;
-constexpr int kRunChunks = 4;                              // position chunks whose partials a CTA keeps running
+constexpr int kRunChunks = 5;                              // position chunks whose partials a CTA keeps running
 constexpr int kStatPitch = 20;                             // floats per row of a warp's 32x16 transpose block
 constexpr uint32_t kStatsBytes = (3 * 4 * 256 + 4 * 32 * kStatPitch) * 4;  // k, sum hi, sum lo [4][256] + blocks
 constexpr int kArgPitch = 36;                              // floats per row of a warp's 32x32 transpose block
@@ -62,6 +68,8 @@ constexpr uint32_t kArgmaxSmallBytes = 2 * 4 * 256 * 4;    // greedy scratch: [4
 constexpr uint32_t kArgmaxBytes = kArgmaxSmallBytes + 4 * 32 * kArgPitch * 4;  // + the 4 transpose blocks
 constexpr int kSlotsPrecise = 4;
 constexpr int kGroupPrecise = 4;  // hidden blocks accumulated per TMEM slot (precise scheme)
+constexpr int kWideN = 128;       // positions per chunk of the wide precise scheme
+constexpr int kGroupWide = 16;    // hidden blocks per TMEM slot there (slot span 1024 products)
 
 constexpr int kModeLogits = static_cast<int>(HeadOut::kLogits);
 constexpr int kModeArgmax = static_cast<int>(HeadOut::kArgmax);
@@ -69,7 +77,8 @@ constexpr int kModeStats = static_cast<int>(HeadOut::kStats);
 
 struct HeadParams {
   int M, d, V;
-  int streamk, groups;          // stream-K schedule; units per tile
+  int streamk, groups;          // stream-K schedule; units (slot groups) per tile
+  int gkb;                      // hidden blocks per TMEM slot (precise schemes)
   float* fix;                   // [grid][64][128] partial sums handed to a tile's first CTA
   unsigned long long* flags;    // [grid][4] = epoch once the CTA's quadrant's sums are stored
   unsigned long long epoch;     // unique per launch
@@ -485,8 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && work_next(p, wc, tile, g0, g1)) {
         const int vt = tile / p.num_chunks;
         const int pc = tile - vt * p.num_chunks;
-        const int kb0 = kPrecise ? g0 * kGroupPrecise : 0;
-        const int kb1 = kPrecise ? min(g1 * kGroupPrecise, p.num_kb) : p.num_kb;
+        const int kb0 = kPrecise ? g0 * p.gkb : 0;
+        const int kb1 = kPrecise ? min(g1 * p.gkb, p.num_kb) : p.num_kb;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u)) {
             report_timeout(p.err);
@@ -539,16 +548,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after_sync();
         }
-        const int kb0 = kPrecise ? g0 * kGroupPrecise : 0;
-        const int kb1 = kPrecise ? min(g1 * kGroupPrecise, p.num_kb) : p.num_kb;
+        const int kb0 = kPrecise ? g0 * p.gkb : 0;
+        const int kb1 = kPrecise ? min(g1 * p.gkb, p.num_kb) : p.num_kb;
+        // position in the current slot group (kb0 starts one); a counter, not
+        // kb % gkb: an integer division per hidden block in this one issuing
+        // thread held the tensor pipe back (wide scheme at 128 positions: 275
+        // vs 212 us per call)
+        int gpos = 0;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[s], ph)) {
             report_timeout(p.err);
             ok = false;
             break;
           }
-          const bool group_first = !kPrecise || (kb % kGroupPrecise) == 0;
-          const bool group_last = kPrecise && ((kb + 1) % kGroupPrecise == 0 || kb + 1 == p.num_kb);
+          const bool group_first = !kPrecise || gpos == 0;
+          const bool group_last = kPrecise && (gpos == p.gkb - 1 || kb + 1 == p.num_kb);
+          gpos = group_last ? 0 : gpos + 1;
           if (kPrecise && group_first) {
             if (!mbar_wait(&afree[slot], sph ^ 1u)) {
               report_timeout(p.err);
@@ -615,7 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     // precise statistics keep per-thread running partials instead of
     // reducing every tile across the quadrants
-    constexpr bool run_stats = kPrecise && kMode == kModeStats;
+    constexpr bool kWide = kPrecN > 64;  // wide precise scheme: the large-batch emit from registers
+    constexpr bool run_stats = kPrecise && !kWide && kMode == kModeStats;
     constexpr bool reduce = kMode != kModeLogits && !run_stats;  // cross-quadrant scratch per tile
     constexpr int kRun = run_stats ? kPrecN : 1;
     Partial run[2 * kRunChunks];  // [chunk][column / 128]: running partials of the standard scheme
@@ -645,7 +661,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float acc[kPrecN];
 #pragma unroll
         for (int i = 0; i < kPrecN; ++i) acc[i] = 0.f;
-        if (g0 == 0 && g1 < p.groups) {
+        if (!kWide && g0 == 0 && g1 < p.groups) {
+          // (stream-K, small precise scheme only)
           // The first part of a tile whose other groups belong to the next
           // CTA(s), each of which stored them before anything else: start
           // from their sums (the loads' latency then hides behind this tile's
@@ -711,7 +728,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        if (g0 > 0) {
+        if (!kWide && g0 > 0) {
           // a later part of a tile: hand this quadrant's sums to the CTA that
           // owns the tile's first group, and emit nothing
           float* f = p.fix + static_cast<size_t>(blockIdx.x) * kFixupFloatsPerCta + et;
@@ -752,6 +769,31 @@ __global__ void __launch_bounds__(kThreads, 1)
               rk[i] = rn;
               const float t = exp2f((h - rn) + expo_lo(z, h, c));
               rs[i] += in ? t : 0.f;
+            }
+          }
+        } else if constexpr (kWide) {
+          // the large-batch scheme's emit, 32 columns at a time from the sums
+#pragma unroll
+          for (int c0 = 0; c0 < kPrecN; c0 += 32) {
+            if (m0 + c0 >= p.M) break;
+            if constexpr (kMode == kModeArgmax) {
+              float v32[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v32[i] = acc[c0 + i];
+              argmax_transpose<32>(p, v32, c0, v, q, lane, scr);
+            } else {
+              float lo[16], hi[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                lo[i] = acc[c0 + i];
+                hi[i] = acc[c0 + 16 + i];
+              }
+              emit16<kModeLogits>(p, lo, c0, m0, v, q, lane, scr);
+              emit16<kModeLogits>(p, hi, c0 + 16, m0, v, q, lane, scr);
+              if constexpr (kMode == kModeStats) {
+                stats_transpose16(p, lo, c0, v, q, lane, scr);
+                stats_transpose16(p, hi, c0 + 16, v, q, lane, scr);
+              }
             }
           }
         } else {
@@ -962,10 +1004,10 @@ cudaError_t launch_variant(const CUtensorMap& map_w, const CUtensorMap& map_h, c
     if (e != cudaSuccess) return e;
     attr_done[dev.device] = true;
   }
-  // the precise scheme is launched as a programmatic dependent of the kernel
-  // before it (see the epilogue's wait): at B=8, V=128256 this hides most of
-  // the previous step's finishing kernel (177 vs 185 us per step); the large
-  // standard-scheme batches measured slightly slower with it, so they launch
+  // the small precise scheme is launched as a programmatic dependent of the
+  // kernel before it (see the epilogue's wait): at B=8, V=128256 this hides
+  // most of the previous step's finishing kernel (177 vs 185 us per step);
+  // the large batches measured slightly slower with it, so they launch
   // plainly
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(h.grid);
@@ -976,7 +1018,7 @@ cudaError_t launch_variant(const CUtensorMap& map_w, const CUtensorMap& map_h, c
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = h.precise ? 1 : 0;
+  cfg.numAttrs = (h.precise && !h.wide) ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, head_kernel<kPrecN, kMode>, map_w, map_h, p);
 }
 
@@ -999,10 +1041,22 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
     h.precise = true;
     h.N = M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 48 ? 48 : 64));
     h.num_chunks = 1;
+    h.gkb = kGroupPrecise;
     // tcgen05.alloc takes a power of two >= 32 columns
     uint32_t cols = 32;
     while (cols < static_cast<uint32_t>(kSlotsPrecise * h.N)) cols <<= 1;
     h.tmem_cols = cols;
+  } else if (mode != HeadOut::kArgmax) {
+    // Sampling needs logits close to the exact ones: an accumulator that
+    // spans the whole hidden dimension (8192 products at d = 8192) moves
+    // ~0.24 % of inverse-CDF draws against fp64 logits, groups of 1024
+    // products summed in registers keep that far below 0.1 %.
+    h.precise = true;
+    h.wide = true;
+    h.N = kWideN;
+    h.num_chunks = (M + kWideN - 1) / kWideN;
+    h.gkb = kGroupWide;
+    h.tmem_cols = kSlotsPrecise * kWideN;
   } else {
     const int chunks = (M + 255) / 256;
     const int per = (M + chunks - 1) / chunks;
@@ -1020,15 +1074,15 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
   // per-tile statistics of the standard scheme only
   size_t scratch = 0;
   if (mode == HeadOut::kArgmax) scratch = h.precise ? kArgmaxSmallBytes : kArgmaxBytes;
-  if (mode == HeadOut::kStats && !h.precise) scratch = kStatsBytes;
+  if (mode == HeadOut::kStats && (!h.precise || h.wide)) scratch = kStatsBytes;
   const size_t fixed = 1024 + kBarrierBytes + scratch;
   const size_t budget = static_cast<size_t>(dev.max_smem_optin);
   int stages = static_cast<int>((budget - fixed) / stage);
   stages = std::min(12, std::max(2, stages));
   h.stages = stages;
   h.smem_bytes = fixed + static_cast<size_t>(stages) * stage;
-  h.streamk = streamk && h.precise;
-  h.groups = h.precise ? (h.num_kb + kGroupPrecise - 1) / kGroupPrecise : 1;
+  h.streamk = streamk && h.precise && !h.wide;
+  h.groups = h.precise ? (h.num_kb + h.gkb - 1) / h.gkb : 1;
   const long long units = h.streamk ? static_cast<long long>(h.num_tiles) * h.groups : h.num_tiles;
   h.grid = static_cast<int>(std::min<long long>(units, std::min(dev.sm_count, kMaxHeadGrid)));
   // one running partial per CTA and target row while a thread's share of
@@ -1067,6 +1121,7 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
   p.ldz = ldz > 0 ? ldz : V;
   p.streamk = h.streamk ? 1 : 0;
   p.groups = h.groups;
+  p.gkb = h.gkb;
   p.fix = h.streamk ? static_cast<float*>(fixup) : nullptr;
   p.flags = h.streamk ? reinterpret_cast<unsigned long long*>(static_cast<char*>(fixup) +
                                                               kMaxHeadGrid * kFixupFloatsPerCta * 4)
@@ -1091,6 +1146,7 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
     p.n_tickets = stats->n_tickets;
   }
   if (!h.precise) return launch_mode<0>(mode, map_w, map_h, p, h, dev, stream);
+  if (h.wide) return launch_mode<kWideN>(mode, map_w, map_h, p, h, dev, stream);
   if (h.N == 16) return launch_mode<16>(mode, map_w, map_h, p, h, dev, stream);
   if (h.N == 32) return launch_mode<32>(mode, map_w, map_h, p, h, dev, stream);
   if (h.N == 48) return launch_mode<48>(mode, map_w, map_h, p, h, dev, stream);

@@ -81,7 +81,7 @@ def test_lm_head_is_deterministic():
 
 @pytest.mark.parametrize("B,K,T", [(2, 3, 0.9),      # 16-column precise head, stream-K split tiles
                                    (8, 4, 0.8),      # 48 columns
-                                   (40, 7, 1.1),     # large-batch scheme, two position chunks, fused statistics
+                                   (40, 7, 1.1),     # wide precise scheme, three position chunks, statistics pass
                                    (40, 7, 0.0)])    # large-batch greedy (transposed argmax epilogue)
 def test_whole_step_is_deterministic(B, K, T):
     """The same inputs twice through the whole step (LM head, statistics,
@@ -291,10 +291,10 @@ def test_determinism_bits():
                                        (8, 7, 512, 7000, 0.9),      # M = 64: every column used
                                        (2, 3, 256, 3000, 1e-6),     # |z / T| in log2 units around 2^22
                                        (2, 3, 256, 3000, 1e-8),     # ... and beyond 2^24
-                                       (40, 7, 256, 3001, 0.9),     # M = 320: two position chunks of 160
-                                       (20, 12, 128, 1500, 1.3),    # M = 260: chunks of 144 and 116 rows
-                                       (100, 10, 128, 2000, 1.0),   # M = 1100: 5 chunks, per-tile partials
-                                       (80, 0, 128, 1000, 1.0)])    # large-batch scheme, bonus draws only
+                                       (40, 7, 256, 3001, 0.9),     # M = 320: wide precise scheme, chunks of 128 (the last 64)
+                                       (20, 12, 128, 1500, 1.3),    # M = 260: three chunks, the last 4 rows
+                                       (100, 10, 128, 2000, 1.0),   # M = 1100: 9 chunks
+                                       (80, 0, 128, 1000, 1.0)])    # wide precise scheme, bonus draws only
 def test_spec_verify_small(B, K, d, V, T):
     w = synth.custom("small", B=B, K=K, d=d, V=V, temperature=T, seed=B + K + d + V)
     inp, tok, n, logits, dbg = _run_head_case(w)
@@ -388,11 +388,11 @@ def test_nonfinite_logit_marks_the_sequence():
     assert np_int(n3)[1] == -1
 
 
-@pytest.mark.parametrize("B,K", [(3, 2), (24, 4)])   # small-batch and large-batch LM-head schemes
+@pytest.mark.parametrize("B,K", [(3, 2), (24, 4)])   # precise and wide precise LM-head schemes
 def test_nonfinite_hidden_marks_the_sequence(B, K):
     """A NaN or infinite hidden state makes its position's logits non-finite
-    inside the LM head's fused statistics: that sequence is flagged, the
-    others are unaffected."""
+    (in the precise head's fused statistics, or in the statistics pass after
+    the wide head): that sequence is flagged, the others are unaffected."""
     w = synth.custom("nf_head", B=B, K=K, d=256, V=3000, temperature=1.0, seed=21 + B)
     inp = synth.make_inputs(w, device="cuda")
     B, K, V, T = w.B, w.K, w.V, w.temperature
@@ -521,11 +521,10 @@ def test_head_precision_keeps_draws_headline():
     assert rate < 1e-3
 
 
-@pytest.mark.xfail(strict=True, reason="the large-batch LM head scheme (above 64 positions) moves ~0.24 % of "
-                                       "draws at d = 8192, above the 0.1 % budget")
 def test_head_precision_keeps_draws_large_batch():
     """The same measure on 48 rows of the B=64, d=8192 workload, whose LM head
-    (576 positions) runs the large-batch scheme."""
+    (576 positions) runs the wide precise scheme (an accumulator over the
+    whole hidden size moved ~0.24 % of these draws)."""
     w = synth.WORKLOADS["head_B64_K8_V152064"]
     inp = synth.make_inputs(w, device="cuda")
     rows = 48
@@ -603,8 +602,10 @@ def test_full_size_greedy_sampled_sequences():
     print(f"\ngreedy full size: {st}; logits {err}; accepted mean {np_int(n).mean():.3f}")
     assert st["mismatched_near_ties"] == 0, st
     np.testing.assert_array_equal(np64(dbg)[seqs][:, :, 1].astype(np.int64), ref["argmax"])
-    # the fused argmax epilogue saw exactly the values the plain LM head writes
-    np.testing.assert_array_equal(np64(dbg)[seqs][:, :, 0].reshape(-1), np64(z_gpu).max(axis=1))
+    # the fused argmax epilogue's maxima are the rows' largest logits (the
+    # greedy head accumulates in the large-batch scheme, the plain head on
+    # these 80 rows in the wide precise one: equal within the logit tolerance)
+    np.testing.assert_allclose(np64(dbg)[seqs][:, :, 0].reshape(-1), z.max(axis=1), rtol=0, atol=1e-3)
 
 
 @pytest.mark.parametrize("B,K,d,V,T", [(1, 4, 4096, 1000, 1.0),     # 8 tiles x 16 groups: 16-way splits
