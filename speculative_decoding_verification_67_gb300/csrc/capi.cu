@@ -271,9 +271,8 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
   int Pt = plan.target_parts;
   if (plan.wide) {
     // Above 64 positions the LM head accumulates in the wide precise scheme
-    // and only writes logits (its epilogue would otherwise hold up the
-    // tensor cores); one streaming pass then forms every target and draft
-    // row's partials, one per 4096-token chunk.
+    // and writes logits; one streaming pass then forms every target and
+    // draft row's partials, one per 4096-token chunk.
     e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kLogits, logits, nullptr, nullptr, nullptr, err,
                         true, dev, s, &enc_fail, ldz, nullptr);
     if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
