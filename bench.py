@@ -883,7 +883,9 @@ def main():
     finish_ms = statistics.mean(t[1].elapsed_time(t[2]) for t in evs)
     nb = step_bytes(w)
     # the timed interval also covers the draft logits' read (by the head's side
-    # warps at M <= 64, by the statistics pass after the head above that)
+    # warps at M <= 64; above that by the statistics pass after the head, which
+    # also re-reads the target logits the head wrote: traffic beyond the
+    # algorithmic bytes, counted against the path)
     head_bytes = nb["head"] if w.greedy else nb["step"]
     gbs = head_bytes / (head_ms * 1e-3) / 1e9
     tflops = nb["flops"] / (head_ms * 1e-3) / 1e12
@@ -895,7 +897,7 @@ def main():
     roofline.update({"traffic": NCU_TRAFFIC.get(w.name), "peak_kind": peak_kind, "launch_ms": head_ms,
                      "kernel": ("head_kernel (LM head)" if w.greedy else
                                 "head_kernel (LM head + fused softmax statistics)" if w.M <= 64 else
-                                "head_kernel (LM head + fused target statistics) + row_stats_kernel (draft statistics)"),
+                                "head_kernel (LM head, wide precise) + row_stats_kernel (target and draft statistics)"),
                      "bytes_per_launch": head_bytes, "flops_per_launch": nb["flops"],
                      "finish_kernel_ms": finish_ms})
     # the whole step against whichever of the step's bytes or flops binds
