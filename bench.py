@@ -805,6 +805,9 @@ def main():
     ap.add_argument("--ngram-workload", default="ngram_B256_L32768_K8", choices=sorted(synth.NGRAM_WORKLOADS))
     ap.add_argument("--draft-workload", default="draft_B8_K4_V128256", choices=sorted(synth.DRAFT_WORKLOADS))
     ap.add_argument("--tree-workload", default="tree_B8_N16_V128256", choices=sorted(synth.TREE_WORKLOADS))
+    ap.add_argument("--shape", default=None, metavar="B,K,d,V,T",
+                    help="a workload of the same recipe at other sizes (small cases for ncu captures); "
+                         "overrides --workload")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.row == "kv_commit":
@@ -825,7 +828,12 @@ def main():
             return run_ngram_reference(args)
         args.steps = min(args.steps, 500)
         return run_ngram(args)
-    w = synth.WORKLOADS[args.workload]
+    if args.shape:
+        B_, K_, d_, V_, T_ = args.shape.split(",")
+        w = synth.custom(f"shape_B{B_}_K{K_}_d{d_}_V{V_}_T{T_}", B=int(B_), K=int(K_), d=int(d_), V=int(V_),
+                         temperature=float(T_), noise=0.3, seed=1)
+    else:
+        w = synth.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)
         return

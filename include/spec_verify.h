@@ -141,8 +141,13 @@ SPEC_API size_t spec_verify_workspace_bytes(spec_dims dims, float temperature, i
  *
  * Dense part: the LM head is a bf16 x bf16 -> f32 contraction on the
  * tensor cores (tcgen05, TMEM accumulators, TMA-fed), streaming W_lm once.
- * Decision arithmetic: logits/T in f32 (IEEE division), exp in f32, row
- * normalisers and residual prefix sums accumulated in f64.
+ * Decision arithmetic (no f64 anywhere): exp(z/T) is evaluated as 2^(z*c)
+ * with c = log2(e)/T held as a pair of f32 values; every row normaliser and
+ * every residual mass or prefix sum is a float-float (paired f32, TwoSum)
+ * sum of terms scaled against an integer power-of-two reference, so the
+ * scaling is exact and the sums carry no systematic error above ~1e-12
+ * (each token's own term keeps the f32 rounding of one exponent and one
+ * exp2f); the ratio S_p/S_q used by the residual is a float-float quotient.
  */
 SPEC_API spec_status spec_verify(const void *hidden, const void *W_lm, const float *draft_logits,
                         const int32_t *draft_tokens, const float *uniforms, float temperature,
@@ -168,8 +173,13 @@ SPEC_API spec_status spec_verify_timed(const void *hidden, const void *W_lm, con
 /*
  * The verify-and-accept part alone, on given target logits
  * (device f32 [B*(K+1)][V]); same arguments and rules as spec_verify
- * otherwise.  dims.d is ignored.  Workspace: spec_verify_workspace_bytes(dims, T, 0).
+ * otherwise.  dims.d is ignored.  Workspace: at least
+ * spec_verify_from_logits_workspace_bytes(dims, T) bytes (with no LM head
+ * there is no stream-K area and one partial per 4096-token chunk, so this is
+ * at most spec_verify_workspace_bytes(dims, T, 0), which also suffices).
  */
+SPEC_API size_t spec_verify_from_logits_workspace_bytes(spec_dims dims, float temperature);
+
 SPEC_API spec_status spec_verify_from_logits(const float *target_logits, const float *draft_logits,
                                     const int32_t *draft_tokens, const float *uniforms,
                                     float temperature, int32_t *out_tokens,
@@ -191,9 +201,10 @@ SPEC_API spec_status spec_verify_from_logits(const float *target_logits, const f
  * memory inside the library, which every GPU that loads the library holds
  * until the process exits.
  *
- *  - Requests whose workspace, spec_verify_workspace_bytes(dims, T, 0), would
- *    exceed SPEC_NOALLOC_SCRATCH_BYTES are refused with
- *    SPEC_ERR_SCRATCH_LIMIT before anything is enqueued.
+ *  - Requests whose workspace, spec_verify_from_logits_workspace_bytes(dims, T),
+ *    would exceed SPEC_NOALLOC_SCRATCH_BYTES are refused with
+ *    SPEC_ERR_SCRATCH_LIMIT before anything is enqueued (and before any
+ *    pointer is looked at); a request of exactly that size is served.
  *  - The first call on a device looks up the array's device address (a
  *    runtime query, once per device, with that device current); make that
  *    first call before capturing any stream on the device.
@@ -223,7 +234,8 @@ SPEC_API spec_status spec_verify_noalloc_read_error(int32_t *error_word, spec_st
  * state goes through the LM head to a score for every token):
  * logits[m][v] = sum_k hidden[m][k] * W_lm[v][k], bf16 inputs, f32 accumulate
  * and output.  hidden device bf16 [M][d], W_lm device bf16 [V][d], logits
- * device f32 [M][V].  1 <= M <= 4096, d % 8 == 0.  No workspace.
+ * device f32 [M][V].  1 <= M <= 2^24, 8 <= d <= 2^20 with d % 8 == 0.
+ * No workspace.
  */
 SPEC_API spec_status spec_lm_head(const void *hidden, const void *W_lm, float *logits, int32_t M,
                          int32_t d, int32_t V, spec_stream_t stream);

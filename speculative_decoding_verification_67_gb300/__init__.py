@@ -75,6 +75,7 @@ _SIGS = {
     "spec_abi_version": (_I32, []),
     "spec_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "spec_verify_workspace_bytes": (_SZ, [SpecDims, _F32, _I32]),
+    "spec_verify_from_logits_workspace_bytes": (_SZ, [SpecDims, _F32]),
     "spec_verify": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _SZ, _VP, _VP, _VP]),
     "spec_verify_timed": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _F32, _VP, _VP, SpecDims, _VP, _SZ, _VP, _VP, _VP,
                                          ctypes.POINTER(_VP)]),
@@ -159,6 +160,14 @@ def workspace_bytes(B: int, K: int, V: int, temperature: float, logits_in_worksp
     return int(n)
 
 
+def from_logits_workspace_bytes(B: int, K: int, V: int, temperature: float) -> int:
+    """Workspace of spec_verify_from_logits (and the no-allocation limit's measure)."""
+    n = library().spec_verify_from_logits_workspace_bytes(SpecDims(B, K, 0, V), float(temperature))
+    if n == 0:
+        raise ValueError("invalid sizes")
+    return int(n)
+
+
 def host_workspace_bytes(B: int, K: int, d: int, V: int, temperature: float) -> int:
     n = library().spec_verify_host_workspace_bytes(SpecDims(B, K, d, V), float(temperature))
     if n == 0:
@@ -228,7 +237,7 @@ def spec_verify_from_logits(target_logits, draft_logits, draft_tokens, uniforms,
     if out_debug is not None:
         _need(out_debug, "out_debug", torch.float32, (B, K + 1, SPEC_DEBUG_FIELDS), "cuda")
     out_tokens, out_num_accepted = _outputs(B, K, target_logits.device, out_tokens, out_num_accepted)
-    need = library().spec_verify_workspace_bytes(SpecDims(B, K, 0, V), T, 0)
+    need = library().spec_verify_from_logits_workspace_bytes(SpecDims(B, K, 0, V), T)
     if workspace is None:
         workspace = torch.empty(max(int(need), 16), dtype=torch.uint8, device=target_logits.device)
     _check(library().spec_verify_from_logits(

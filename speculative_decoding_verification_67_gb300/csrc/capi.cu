@@ -207,6 +207,11 @@ size_t spec_verify_workspace_bytes(spec_dims dims, float temperature, int32_t lo
   return make_layout(dims.B, dims.K, dims.V, temperature == 0.f, logits_in_workspace != 0, false).total;
 }
 
+size_t spec_verify_from_logits_workspace_bytes(spec_dims dims, float temperature) {
+  if (!dims_ok(dims, false) || !(temperature >= 0.f) || !std::isfinite(temperature)) return 0;
+  return make_layout(dims.B, dims.K, dims.V, temperature == 0.f, false, true).total;
+}
+
 }  // extern "C"
 
 namespace {
@@ -262,17 +267,13 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
   hs.dpart = reinterpret_cast<sv::StatPart*>(ws + L.dpart);
   hs.tickets = reinterpret_cast<unsigned*>(reinterpret_cast<int*>(ws) + kCtrlTickets);
   hs.n_tickets = dims.B;
-  // The LM head's epilogue produces the target statistics as it writes the
-  // logits (per CTA in the small-batch scheme, per vocabulary tile in the
-  // large-batch one).  The draft statistics come from the head's side warps
-  // in the small-batch scheme, whose weight stream leaves the SM idle; next
-  // to the large-batch head's tensor-bound MMAs that work slowed them by
-  // ~30 % (B=64, K=8, V=152064), so there a separate streaming pass follows.
+  // Up to 64 positions the LM head's epilogue produces the target statistics
+  // as it writes the logits (one partial per CTA), and its side warps reduce
+  // the draft rows meanwhile, hidden under the weight stream.  Above that the
+  // head is tensor-bound: it writes logits only, and one streaming pass forms
+  // every target and draft row's partials.
   int Pt = plan.target_parts;
-  if (plan.wide) {
-    // Above 64 positions the LM head accumulates in the wide precise scheme
-    // and writes logits; one streaming pass then forms every target and
-    // draft row's partials, one per 4096-token chunk.
+  if (plan.large) {
     e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kLogits, logits, nullptr, nullptr, nullptr, err,
                         true, dev, s, &enc_fail, ldz, nullptr);
     if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
@@ -281,15 +282,9 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
     Pt = L.CA;
   } else {
-    if (!plan.precise) hs.draft_rows = 0;
     e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kStats, logits, nullptr, nullptr, &hs, err,
                         true, dev, s, &enc_fail, ldz, L.fix ? ws + L.fix : nullptr);
     if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
-    if (!plan.precise) {
-      e = sv::launch_row_stats(nullptr, draft_logits, 0, dims.B * dims.K, dims.V, hs.c_hi, hs.c_lo, nullptr,
-                               hs.dpart, nullptr, nullptr, 0, s, dims.V);
-      if (e != cudaSuccess) return SPEC_ERR_CUDA;
-    }
   }
   if (!mark(1)) return SPEC_ERR_CUDA;
   sv::VerifyArgs a = sampling_args(L, dims, temperature, logits, draft_logits, draft_tokens, uniforms,
@@ -382,6 +377,8 @@ void* g_noalloc_ptr[64] = {nullptr};
 // Device address of the scratch array on the current device; looked up once
 // per device (host code cannot use the symbol's name as an address).
 spec_status noalloc_scratch(const DeviceInfo& dev, char** out) {
+  if (dev.device < 0 || dev.device >= static_cast<int>(sizeof(g_noalloc_ptr) / sizeof(g_noalloc_ptr[0])))
+    return SPEC_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   if (!g_noalloc_ptr[dev.device]) {
     void* ptr = nullptr;
@@ -402,8 +399,9 @@ spec_status spec_verify_from_logits_noalloc(const float* target_logits, const fl
                                             float* out_debug, spec_stream_t stream) {
   if (!dims_ok(dims, false)) return SPEC_ERR_DIMS;
   if (!(temperature >= 0.f) || !std::isfinite(temperature)) return SPEC_ERR_ARG;
-  const size_t need = make_layout(dims.B, dims.K, dims.V, temperature == 0.f, false, true).total;
-  if (need > SPEC_NOALLOC_SCRATCH_BYTES) return SPEC_ERR_SCRATCH_LIMIT;
+  // the same rule the header states: the exact from-logits workspace size
+  if (spec_verify_from_logits_workspace_bytes(dims, temperature) > SPEC_NOALLOC_SCRATCH_BYTES)
+    return SPEC_ERR_SCRATCH_LIMIT;
   DeviceInfo dev;
   spec_status st = device_status(dev);
   if (st != SPEC_OK) return st;

@@ -70,9 +70,10 @@ struct HeadPlan {
   // equal contiguous range of the num_tiles * groups (tile, 4-block group) units
   bool streamk = false;
   int groups = 1;        // units per tile
-  // the wide precise scheme (above 64 positions, logits and statistics):
-  // 128-position chunks, four 128-column slots of gkb hidden blocks each
-  bool wide = false;
+  // the large-batch kernel (above 64 positions, logits or greedy partials):
+  // chunks of N <= 256 positions, two N-column TMEM slots of gkb hidden
+  // blocks each, summed in registers by eight epilogue warps
+  bool large = false;
   int gkb = 4;           // hidden blocks accumulated per TMEM slot (precise schemes)
 };
 

@@ -953,6 +953,354 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
 }
 
+// ---------------------------------------------------------------- large batches
+// Above 64 positions.  A tile is 128 vocabulary rows times a position chunk of
+// N <= 256 columns (a multiple of 32; B = 64, K = 8 gives three chunks of 192,
+// B = 256, K = 4 five of 256), the same operand shapes as one accumulator over
+// the whole hidden size would use, so the tensor core sees the same operand
+// traffic per product.  The accumulation is precise: groups of kLargeGroup
+// hidden blocks (1024 products) go into two TMEM slots of N columns in turn,
+// and the epilogue adds the slots in f32 registers.  Eight epilogue warps
+// share the work: warp w reads TMEM lane quadrant w % 4 and one half of the
+// columns, so that a thread keeps N/2 <= 128 running sums; while it drains one
+// slot the MMAs fill the other.
+constexpr int kLargeWarps = 10;                  // producer, MMA, 8 epilogue warps
+constexpr int kLargeThreads = 32 * kLargeWarps;
+constexpr int kLargeGroup = 16;                  // hidden blocks per TMEM slot (1024 products)
+constexpr int kLargeHalfMax = 128;               // columns per epilogue thread at N = 256
+constexpr int kLargePitch = 20;                  // floats per row of a warp's 32 x 16 transpose block
+// greedy scratch: [4 quadrants][256 columns] values and indices, then one
+// 32 x 16 transpose block per epilogue warp
+constexpr uint32_t kLargeArgmaxBytes = (2 * 4 * 256 + 8 * 32 * kLargePitch) * 4;
+
+// Greedy partials of 16 columns [col, col + 16) over the warp's 32 rows: the
+// block goes through the warp's own transpose block (128-bit stores at a pitch
+// of 20 floats: conflict-free stores and column reads), then lane c < 16 scans
+// column col + c for the first row holding the largest finite value.  Rows
+// past V are skipped; a non-finite value marks the column (index -2).
+__device__ __forceinline__ void argmax_large16(const HeadParams& p, const float (&val)[16], int col, int v, int q,
+                                               int lane, float* tb, float* red_val, int* red_idx) {
+  __syncwarp();  // every lane's reads of the previous block are done
+#pragma unroll
+  for (int j = 0; j < 16; j += 4)
+    *reinterpret_cast<float4*>(tb + lane * kLargePitch + j) = make_float4(val[j], val[j + 1], val[j + 2], val[j + 3]);
+  __syncwarp();
+  const int v0 = v - lane;             // the warp's first row
+  const int rows = min(32, p.V - v0);  // of which inside the vocabulary (may be <= 0)
+  if (lane < 16) {
+    float best = -INFINITY;
+    int br = -1;
+    bool bad = false;
+#pragma unroll 8
+    for (int r = 0; r < 32; ++r) {
+      const float x = tb[r * kLargePitch + lane];
+      const bool use = r < rows;
+      const bool fin = isfinite(x);
+      bad |= use && !fin;
+      if (use && fin && x > best) {
+        best = x;
+        br = r;
+      }
+    }
+    red_val[q * 256 + col + lane] = best;
+    red_idx[q * 256 + col + lane] = bad ? -2 : (br < 0 ? 0x7fffffff : v0 + br);
+  }
+}
+
+// The tile's greedy partial per column: the four lane quadrants merged (the
+// lower quadrant holds the lower token ids, so equal values keep the lower).
+__device__ __forceinline__ void argmax_merge_large(const HeadParams& p, int N, int vt, int m0, int et,
+                                                   const float* red_val, const int* red_idx) {
+  for (int c = et; c < N; c += 256) {
+    const int m = m0 + c;
+    if (m >= p.M) continue;
+    float bv = red_val[c];
+    int bi = red_idx[c];
+    bool bad = bi == -2;
+#pragma unroll
+    for (int qq = 1; qq < 4; ++qq) {
+      const float ov = red_val[qq * 256 + c];
+      const int oi = red_idx[qq * 256 + c];
+      bad |= oi == -2;
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    p.part_max[static_cast<size_t>(m) * p.num_vt + vt] = bv;
+    p.part_idx[static_cast<size_t>(m) * p.num_vt + vt] = bad ? -2 : bi;
+  }
+}
+
+// kMode: kModeLogits (f32 logits) or kModeArgmax (per-tile greedy partials).
+template <int kMode>
+__global__ void __launch_bounds__(kLargeThreads, 1)
+    head_large_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_h,
+                      const HeadParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int S = p.stages;
+  const int N = p.N;
+  const int NH = N >> 1;  // columns per epilogue half
+  const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(N) * 128u;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
+  uint64_t* full = bars;              // [S] TMA landed
+  uint64_t* empty = bars + S;         // [S] MMAs reading the stage are done
+  uint64_t* afull = bars + 2 * S;     // [2] slot holds a finished group
+  uint64_t* afree = afull + 2;        // [2] slot drained by the 8 epilogue warps
+  uint64_t* mma_done = afree + 2;     // [1] teardown
+  uint64_t* red_full = mma_done + 1;  // [1] greedy scratch written by the 8 epilogue warps
+  uint64_t* red_free = red_full + 1;  // [1] greedy scratch consumed
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(red_free + 1);
+  float* scr = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + kBarrierBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&afull[i], 1);
+      mbar_init(&afree[i], 8);
+    }
+    mbar_init(mma_done, 1);
+    mbar_init(red_full, 8);
+    mbar_init(red_free, 8);
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensor_map(&tmap_w);
+    prefetch_tensor_map(&tmap_h);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, p.tmem_cols);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = l2_policy_evict_first();
+      const uint64_t pol_h = l2_policy_evict_last();
+      int s = 0;
+      uint32_t ph = 0;
+      long long issued = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const int vt = tile / p.num_chunks;
+        const int pc = tile - vt * p.num_chunks;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&empty[s], ph ^ 1u)) {
+            report_timeout(p.err);
+            ok = false;
+            break;
+          }
+          uint8_t* a_dst = smem + static_cast<size_t>(s) * stage_bytes;
+          mbar_arrive_expect_tx(&full[s], stage_bytes);
+          tma_load_2d(a_dst, &tmap_w, &full[s], kb * kHeadTileK, vt * kHeadTileV, pol_w);
+          tma_load_2d(a_dst + kABytes, &tmap_h, &full[s], kb * kHeadTileK, pc * N, pol_h);
+          ++issued;
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      griddep_launch_dependents();
+      // the last copies land before the CTA may exit
+      const long long tail = issued < S ? issued : S;
+      for (long long i = 0; i < tail; ++i) {
+        if (--s < 0) {
+          s = S - 1;
+          ph ^= 1u;
+        }
+        if (!mbar_wait(&full[s], ph)) {
+          report_timeout(p.err);
+          break;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kHeadTileV, static_cast<uint32_t>(N));
+      int s = 0;
+      uint32_t ph = 0;
+      int slot = 0;
+      uint32_t sph = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int gpos = 0;  // position in the current group (a counter: no division in this thread)
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!mbar_wait(&full[s], ph)) {
+            report_timeout(p.err);
+            ok = false;
+            break;
+          }
+          const bool group_first = gpos == 0;
+          const bool group_last = gpos == kLargeGroup - 1 || kb + 1 == p.num_kb;
+          gpos = group_last ? 0 : gpos + 1;
+          if (group_first && !mbar_wait(&afree[slot], sph ^ 1u)) {
+            report_timeout(p.err);
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(slot * N);
+          const uint32_t a_addr = smem_u32(smem + static_cast<size_t>(s) * stage_bytes);
+          const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+          for (int k = 0; k < kHeadTileK / 16; ++k)
+            mma_bf16_ss(d_tmem, smem_desc_k_sw128(a_addr + k * 32), smem_desc_k_sw128(b_addr + k * 32), idesc,
+                        (group_first && k == 0) ? 0u : 1u);
+          mma_commit(&empty[s]);
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+          if (group_last) {
+            mma_commit(&afull[slot]);
+            slot ^= 1;
+            if (slot == 0) sph ^= 1u;
+          }
+        }
+      }
+      // every MMA issued by this thread has retired once this arrives
+      mma_commit(mma_done);
+      if (!mbar_wait(mma_done, 0)) report_timeout(p.err);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..9)
+    const int q = warp & 3;               // TMEM lane quadrant this warp may read
+    const int half = (warp - 2) >> 2;     // which half of the tile's columns
+    const int et = threadIdx.x - 64;      // 0..255 among the epilogue threads
+    const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(half * NH);
+    float* red_val = scr;
+    int* red_idx = reinterpret_cast<int*>(scr + 1024);
+    float* tb = scr + 2048 + (warp - 2) * (32 * kLargePitch);
+    // with programmatic launch this grid may start while the kernel before it
+    // still runs: the first write (logits, partials, the error word) waits
+    bool waited = false;
+    auto wait_prev = [&]() {
+      if (waited) return;
+      griddep_wait();
+      waited = true;
+      if (blockIdx.x == 0) {
+        if (p.zero_err && et == 0) *p.err = 0;
+        for (int i = et; i < p.n_tickets; i += 256) p.tickets[i] = 0u;
+      }
+    };
+    const int groups = (p.num_kb + kLargeGroup - 1) / kLargeGroup;
+    int slot = 0;
+    uint32_t sph = 0, rph = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      const int vt = tile / p.num_chunks;
+      const int pc = tile - vt * p.num_chunks;
+      const int v = vt * kHeadTileV + q * 32 + lane;
+      const int m0 = pc * N;
+      const int c0 = half * NH;  // this thread's first column of the tile
+      float acc[kLargeHalfMax];
+#pragma unroll
+      for (int i = 0; i < kLargeHalfMax; ++i) acc[i] = 0.f;
+      for (int g = 0; g < groups; ++g) {
+        if (!mbar_wait(&afull[slot], sph)) {
+          report_timeout(p.err);
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t t_slot = t_lane + static_cast<uint32_t>(slot * N);
+        // 16 columns per load: 128 sums and 16 loaded values stay within the
+        // 168 registers a thread of a 320-thread block may hold
+#pragma unroll
+        for (int j = 0; j < kLargeHalfMax; j += 16) {
+          if (j < NH) {
+            float val[16];
+            tmem_load_16(t_slot + j, val);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[j + i] += val[i];
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&afree[slot]);
+        slot ^= 1;
+        if (slot == 0) sph ^= 1u;
+      }
+      if (!ok) break;
+      wait_prev();
+      if constexpr (kMode == kModeLogits) {
+        if (v < p.V) {
+#pragma unroll
+          for (int i = 0; i < kLargeHalfMax; ++i) {
+            const int m = m0 + c0 + i;
+            if (i < NH && m < p.M) p.logits[static_cast<size_t>(m) * p.ldz + v] = acc[i];
+          }
+        }
+      } else {
+        if (!mbar_wait(red_free, rph ^ 1u)) {  // the previous tile's scratch consumed
+          report_timeout(p.err);
+          break;
+        }
+#pragma unroll
+        for (int j = 0; j < kLargeHalfMax; j += 16) {
+          if (j < NH) {
+            float v16[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v16[i] = acc[j + i];
+            argmax_large16(p, v16, c0 + j, v, q, lane, tb, red_val, red_idx);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(red_full);
+        if (!mbar_wait(red_full, rph)) {
+          report_timeout(p.err);
+          break;
+        }
+        argmax_merge_large(p, N, vt, m0, et, red_val, red_idx);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(red_free);
+        rph ^= 1u;
+      }
+    }
+    wait_prev();  // (a CTA that finished no tile still clears the error word)
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
+}
+
+template <int kMode>
+cudaError_t launch_large(const CUtensorMap& map_w, const CUtensorMap& map_h, const HeadParams& p, const HeadPlan& h,
+                         const DeviceInfo& dev, cudaStream_t stream) {
+  static bool attr_done[64] = {false};
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev.device]) {
+    const cudaError_t e = cudaFuncSetAttribute(head_large_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               dev.max_smem_optin);
+    if (e != cudaSuccess) return e;
+    attr_done[dev.device] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(h.grid);
+  cfg.blockDim = dim3(kLargeThreads);
+  cfg.dynamicSmemBytes = h.smem_bytes;
+  cfg.stream = stream;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, head_large_kernel<kMode>, map_w, map_h, p);
+}
+
 // A 64-bit value unique to each launch in this process (the stream-K flags
 // compare against it, so a workspace needs no clearing between calls).
 unsigned long long next_epoch() {
@@ -1018,7 +1366,7 @@ cudaError_t launch_variant(const CUtensorMap& map_w, const CUtensorMap& map_h, c
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = (h.precise && !h.wide) ? 1 : 0;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, head_kernel<kPrecN, kMode>, map_w, map_h, p);
 }
 
@@ -1046,22 +1394,15 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
     uint32_t cols = 32;
     while (cols < static_cast<uint32_t>(kSlotsPrecise * h.N)) cols <<= 1;
     h.tmem_cols = cols;
-  } else if (mode != HeadOut::kArgmax) {
-    // Sampling needs logits close to the exact ones: an accumulator that
-    // spans the whole hidden dimension (8192 products at d = 8192) moves
-    // ~0.24 % of inverse-CDF draws against fp64 logits, groups of 1024
-    // products summed in registers keep that far below 0.1 %.
-    h.precise = true;
-    h.wide = true;
-    h.N = kWideN;
-    h.num_chunks = (M + kWideN - 1) / kWideN;
-    h.gkb = kGroupWide;
-    h.tmem_cols = kSlotsPrecise * kWideN;
   } else {
+    // above 64 positions: chunks of at most 256 positions, as even as
+    // multiples of 32 allow, two TMEM slots of N columns (large-batch kernel)
+    h.large = true;
     const int chunks = (M + 255) / 256;
     const int per = (M + chunks - 1) / chunks;
-    h.N = std::max(16, (per + 15) / 16 * 16);
+    h.N = (per + 31) / 32 * 32;
     h.num_chunks = (M + h.N - 1) / h.N;
+    h.gkb = kLargeGroup;
     uint32_t cols = 32;
     while (cols < static_cast<uint32_t>(2 * h.N)) cols <<= 1;
     h.tmem_cols = cols;
@@ -1073,16 +1414,15 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
   // the cross-quadrant scratch is used by the greedy epilogue and by the
   // per-tile statistics of the standard scheme only
   size_t scratch = 0;
-  if (mode == HeadOut::kArgmax) scratch = h.precise ? kArgmaxSmallBytes : kArgmaxBytes;
-  if (mode == HeadOut::kStats && (!h.precise || h.wide)) scratch = kStatsBytes;
+  if (mode == HeadOut::kArgmax) scratch = h.large ? kLargeArgmaxBytes : kArgmaxSmallBytes;
   const size_t fixed = 1024 + kBarrierBytes + scratch;
   const size_t budget = static_cast<size_t>(dev.max_smem_optin);
   int stages = static_cast<int>((budget - fixed) / stage);
   stages = std::min(12, std::max(2, stages));
   h.stages = stages;
   h.smem_bytes = fixed + static_cast<size_t>(stages) * stage;
-  h.streamk = streamk && h.precise && !h.wide;
-  h.groups = h.precise ? (h.num_kb + h.gkb - 1) / h.gkb : 1;
+  h.streamk = streamk && h.precise;
+  h.groups = (h.num_kb + h.gkb - 1) / h.gkb;
   const long long units = h.streamk ? static_cast<long long>(h.num_tiles) * h.groups : h.num_tiles;
   h.grid = static_cast<int>(std::min<long long>(units, std::min(dev.sm_count, kMaxHeadGrid)));
   // one running partial per CTA and target row while a thread's share of
@@ -1145,8 +1485,13 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
     p.tickets = stats->tickets;
     p.n_tickets = stats->n_tickets;
   }
-  if (!h.precise) return launch_mode<0>(mode, map_w, map_h, p, h, dev, stream);
-  if (h.wide) return launch_mode<kWideN>(mode, map_w, map_h, p, h, dev, stream);
+  if (h.large) {
+    // the large-batch kernel writes logits or greedy partials; its callers
+    // form the softmax statistics in a streaming pass over the logits
+    if (mode == HeadOut::kLogits) return launch_large<kModeLogits>(map_w, map_h, p, h, dev, stream);
+    if (mode == HeadOut::kArgmax) return launch_large<kModeArgmax>(map_w, map_h, p, h, dev, stream);
+    return cudaErrorInvalidValue;
+  }
   if (h.N == 16) return launch_mode<16>(mode, map_w, map_h, p, h, dev, stream);
   if (h.N == 32) return launch_mode<32>(mode, map_w, map_h, p, h, dev, stream);
   if (h.N == 48) return launch_mode<48>(mode, map_w, map_h, p, h, dev, stream);

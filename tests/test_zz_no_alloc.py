@@ -68,3 +68,24 @@ def test_noalloc_refuses_requests_beyond_its_scratch():
     status = sv.library().spec_verify_from_logits_noalloc(None, None, None, None, 1.0, None, None, d, None, None)
     assert status == 8  # SPEC_ERR_SCRATCH_LIMIT, before any argument is touched
     assert "scratch" in sv.library().spec_status_string(8).decode()
+
+
+def test_noalloc_at_the_largest_request_that_fits():
+    """The largest batch whose from-logits workspace fits the fixed scratch
+    (K = 4, V = 128256, T = 0.8), twice in a row: identical to the
+    workspace entry point."""
+    K, V, T = 4, 128256, 0.8
+    lib = sv.library()
+    size = lambda b: lib.spec_verify_from_logits_workspace_bytes(sv.SpecDims(b, K, 0, V), T)
+    B = 1
+    while size(B + 1) <= sv.NOALLOC_SCRATCH_BYTES:
+        B += 1
+    for seed in (11, 12):
+        zp, zq, x, u = _case(B, K, V, T, seed)
+        ref_tok, ref_n, _ = _outputs(B, K)
+        sv.spec_verify_from_logits(zp, zq, x, u, T, out_tokens=ref_tok, out_num_accepted=ref_n)
+        tok, n, _ = _outputs(B, K)
+        sv.spec_verify_from_logits_noalloc(zp, zq, x, u, T, out_tokens=tok, out_num_accepted=n)
+        torch.cuda.synchronize()
+        assert torch.equal(tok, ref_tok) and torch.equal(n, ref_n), (B, seed)
+        assert sv.noalloc_read_error() == 0
