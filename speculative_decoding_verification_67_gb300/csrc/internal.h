@@ -63,9 +63,7 @@ struct HeadPlan {
   uint32_t tmem_cols = 0;
   size_t smem_bytes = 0;
   int grid = 0;
-  // target-row partials: one per CTA (num_chunks == 1) or one per tile
-  bool per_cta_partials = false;
-  int target_parts = 0;  // partials per target row
+  int target_parts = 0;  // target-row partials per row (one per CTA, small-batch statistics)
   // stream-K schedule (precise scheme with a fixup buffer): every CTA takes an
   // equal contiguous range of the num_tiles * groups (tile, 4-block group) units
   bool streamk = false;

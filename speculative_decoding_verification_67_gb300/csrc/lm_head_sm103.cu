@@ -18,29 +18,22 @@
 //    same W rows run together and share them through L2;
 //  * warp roles: warp 0 issues TMA loads (W tile 128x64 with an evict-first
 //    L2 hint, hidden tile Nx64 with evict-last), warp 1 allocates TMEM and
-//    issues tcgen05.mma from one thread, warps 2-5 drain TMEM (tcgen05.ld)
-//    and write the f32 logits, per-tile (max, lowest argmax) partials for
-//    the greedy path, or the logits plus the softmax(z/T) normaliser
-//    partials of every target row for the sampling path (the epilogue holds
-//    each logit in a register already, so the statistics cost no extra
-//    pass over the logits); in that mode, in the small-batch scheme, warps 6-7
-//    reduce the draft logits to the same partials meanwhile, hidden under the
-//    weight stream (beside the large-batch scheme's tensor-bound MMAs that
-//    work slowed them, so the caller passes no draft rows there);
-//  * three accumulation schemes.  Precise (N <= 64, the small-batch
-//    regime): every four 64-wide hidden blocks are accumulated into a fresh
-//    TMEM slot (4 slots rotate) and the epilogue adds the slot results in
-//    f32 registers with round-to-nearest, so the tensor core's own
-//    accumulation only ever spans 256 products; this cuts the logits' error
-//    against exact arithmetic several-fold at no cost to the weight stream.
-//    Wide precise (above 64 positions, logits and statistics): the same with
-//    128-position chunks and slots of 16 hidden blocks (1024 products), the
-//    sums emitted through the large-batch scheme's epilogue blocks; an
-//    accumulator over the whole hidden size would move ~0.24 % of the
-//    sampling step's inverse-CDF draws at d = 8192, this keeps it ~0.01 %.
-//    Standard (greedy above 64 positions, any N <= 256): one TMEM
-//    accumulator per tile over the whole hidden size, double-buffered so the
-//    epilogue of a tile overlaps the next tile's MMAs;
+//    issues tcgen05.mma from one thread, the epilogue warps drain TMEM
+//    (tcgen05.ld) and write the f32 logits, per-tile (max, lowest argmax)
+//    partials for the greedy path, or -- up to 64 positions -- the logits
+//    plus the softmax(z/T) normaliser partials of every target row (the
+//    epilogue holds each logit in a register already, so the statistics
+//    cost no extra pass over the logits), while warps 6-7 reduce the draft
+//    logits to the same partials, hidden under the weight stream;
+//  * precise accumulation everywhere: the tensor core never accumulates
+//    over the whole hidden size.  Up to 64 positions (head_kernel) every
+//    four 64-wide hidden blocks go into a fresh TMEM slot (4 slots rotate)
+//    and the epilogue adds the slot results in f32 registers, so the tensor
+//    core's own accumulation spans 256 products; above 64 positions
+//    (head_large_kernel, further down) groups of 16 blocks (1024 products)
+//    alternate between two slots.  An accumulator over the whole hidden size
+//    moved ~0.24 % of the sampling step's inverse-CDF draws at d = 8192
+//    against fp64 logits; 1024-product groups keep that ~0.01 %;
 //  * every wait is bounded; a timeout sets the error word, drains the copies
 //    in flight and frees TMEM before returning.
 #include <cudaTypedefs.h>
@@ -60,16 +53,9 @@ namespace {
 constexpr int kThreads = 256;  // 8 warps: producer, MMA, 4 epilogue, 2 draft statistics
 constexpr uint32_t kABytes = kHeadTileV * kHeadTileK * 2;  // 16 KB W tile per stage
 constexpr uint32_t kBarrierBytes = 512;
-constexpr int kRunChunks = 5;                              // position chunks whose partials a CTA keeps running
-constexpr int kStatPitch = 20;                             // floats per row of a warp's 32x16 transpose block
-constexpr uint32_t kStatsBytes = (3 * 4 * 256 + 4 * 32 * kStatPitch) * 4;  // k, sum hi, sum lo [4][256] + blocks
-constexpr int kArgPitch = 36;                              // floats per row of a warp's 32x32 transpose block
 constexpr uint32_t kArgmaxSmallBytes = 2 * 4 * 256 * 4;    // greedy scratch: [4 warps][256] values and indices
-constexpr uint32_t kArgmaxBytes = kArgmaxSmallBytes + 4 * 32 * kArgPitch * 4;  // + the 4 transpose blocks
 constexpr int kSlotsPrecise = 4;
 constexpr int kGroupPrecise = 4;  // hidden blocks accumulated per TMEM slot (precise scheme)
-constexpr int kWideN = 128;       // positions per chunk of the wide precise scheme
-constexpr int kGroupWide = 16;    // hidden blocks per TMEM slot there (slot span 1024 products)
 
 constexpr int kModeLogits = static_cast<int>(HeadOut::kLogits);
 constexpr int kModeArgmax = static_cast<int>(HeadOut::kArgmax);
@@ -93,8 +79,7 @@ struct HeadParams {
   // sampling statistics
   float c_hi, c_lo;
   StatPart* tpart;
-  int tparts;          // partials per target row
-  int per_cta;         // one partial per CTA (else one per tile)
+  int tparts;          // partials per target row (one per CTA)
   const float* zq;
   int draft_rows;
   StatPart* dpart;
@@ -182,47 +167,6 @@ __device__ __forceinline__ void argmax_redux(const HeadParams& p, const float* v
   }
 }
 
-// The same partials for the large-batch scheme, where the epilogue of a
-// 128 x 256 tile must keep pace with its MMAs: the warp's 32 rows x kCols
-// block goes through a per-warp transpose in shared memory (each lane stores
-// its row with 128-bit stores; a pitch of 36 floats keeps every quarter-warp
-// phase and every column read conflict-free), then lane c scans column c0 + c
-// row by row, keeping the first (lowest-id) row of the largest finite value.
-// A few plain instructions per value instead of a chain of warp collectives
-// per column (measured ~49 issued instructions a column with those).
-template <int kCols>
-__device__ __forceinline__ void argmax_transpose(const HeadParams& p, const float* val, int c0, int v, int q,
-                                                 int lane, float* scr) {
-  float* red_val = scr;
-  int* red_idx = reinterpret_cast<int*>(scr + 1024);
-  float* tb = scr + 2048 + q * (32 * kArgPitch);
-  __syncwarp();  // every lane's reads of the previous block are done
-#pragma unroll
-  for (int j = 0; j < kCols; j += 4)
-    *reinterpret_cast<float4*>(tb + lane * kArgPitch + j) = make_float4(val[j], val[j + 1], val[j + 2], val[j + 3]);
-  __syncwarp();
-  const int v0 = v - lane;                // the warp's first row
-  const int rows = min(32, p.V - v0);     // of which inside the vocabulary (may be <= 0)
-  if (lane < kCols) {
-    float best = -INFINITY;
-    int br = -1;
-    bool bad = false;
-#pragma unroll 8
-    for (int r = 0; r < 32; ++r) {
-      const float x = tb[r * kArgPitch + lane];
-      const bool use = r < rows;
-      const bool fin = isfinite(x);
-      bad |= use && !fin;
-      if (use && fin && x > best) {
-        best = x;
-        br = r;
-      }
-    }
-    red_val[q * 256 + c0 + lane] = best;
-    red_idx[q * 256 + c0 + lane] = bad ? -2 : (br < 0 ? 0x7fffffff : v0 + br);
-  }
-}
-
 // Output of 16 columns [c0, c0+16) of this thread's vocabulary row v: the
 // logits, or the greedy partials of the small-batch scheme.  Scratch layout
 // (per lane quadrant q and column): argmax uses [0] value, [1] index;
@@ -242,56 +186,6 @@ __device__ __forceinline__ void emit16(const HeadParams& p, const float (&val)[1
   if (kMode == kModeArgmax) argmax_redux<16>(p, val, c0, v, q, lane, scr);
 }
 
-// Softmax partials of the 16 columns [c0, c0 + 16) over the warp's 32 rows
-// (large-batch scheme): the warp's 32 x 16 block goes through a per-warp
-// transpose in shared memory (128-bit stores, pitch kStatPitch); lane
-// (c, h) = (lane & 15, lane >> 4) takes column c0 + c over rows 16h .. 16h+15,
-// the two halves exchange their largest exponent so that both use the same
-// integer reference k = ceil(max z c), and their compensated sums meet in one
-// shuffle.  Written to the scratch as [q][col] k, sum hi, sum lo (NaN sum hi
-// for a column with a non-finite value).
-__device__ __forceinline__ void stats_transpose16(const HeadParams& p, const float* val, int c0, int v, int q,
-                                                  int lane, float* scr) {
-  float* tb = scr + 3072 + q * (32 * kStatPitch);
-  __syncwarp();  // every lane's reads of the previous block are done
-#pragma unroll
-  for (int j = 0; j < 16; j += 4)
-    *reinterpret_cast<float4*>(tb + lane * kStatPitch + j) = make_float4(val[j], val[j + 1], val[j + 2], val[j + 3]);
-  __syncwarp();
-  const Expo ce{p.c_hi, p.c_lo};
-  const int c = lane & 15, h = lane >> 4;
-  const int rows = min(32, p.V - (v - lane)) - 16 * h;  // of this lane's 16 rows, inside the vocabulary
-  float z[16], e[16];
-  float hm = -INFINITY;
-  bool bad = false;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    z[i] = tb[(16 * h + i) * kStatPitch + c];
-    e[i] = expo_hi(z[i], ce);
-    const bool use = i < rows;
-    const bool fin = isfinite(e[i]);
-    bad |= use && !fin;
-    if (!(use && fin)) e[i] = -INFINITY;
-    hm = fmaxf(hm, e[i]);
-  }
-  hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 16));
-  bad = (__shfl_xor_sync(0xffffffffu, bad ? 1 : 0, 16) != 0) || bad;
-  const float k = hm == -INFINITY ? -INFINITY : ceilf(hm);
-  float sh = 0.f, sl = 0.f;
-  if (k != -INFINITY) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if (e[i] != -INFINITY) ff_accumulate(sh, sl, exp2f((e[i] - k) + expo_lo(z[i], e[i], ce)));
-  }
-  ff sum = ff_norm(sh, sl);
-  sum = ff_add(sum, shfl_xor_ff(sum, 16));
-  if (h == 0) {
-    scr[q * 256 + c0 + c] = k;
-    scr[1024 + q * 256 + c0 + c] = bad ? __int_as_float(0x7fc00000) : sum.hi;
-    scr[2048 + q * 256 + c0 + c] = sum.lo;
-  }
-}
-
 __device__ __forceinline__ void store_part(StatPart* dst, const Partial& a) {
   StatPart sp;
   sp.k = a.k;
@@ -299,32 +193,6 @@ __device__ __forceinline__ void store_part(StatPart* dst, const Partial& a) {
   sp.s_lo = a.s.lo;
   sp.bad = a.bad;
   *dst = sp;
-}
-
-// Softmax partials of one tile's columns: merge the four lane quadrants;
-// fold into the CTA's running partials (one per CTA) or store per tile.
-__device__ __forceinline__ void stats_finish(const HeadParams& p, int N, int vt, int m0, int et, const float* scr,
-                                             Partial (&run)[2 * kRunChunks]) {
-  const int pc = m0 / N;  // the tile's position chunk
-  int r = 0;
-  for (int c = et; c < N; c += 128, ++r) {
-    const int m = m0 + c;
-    if (m >= p.M) continue;
-    Partial acc = partial_empty();
-#pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-      Partial pq;
-      pq.k = scr[qq * 256 + c];
-      pq.s = {scr[1024 + qq * 256 + c], scr[2048 + qq * 256 + c]};
-      pq.bad = isnan(pq.s.hi) ? 1 : 0;
-      if (pq.bad) pq.s = {0.f, 0.f};
-      acc = partial_merge(acc, pq);
-    }
-    if (p.per_cta)
-      run[pc * 2 + r] = partial_merge(run[pc * 2 + r], acc);
-    else
-      store_part(&p.tpart[static_cast<size_t>(m) * p.tparts + vt], acc);
-  }
 }
 
 // Draft-row statistics by warps 6-7: units of (draft row, 4096-token chunk)
@@ -424,19 +292,18 @@ __device__ __forceinline__ void argmax_finish(const HeadParams& p, int N, int vt
   }
 }
 
-// kPrecN == 0: standard accumulation; kPrecN == 16, 32, 48 or 64: precise
-// accumulation with N == kPrecN.  kMode: HeadOut as int.
+// Up to 64 positions: precise accumulation with N == kPrecN (16, 32, 48 or
+// 64) positions per tile.  kMode: HeadOut as int.
 template <int kPrecN, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     head_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_h,
                 const HeadParams p) {
-  constexpr bool kPrecise = kPrecN > 0;
-  constexpr int kSlots = kPrecise ? kSlotsPrecise : 2;
+  constexpr int kSlots = kSlotsPrecise;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
-  const int N = kPrecise ? kPrecN : p.N;
+  const int N = kPrecN;
   const uint32_t b_bytes = static_cast<uint32_t>(N) * 128u;
   const uint32_t stage_bytes = kABytes + b_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
@@ -494,8 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && work_next(p, wc, tile, g0, g1)) {
         const int vt = tile / p.num_chunks;
         const int pc = tile - vt * p.num_chunks;
-        const int kb0 = kPrecise ? g0 * p.gkb : 0;
-        const int kb1 = kPrecise ? min(g1 * p.gkb, p.num_kb) : p.num_kb;
+        const int kb0 = g0 * p.gkb;
+        const int kb1 = min(g1 * p.gkb, p.num_kb);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u)) {
             report_timeout(p.err);
@@ -541,15 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       WorkCursor wc = work_begin(p);
       int tile, g0, g1;
       while (ok && work_next(p, wc, tile, g0, g1)) {
-        if (!kPrecise) {
-          if (!mbar_wait(&afree[slot], sph ^ 1u)) {
-            report_timeout(p.err);
-            break;
-          }
-          tc_fence_after_sync();
-        }
-        const int kb0 = kPrecise ? g0 * p.gkb : 0;
-        const int kb1 = kPrecise ? min(g1 * p.gkb, p.num_kb) : p.num_kb;
+        const int kb0 = g0 * p.gkb;
+        const int kb1 = min(g1 * p.gkb, p.num_kb);
         // position in the current slot group (kb0 starts one); a counter, not
         // kb % gkb: an integer division per hidden block in this one issuing
         // thread held the tensor pipe back (wide scheme at 128 positions: 275
@@ -561,10 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          const bool group_first = !kPrecise || gpos == 0;
-          const bool group_last = kPrecise && (gpos == p.gkb - 1 || kb + 1 == p.num_kb);
+          const bool group_first = gpos == 0;
+          const bool group_last = gpos == p.gkb - 1 || kb + 1 == p.num_kb;
           gpos = group_last ? 0 : gpos + 1;
-          if (kPrecise && group_first) {
+          if (group_first) {
             if (!mbar_wait(&afree[slot], sph ^ 1u)) {
               report_timeout(p.err);
               ok = false;
@@ -577,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
           for (int k = 0; k < kHeadTileK / 16; ++k) {
-            const bool acc = kPrecise ? !(group_first && k == 0) : ((kb | k) != 0);
+            const bool acc = !(group_first && k == 0);
             mma_bf16_ss(d_tmem, smem_desc_k_sw128(a_addr + k * 32), smem_desc_k_sw128(b_addr + k * 32), idesc,
                         acc ? 1u : 0u);
           }
@@ -595,13 +455,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        if (!kPrecise) {
-          mma_commit(&afull[slot]);
-          if (++slot == kSlots) {
-            slot = 0;
-            sph ^= 1u;
-          }
-        }
       }
       // Every MMA issued by this thread has retired once this arrives.
       mma_commit(mma_done);
@@ -628,15 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = et; i < p.n_tickets; i += 128) p.tickets[i] = 0u;
       }
     };
-    // precise statistics keep per-thread running partials instead of
-    // reducing every tile across the quadrants
-    constexpr bool kWide = kPrecN > 64;  // wide precise scheme: the large-batch emit from registers
-    constexpr bool run_stats = kPrecise && !kWide && kMode == kModeStats;
-    constexpr bool reduce = kMode != kModeLogits && !run_stats;  // cross-quadrant scratch per tile
+    // statistics keep per-thread running partials (one per column), merged
+    // across the CTA's threads once at the end; greedy partials are reduced
+    // across the quadrants per tile through the scratch
+    constexpr bool run_stats = kMode == kModeStats;
+    constexpr bool reduce = kMode == kModeArgmax;
     constexpr int kRun = run_stats ? kPrecN : 1;
-    Partial run[2 * kRunChunks];  // [chunk][column / 128]: running partials of the standard scheme
-#pragma unroll
-    for (int i = 0; i < 2 * kRunChunks; ++i) run[i] = partial_empty();
     float rk[kRun], rs[kRun];
 #pragma unroll
     for (int i = 0; i < kRun; ++i) {
@@ -657,12 +507,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         report_timeout(p.err);
         break;
       }
-      if constexpr (kPrecise) {
+      {
         float acc[kPrecN];
 #pragma unroll
         for (int i = 0; i < kPrecN; ++i) acc[i] = 0.f;
-        if (!kWide && g0 == 0 && g1 < p.groups) {
-          // (stream-K, small precise scheme only)
+        if (g0 == 0 && g1 < p.groups) {
+          // (stream-K)
           // The first part of a tile whose other groups belong to the next
           // CTA(s), each of which stored them before anything else: start
           // from their sums (the loads' latency then hides behind this tile's
@@ -728,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!ok) break;
-        if (!kWide && g0 > 0) {
+        if (g0 > 0) {
           // a later part of a tile: hand this quadrant's sums to the CTA that
           // owns the tile's first group, and emit nothing
           float* f = p.fix + static_cast<size_t>(blockIdx.x) * kFixupFloatsPerCta + et;
@@ -771,31 +621,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               rs[i] += in ? t : 0.f;
             }
           }
-        } else if constexpr (kWide) {
-          // the large-batch scheme's emit, 32 columns at a time from the sums
-#pragma unroll
-          for (int c0 = 0; c0 < kPrecN; c0 += 32) {
-            if (m0 + c0 >= p.M) break;
-            if constexpr (kMode == kModeArgmax) {
-              float v32[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v32[i] = acc[c0 + i];
-              argmax_transpose<32>(p, v32, c0, v, q, lane, scr);
-            } else {
-              float lo[16], hi[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                lo[i] = acc[c0 + i];
-                hi[i] = acc[c0 + 16 + i];
-              }
-              emit16<kModeLogits>(p, lo, c0, m0, v, q, lane, scr);
-              emit16<kModeLogits>(p, hi, c0 + 16, m0, v, q, lane, scr);
-              if constexpr (kMode == kModeStats) {
-                stats_transpose16(p, lo, c0, v, q, lane, scr);
-                stats_transpose16(p, hi, c0 + 16, v, q, lane, scr);
-              }
-            }
-          }
         } else {
 #pragma unroll
           for (int c0 = 0; c0 < kPrecN; c0 += 16) {
@@ -805,53 +630,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             emit16<kMode>(p, val, c0, m0, v, q, lane, scr);
           }
         }
-      } else {
-        if (!mbar_wait(&afull[slot], sph)) {
-          report_timeout(p.err);
-          break;
-        }
-        tc_fence_after_sync();
-        wait_prev();
-        const uint32_t t_row = t_lane + static_cast<uint32_t>(slot * N);
-        // 32 columns per TMEM load (one wait for two emits), 16 for the tail
-        int c0 = 0;
-        for (; c0 + 32 <= N; c0 += 32) {
-          float v32[32];
-          tmem_load_32(t_row + c0, v32);
-          if constexpr (kMode == kModeArgmax) {
-            argmax_transpose<32>(p, v32, c0, v, q, lane, scr);
-          } else {
-            float lo[16], hi[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              lo[i] = v32[i];
-              hi[i] = v32[16 + i];
-            }
-            emit16<kModeLogits>(p, lo, c0, m0, v, q, lane, scr);
-            emit16<kModeLogits>(p, hi, c0 + 16, m0, v, q, lane, scr);
-            if constexpr (kMode == kModeStats) {
-              stats_transpose16(p, lo, c0, v, q, lane, scr);
-              stats_transpose16(p, hi, c0 + 16, v, q, lane, scr);
-            }
-          }
-        }
-        if (c0 < N) {
-          float val[16];
-          tmem_load_16(t_row + c0, val);
-          if constexpr (kMode == kModeArgmax) {
-            argmax_transpose<16>(p, val, c0, v, q, lane, scr);
-          } else {
-            emit16<kModeLogits>(p, val, c0, m0, v, q, lane, scr);
-            if constexpr (kMode == kModeStats) stats_transpose16(p, val, c0, v, q, lane, scr);
-          }
-        }
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&afree[slot]);
-        if (++slot == kSlots) {
-          slot = 0;
-          sph ^= 1u;
-        }
       }
       if (reduce) {
         __syncwarp();
@@ -860,8 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           report_timeout(p.err);
           break;
         }
-        if (kMode == kModeArgmax) argmax_finish(p, N, vt, m0, et, scr);
-        if (kMode == kModeStats) stats_finish(p, N, vt, m0, et, scr, run);
+        argmax_finish(p, N, vt, m0, et, scr);
         __syncwarp();
         if (lane == 0) mbar_arrive(red_free);
         rph ^= 1u;
@@ -931,14 +708,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc.bad = !isfinite(sum.hi) || kmax == INFINITY;
         if (part == 0 && col < kPrecN && col < p.M)
           store_part(&p.tpart[static_cast<size_t>(col) * p.tparts + blockIdx.x], acc);
-      }
-    } else if (kMode == kModeStats && p.per_cta) {
-      for (int pc = 0; pc < p.num_chunks; ++pc) {
-        int r = 0;
-        for (int c = et; c < N; c += 128, ++r) {
-          const int m = pc * N + c;
-          if (m < p.M) store_part(&p.tpart[static_cast<size_t>(m) * p.tparts + blockIdx.x], run[pc * 2 + r]);
-        }
       }
     }
   } else if (kMode == kModeStats) {
@@ -1425,11 +1194,8 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
   h.groups = (h.num_kb + h.gkb - 1) / h.gkb;
   const long long units = h.streamk ? static_cast<long long>(h.num_tiles) * h.groups : h.num_tiles;
   h.grid = static_cast<int>(std::min<long long>(units, std::min(dev.sm_count, kMaxHeadGrid)));
-  // one running partial per CTA and target row while a thread's share of
-  // the columns fits in registers (up to kRunChunks position chunks), else
-  // one per vocabulary tile
-  h.per_cta_partials = h.num_chunks <= kRunChunks;
-  h.target_parts = h.per_cta_partials ? h.grid : h.num_vt;
+  // the small-batch statistics: one running partial per CTA and target row
+  h.target_parts = h.grid;
   return h;
 }
 
@@ -1477,7 +1243,6 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
     p.c_lo = stats->c_lo;
     p.tpart = stats->tpart;
     p.tparts = h.target_parts;
-    p.per_cta = h.per_cta_partials ? 1 : 0;
     p.zq = stats->zq;
     p.draft_rows = stats->draft_rows;
     p.dpart = stats->dpart;
