@@ -77,17 +77,75 @@ def step_bytes(w) -> dict:
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    """SM clock and throttle reasons while the benchmark runs.
+
+    NVML (the driver's management library, loaded with ctypes) is polled from
+    a thread every ~0.25 ms between start() and stop(); the device is matched
+    to the CUDA device by UUID.  The reported figures are those of the samples
+    taken inside the timed region (begin_timed() .. end_timed()), which even a
+    few-millisecond region fills, with the whole window beside them.  Without
+    NVML it falls back to ``nvidia-smi -lms 100`` over the whole window."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # nvmlClocksEventReasons bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, gpu_index: int):
-        self.proc = None
         self.gpu = gpu_index
+        self.proc = None
+        self.lib = None
+        self.samples = []
+        self.t_begin = self.t_end = None
+        self.max_mhz = None
+        self.matched = None
+
+    def _open_nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        try:
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(self.gpu).uuid)
+        except Exception:
+            uuid = None
+        if uuid and lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) == 0:
+            self.matched = "uuid"
+        elif lib.nvmlDeviceGetHandleByIndex_v2(self.gpu, ctypes.byref(h)) == 0:
+            self.matched = "index"
+        else:
+            raise RuntimeError("no NVML handle")
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h
+
+    def _poll(self):
+        import ctypes
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_flag.is_set():
+            ok = self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0
+            ok = ok and self.reasons_fn(self.h, ctypes.byref(rs)) == 0
+            if ok:
+                self.samples.append((time.perf_counter(), float(clk.value), int(rs.value)))
+            time.sleep(0.00025)
 
     def start(self):
+        import threading
+        try:
+            self.lib, self.h = self._open_nvml()
+        except Exception:
+            self.lib = None
+        if self.lib is not None:
+            self.stop_flag = threading.Event()
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -95,7 +153,31 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
+    def begin_timed(self):
+        self.t_begin = time.perf_counter()
+
+    def end_timed(self):
+        self.t_end = time.perf_counter()
+
+    def _summary(self, samples):
+        if not samples:
+            return {"sm_mhz": None, "samples": 0, "reasons": []}
+        names = sorted({nm for _, _, r in samples for bit, nm in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(c for _, c, _ in samples), "sm_min_mhz": min(c for _, c, _ in samples),
+                "samples": len(samples), "reasons": names}
+
     def stop(self) -> dict:
+        if self.lib is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=5)
+            t0 = self.t_begin if self.t_begin is not None else float("-inf")
+            t1 = self.t_end if self.t_end is not None else float("inf")
+            timed = [x for x in self.samples if t0 <= x[0] <= t1]
+            out = self._summary(timed)
+            out.update({"sm_max_mhz": self.max_mhz, "source": f"NVML every ~0.25 ms inside the timed region "
+                                                             f"(device matched by {self.matched})",
+                        "whole_run": self._summary(self.samples)})
+            return out
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
@@ -119,7 +201,7 @@ class ClockSampler:
                 if val.lower().startswith("active"):
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "reasons": sorted(reasons), "source": "nvidia-smi -lms 100 over the whole run"}
 
 
 def dist_setup(n_gpus: int, backend: str = "nccl"):
@@ -349,7 +431,9 @@ def run_kv_commit(args):
     # each launch timed alone between events; the lengths are reset and L2 is
     # flushed between launches, outside the event pairs (a decode step reaches
     # the commit with L2 full of the LM head's clean weight lines)
+    clocks.begin_timed()
     launch_ms = time_launches(commit, args.steps, stream, before=lambda: inp["seq_len"].copy_(seq0), flush=flush)
+    clocks.end_timed()
     barrier(world)
     clk = clocks.stop()
     mean_ms = max_over_ranks(statistics.mean(launch_ms), world)
@@ -471,7 +555,9 @@ def run_ngram(args):
         call()
     torch.cuda.synchronize()
     barrier(world)
+    clocks.begin_timed()
     launch_ms = time_launches(call, args.steps, stream, flush=flush)
+    clocks.end_timed()
     barrier(world)
     clk = clocks.stop()
     mean_ms = max_over_ranks(statistics.mean(launch_ms), world)
@@ -581,11 +667,13 @@ def run_draft(args):
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.begin_timed()
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    clocks.end_timed()
     barrier(world)
     clk = clocks.stop()
     value, ms = job_throughput(e0.elapsed_time(e1), world, B, args.steps)
@@ -702,11 +790,13 @@ def run_tree(args):
     torch.cuda.synchronize()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.begin_timed()
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    clocks.end_timed()
     barrier(world)
     clk = clocks.stop()
     value, ms = job_throughput(e0.elapsed_time(e1), world, M, args.steps)
@@ -859,11 +949,13 @@ def main():
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.begin_timed()
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    clocks.end_timed()
     barrier(world)
     ms = e0.elapsed_time(e1)
     clk = clocks.stop()

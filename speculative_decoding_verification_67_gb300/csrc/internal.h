@@ -72,6 +72,8 @@ struct HeadPlan {
   // chunks of N <= 256 positions, two N-column TMEM slots of gkb hidden
   // blocks each, summed in registers by eight epilogue warps
   bool large = false;
+  // ... on CTA pairs (tcgen05 cta_group::2, 256-row vocabulary tiles)
+  bool pair = false;
   int gkb = 4;           // hidden blocks accumulated per TMEM slot (precise schemes)
 };
 

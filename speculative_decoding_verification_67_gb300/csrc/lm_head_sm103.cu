@@ -780,6 +780,7 @@ __device__ __forceinline__ void argmax_large16(const HeadParams& p, const float 
 // lower quadrant holds the lower token ids, so equal values keep the lower).
 __device__ __forceinline__ void argmax_merge_large(const HeadParams& p, int N, int vt, int m0, int et,
                                                    const float* red_val, const int* red_idx) {
+  if (vt >= p.num_vt) return;  // the peer half of a pair's last tile lies past V
   for (int c = et; c < N; c += 256) {
     const int m = m0 + c;
     if (m >= p.M) continue;
@@ -802,7 +803,14 @@ __device__ __forceinline__ void argmax_merge_large(const HeadParams& p, int N, i
 }
 
 // kMode: kModeLogits (f32 logits) or kModeArgmax (per-tile greedy partials).
-template <int kMode>
+// kPair: the MMAs run over a CTA pair (a cluster of two on neighbouring SMs,
+// tcgen05 cta_group::2): a tile is 256 vocabulary rows, each CTA loads its
+// 128 rows of W and half of the chunk's hidden rows, the leader (even rank)
+// issues M = 256 MMAs that read both CTAs' shared memory and write both CTAs'
+// tensor memory, and each CTA's epilogue drains its own 128 rows.  Per SM
+// that halves the hidden-state operand traffic of a product, the part of
+// shared-memory and L2 bandwidth that bounds the single-CTA MMAs.
+template <int kMode, bool kPair>
 __global__ void __launch_bounds__(kLargeThreads, 1)
     head_large_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_h,
                       const HeadParams p) {
@@ -811,13 +819,14 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int S = p.stages;
   const int N = p.N;
-  const int NH = N >> 1;  // columns per epilogue half
-  const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(N) * 128u;
+  const int NH = N >> 1;                 // columns per epilogue half
+  const int NB = kPair ? NH : N;         // hidden rows of this CTA's B tile
+  const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(NB) * 128u;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
-  uint64_t* full = bars;              // [S] TMA landed
+  uint64_t* full = bars;              // [S] TMA landed (pair: both CTAs' bytes, on the leader)
   uint64_t* empty = bars + S;         // [S] MMAs reading the stage are done
   uint64_t* afull = bars + 2 * S;     // [2] slot holds a finished group
-  uint64_t* afree = afull + 2;        // [2] slot drained by the 8 epilogue warps
+  uint64_t* afree = afull + 2;        // [2] slot drained by the epilogue warps (pair: of both CTAs, on the leader)
   uint64_t* mma_done = afree + 2;     // [1] teardown
   uint64_t* red_full = mma_done + 1;  // [1] greedy scratch written by the 8 epilogue warps
   uint64_t* red_free = red_full + 1;  // [1] greedy scratch consumed
@@ -826,6 +835,10 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;  // 0: the pair's leader
+  const int unit0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int units = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  constexpr int kRowsPerTile = kPair ? 2 * kHeadTileV : kHeadTileV;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -834,7 +847,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&afull[i], 1);
-      mbar_init(&afree[i], 8);
+      mbar_init(&afree[i], kPair ? 16 : 8);
     }
     mbar_init(mma_done, 1);
     mbar_init(red_full, 8);
@@ -846,11 +859,19 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     prefetch_tensor_map(&tmap_h);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, p.tmem_cols);
-    tmem_relinquish_alloc_permit();
+    if constexpr (kPair) {
+      tmem_alloc_pair(tmem_holder, p.tmem_cols);
+      tmem_relinquish_alloc_permit_pair();
+    } else {
+      tmem_alloc(tmem_holder, p.tmem_cols);
+      tmem_relinquish_alloc_permit();
+    }
   }
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (kPair)
+    cluster_sync();  // both CTAs' barriers initialised and tensor memory allocated
+  else
+    __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_holder;
 
@@ -863,9 +884,11 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
       uint32_t ph = 0;
       long long issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int tile = unit0; ok && tile < p.num_tiles; tile += units) {
         const int vt = tile / p.num_chunks;
         const int pc = tile - vt * p.num_chunks;
+        const int w_row = vt * kRowsPerTile + static_cast<int>(rank) * kHeadTileV;
+        const int h_row = pc * N + static_cast<int>(rank) * NB;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(&empty[s], ph ^ 1u)) {
             report_timeout(p.err);
@@ -873,9 +896,18 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
             break;
           }
           uint8_t* a_dst = smem + static_cast<size_t>(s) * stage_bytes;
-          mbar_arrive_expect_tx(&full[s], stage_bytes);
-          tma_load_2d(a_dst, &tmap_w, &full[s], kb * kHeadTileK, vt * kHeadTileV, pol_w);
-          tma_load_2d(a_dst + kABytes, &tmap_h, &full[s], kb * kHeadTileK, pc * N, pol_h);
+          if constexpr (kPair) {
+            // both CTAs' bytes complete on the leader's barrier, which
+            // expects them all
+            if (rank == 0) mbar_arrive_expect_tx(&full[s], 2u * stage_bytes);
+            const uint32_t bar = cluster_map(&full[s], 0);
+            tma_load_2d_pair(a_dst, &tmap_w, bar, kb * kHeadTileK, w_row, pol_w);
+            tma_load_2d_pair(a_dst + kABytes, &tmap_h, bar, kb * kHeadTileK, h_row, pol_h);
+          } else {
+            mbar_arrive_expect_tx(&full[s], stage_bytes);
+            tma_load_2d(a_dst, &tmap_w, &full[s], kb * kHeadTileK, w_row, pol_w);
+            tma_load_2d(a_dst + kABytes, &tmap_h, &full[s], kb * kHeadTileK, h_row, pol_h);
+          }
           ++issued;
           if (++s == S) {
             s = 0;
@@ -884,29 +916,33 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
         }
       }
       griddep_launch_dependents();
-      // the last copies land before the CTA may exit
-      const long long tail = issued < S ? issued : S;
-      for (long long i = 0; i < tail; ++i) {
-        if (--s < 0) {
-          s = S - 1;
-          ph ^= 1u;
-        }
-        if (!mbar_wait(&full[s], ph)) {
-          report_timeout(p.err);
-          break;
+      // the last copies land before the CTA may exit (a pair's peer cannot
+      // see its bytes land: the leader waits for both CTAs' here, and the
+      // peer stays until the leader reaches the final cluster barrier)
+      if (!kPair || rank == 0) {
+        const long long tail = issued < S ? issued : S;
+        for (long long i = 0; i < tail; ++i) {
+          if (--s < 0) {
+            s = S - 1;
+            ph ^= 1u;
+          }
+          if (!mbar_wait(&full[s], ph)) {
+            report_timeout(p.err);
+            break;
+          }
         }
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kHeadTileV, static_cast<uint32_t>(N));
+    // ------------------------------------------------------------ MMA issuer (the leader's)
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kHeadTileV : kHeadTileV, static_cast<uint32_t>(N));
       int s = 0;
       uint32_t ph = 0;
       int slot = 0;
       uint32_t sph = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int tile = unit0; ok && tile < p.num_tiles; tile += units) {
         int gpos = 0;  // position in the current group (a counter: no division in this thread)
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(&full[s], ph)) {
@@ -917,7 +953,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
           const bool group_first = gpos == 0;
           const bool group_last = gpos == kLargeGroup - 1 || kb + 1 == p.num_kb;
           gpos = group_last ? 0 : gpos + 1;
-          if (group_first && !mbar_wait(&afree[slot], sph ^ 1u)) {
+          if (group_first && !(kPair ? mbar_wait_cluster(&afree[slot], sph ^ 1u) : mbar_wait(&afree[slot], sph ^ 1u))) {
             report_timeout(p.err);
             ok = false;
             break;
@@ -927,23 +963,38 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
           const uint32_t a_addr = smem_u32(smem + static_cast<size_t>(s) * stage_bytes);
           const uint32_t b_addr = a_addr + kABytes;
 #pragma unroll
-          for (int k = 0; k < kHeadTileK / 16; ++k)
-            mma_bf16_ss(d_tmem, smem_desc_k_sw128(a_addr + k * 32), smem_desc_k_sw128(b_addr + k * 32), idesc,
-                        (group_first && k == 0) ? 0u : 1u);
-          mma_commit(&empty[s]);
+          for (int k = 0; k < kHeadTileK / 16; ++k) {
+            const uint32_t accumulate = (group_first && k == 0) ? 0u : 1u;
+            if constexpr (kPair)
+              mma_bf16_ss_pair(d_tmem, smem_desc_k_sw128(a_addr + k * 32), smem_desc_k_sw128(b_addr + k * 32), idesc,
+                               accumulate);
+            else
+              mma_bf16_ss(d_tmem, smem_desc_k_sw128(a_addr + k * 32), smem_desc_k_sw128(b_addr + k * 32), idesc,
+                          accumulate);
+          }
+          if constexpr (kPair)
+            mma_commit_pair(&empty[s], 0x3);  // frees the stage in both CTAs
+          else
+            mma_commit(&empty[s]);
           if (++s == S) {
             s = 0;
             ph ^= 1u;
           }
           if (group_last) {
-            mma_commit(&afull[slot]);
+            if constexpr (kPair)
+              mma_commit_pair(&afull[slot], 0x3);  // both CTAs' epilogues
+            else
+              mma_commit(&afull[slot]);
             slot ^= 1;
             if (slot == 0) sph ^= 1u;
           }
         }
       }
       // every MMA issued by this thread has retired once this arrives
-      mma_commit(mma_done);
+      if constexpr (kPair)
+        mma_commit_pair(mma_done, 0x1);
+      else
+        mma_commit(mma_done);
       if (!mbar_wait(mma_done, 0)) report_timeout(p.err);
     }
   } else {
@@ -955,6 +1006,9 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     float* red_val = scr;
     int* red_idx = reinterpret_cast<int*>(scr + 1024);
     float* tb = scr + 2048 + (warp - 2) * (32 * kLargePitch);
+    // a drained slot is reported to the MMA issuer, in the leader CTA
+    const uint32_t afree_leader0 = kPair ? cluster_map(&afree[0], 0) : 0u;
+    const uint32_t afree_leader1 = kPair ? cluster_map(&afree[1], 0) : 0u;
     // with programmatic launch this grid may start while the kernel before it
     // still runs: the first write (logits, partials, the error word) waits
     bool waited = false;
@@ -971,9 +1025,10 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     int slot = 0;
     uint32_t sph = 0, rph = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      const int vt = tile / p.num_chunks;
-      const int pc = tile - vt * p.num_chunks;
+    for (int tile = unit0; ok && tile < p.num_tiles; tile += units) {
+      const int vt2 = tile / p.num_chunks;
+      const int pc = tile - vt2 * p.num_chunks;
+      const int vt = kPair ? 2 * vt2 + static_cast<int>(rank) : vt2;  // this CTA's 128-row vocabulary tile
       const int v = vt * kHeadTileV + q * 32 + lane;
       const int m0 = pc * N;
       const int c0 = half * NH;  // this thread's first column of the tile
@@ -981,7 +1036,7 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
 #pragma unroll
       for (int i = 0; i < kLargeHalfMax; ++i) acc[i] = 0.f;
       for (int g = 0; g < groups; ++g) {
-        if (!mbar_wait(&afull[slot], sph)) {
+        if (!(kPair ? mbar_wait_cluster(&afull[slot], sph) : mbar_wait(&afull[slot], sph))) {
           report_timeout(p.err);
           ok = false;
           break;
@@ -1001,7 +1056,12 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&afree[slot]);
+        if (lane == 0) {
+          if constexpr (kPair)
+            mbar_arrive_remote(slot == 0 ? afree_leader0 : afree_leader1);
+          else
+            mbar_arrive(&afree[slot]);
+        }
         slot ^= 1;
         if (slot == 0) sph ^= 1u;
       }
@@ -1045,19 +1105,29 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
   }
 
   tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
+  if constexpr (kPair) {
+    // every MMA of the pair has retired (the leader's MMA thread waited for
+    // them) and both epilogues are done before either CTA frees its tensor
+    // memory; neither CTA exits while the other may still reach it
+    cluster_sync();
+    tc_fence_after_sync();
+    if (warp == 1) tmem_dealloc_pair(tmem_base, p.tmem_cols);
+    cluster_sync();
+  } else {
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem_base, p.tmem_cols);
+  }
 }
 
-template <int kMode>
+template <int kMode, bool kPair>
 cudaError_t launch_large(const CUtensorMap& map_w, const CUtensorMap& map_h, const HeadParams& p, const HeadPlan& h,
                          const DeviceInfo& dev, cudaStream_t stream) {
   static bool attr_done[64] = {false};
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev.device]) {
-    const cudaError_t e = cudaFuncSetAttribute(head_large_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               dev.max_smem_optin);
+    const cudaError_t e = cudaFuncSetAttribute(head_large_kernel<kMode, kPair>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, dev.max_smem_optin);
     if (e != cudaSuccess) return e;
     attr_done[dev.device] = true;
   }
@@ -1066,8 +1136,45 @@ cudaError_t launch_large(const CUtensorMap& map_w, const CUtensorMap& map_h, con
   cfg.blockDim = dim3(kLargeThreads);
   cfg.dynamicSmemBytes = h.smem_bytes;
   cfg.stream = stream;
-  cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, head_large_kernel<kMode>, map_w, map_h, p);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = kPair ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, head_large_kernel<kMode, kPair>, map_w, map_h, p);
+}
+
+// Clusters of two large-batch CTAs that fit the device at once (0 if the
+// pair form cannot be resident), probed once per device.
+int large_pair_clusters(const DeviceInfo& dev, size_t smem_bytes) {
+  static int cached[64] = {0};
+  static size_t cached_smem[64] = {0};
+  static std::mutex mu;
+  if (dev.device < 0 || dev.device >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached_smem[dev.device] == smem_bytes) return cached[dev.device];
+  int n = 0;
+  if (cudaFuncSetAttribute(head_large_kernel<kModeLogits, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           dev.max_smem_optin) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(dev.sm_count / 2));
+    cfg.blockDim = dim3(kLargeThreads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, head_large_kernel<kModeLogits, true>, &cfg) != cudaSuccess) n = 0;
+  }
+  cudaGetLastError();  // a failed probe leaves no sticky error
+  cached[dev.device] = n;
+  cached_smem[dev.device] = smem_bytes;
+  return n;
 }
 
 // A 64-bit value unique to each launch in this process (the stream-K flags
@@ -1179,21 +1286,33 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
   h.num_vt = (V + kHeadTileV - 1) / kHeadTileV;
   h.num_tiles = h.num_vt * h.num_chunks;
   h.num_kb = (d + kHeadTileK - 1) / kHeadTileK;
-  const size_t stage = kABytes + static_cast<size_t>(h.N) * 128;
-  // the cross-quadrant scratch is used by the greedy epilogue and by the
-  // per-tile statistics of the standard scheme only
+  // the cross-quadrant scratch is used by the greedy epilogues only
   size_t scratch = 0;
   if (mode == HeadOut::kArgmax) scratch = h.large ? kLargeArgmaxBytes : kArgmaxSmallBytes;
   const size_t fixed = 1024 + kBarrierBytes + scratch;
   const size_t budget = static_cast<size_t>(dev.max_smem_optin);
-  int stages = static_cast<int>((budget - fixed) / stage);
-  stages = std::min(12, std::max(2, stages));
-  h.stages = stages;
-  h.smem_bytes = fixed + static_cast<size_t>(stages) * stage;
+  auto fit = [&](size_t stage) {
+    h.stages = std::min(12, std::max(2, static_cast<int>((budget - fixed) / stage)));
+    h.smem_bytes = fixed + static_cast<size_t>(h.stages) * stage;
+  };
+  fit(kABytes + static_cast<size_t>(h.N) * 128);
   h.streamk = streamk && h.precise;
   h.groups = (h.num_kb + h.gkb - 1) / h.gkb;
   const long long units = h.streamk ? static_cast<long long>(h.num_tiles) * h.groups : h.num_tiles;
   h.grid = static_cast<int>(std::min<long long>(units, std::min(dev.sm_count, kMaxHeadGrid)));
+  if (h.large) {
+    // CTA pairs where their clusters fit: tiles of 256 vocabulary rows, each
+    // CTA holding half of the chunk's hidden rows
+    fit(kABytes + static_cast<size_t>(h.N / 2) * 128);
+    const int clusters = large_pair_clusters(dev, h.smem_bytes);
+    if (clusters > 0) {
+      h.pair = true;
+      h.num_tiles = ((V + 2 * kHeadTileV - 1) / (2 * kHeadTileV)) * h.num_chunks;
+      h.grid = 2 * std::min(clusters, h.num_tiles);
+    } else {
+      fit(kABytes + static_cast<size_t>(h.N) * 128);
+    }
+  }
   // the small-batch statistics: one running partial per CTA and target row
   h.target_parts = h.grid;
   return h;
@@ -1208,7 +1327,7 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
   CUtensorMap map_w, map_h;
   if (!encode_bf16_rows(&map_w, W, static_cast<uint64_t>(d), static_cast<uint64_t>(V), kHeadTileV) ||
       !encode_bf16_rows(&map_h, hidden, static_cast<uint64_t>(d), static_cast<uint64_t>(M),
-                        static_cast<uint32_t>(h.N))) {
+                        static_cast<uint32_t>(h.pair ? h.N / 2 : h.N))) {
     *encode_failed = true;
     return cudaErrorInvalidValue;
   }
@@ -1253,8 +1372,12 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
   if (h.large) {
     // the large-batch kernel writes logits or greedy partials; its callers
     // form the softmax statistics in a streaming pass over the logits
-    if (mode == HeadOut::kLogits) return launch_large<kModeLogits>(map_w, map_h, p, h, dev, stream);
-    if (mode == HeadOut::kArgmax) return launch_large<kModeArgmax>(map_w, map_h, p, h, dev, stream);
+    if (mode == HeadOut::kLogits)
+      return h.pair ? launch_large<kModeLogits, true>(map_w, map_h, p, h, dev, stream)
+                    : launch_large<kModeLogits, false>(map_w, map_h, p, h, dev, stream);
+    if (mode == HeadOut::kArgmax)
+      return h.pair ? launch_large<kModeArgmax, true>(map_w, map_h, p, h, dev, stream)
+                    : launch_large<kModeArgmax, false>(map_w, map_h, p, h, dev, stream);
     return cudaErrorInvalidValue;
   }
   if (h.N == 16) return launch_mode<16>(mode, map_w, map_h, p, h, dev, stream);
