@@ -838,7 +838,8 @@ def run_tree(args):
                    "l2": f"inputs exceed L2: W_lm {2 * V * d / 1e9:.2f} GB is streamed every step"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs,
                      "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "head_kernel + tree_sample_kernel (the whole step, both launches)",
+                     "kernel": ("head_kernel" if w.B * w.N <= 64 else "head_large_kernel") +
+                               " + tree_sample_kernel (the whole step, both launches)",
                      "bytes_per_launch": nbytes, "launch_ms": ms_per_step},
         "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk,
     }
@@ -995,9 +996,10 @@ def main():
     else:
         roofline = {"bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s", "frac": tflops / peak_tf}
     roofline.update({"traffic": NCU_TRAFFIC.get(w.name), "peak_kind": peak_kind, "launch_ms": head_ms,
-                     "kernel": ("head_kernel (LM head)" if w.greedy else
+                     "kernel": (("head_kernel" if w.M <= 64 else "head_large_kernel (CTA pairs)") + " (LM head, greedy partials)"
+                                if w.greedy else
                                 "head_kernel (LM head + fused softmax statistics)" if w.M <= 64 else
-                                "head_kernel (LM head, wide precise) + row_stats_kernel (target and draft statistics)"),
+                                "head_large_kernel (LM head on CTA pairs) + row_stats_kernel (target and draft statistics)"),
                      "bytes_per_launch": head_bytes, "flops_per_launch": nb["flops"],
                      "finish_kernel_ms": finish_ms})
     # the whole step against whichever of the step's bytes or flops binds

@@ -412,8 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kb1 = min(g1 * p.gkb, p.num_kb);
         // position in the current slot group (kb0 starts one); a counter, not
         // kb % gkb: an integer division per hidden block in this one issuing
-        // thread held the tensor pipe back (wide scheme at 128 positions: 275
-        // vs 212 us per call)
+        // thread held the tensor pipe back (a 128-position head: 275 vs 212 us
+        // per call)
         int gpos = 0;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[s], ph)) {
