@@ -305,6 +305,218 @@ __global__ void __launch_bounds__(kStatThreads, 3) row_stats_kernel(const float*
   }
 }
 
+// The same partials from a bulk-copy stream (V % 4 == 0, 16-byte aligned
+// rows): one persistent CTA per SM; lane 0 of warp 0 copies whole
+// (row, 4096-token) units -- 16 KB, contiguous -- into a ring of S <= 12
+// shared-memory stages with cp.async.bulk.  Two consumer warps own each stage
+// s: they fold units s, s + S, s + 2S, ... of the CTA's sequence in order
+// (one warp the unit's first two 1024-token blocks, the other the last two,
+// merged through shared memory), so neither waits on its stage's barrier more
+// than one phase ahead (a parity wait two phases ahead would pass on the older
+// phase).  The fold's exp2 chains need many warps to keep the SM busy:
+// twelve warps folding whole units ran at ~4.4 TB/s, the stream alone ~7.5.  Each SM keeps up to S units (~190 KB) in flight, which a
+// register double buffer (one 4 KB block per warp) cannot; the fold reads
+// shared memory four values at a time, so a thread needs few registers.
+constexpr int kBulkConsumers = 24;  // two per stage (S <= 12)
+constexpr int kBulkThreads = 32 * (1 + kBulkConsumers);
+constexpr uint32_t kBulkUnitBytes = kChunk * 4;
+
+// Folds the lane's 32 values of one 1024-token block of a shared-memory stage
+// (the same lane layout as load_block32: tokens 4(32j + lane) .. +3) into its
+// running partial, reading four values at a time, so that a thread needs few
+// registers and sixteen warps per SM fit.  `nv` is the number of the block's
+// tokens inside the row (a multiple of 4; <= 0: none).  Same rules as
+// fold_block32: a non-finite value adds nothing and marks the partial; the
+// terms are summed in four chains of eight.
+__device__ __forceinline__ void fold_smem32(const float* blk, int nv, int lane, Expo c, Partial& lp) {
+  if (nv >= 1024) {
+    float zm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 f = *reinterpret_cast<const float4*>(blk + (j * 32 + lane) * 4);
+      zm = fmaxf(fmaxf(zm, fmaxf(f.x, f.y)), fmaxf(f.z, f.w));
+    }
+    const float hm = expo_hi(zm, c);
+    if (isfinite(hm)) {
+      const float kn = ceilf(hm);
+      const float k = lp.k == -INFINITY ? kn : fmaxf(lp.k, kn);
+      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 f = *reinterpret_cast<const float4*>(blk + (j * 32 + lane) * 4);
+        a0 += pow2_rel(f.x, c, k);
+        a1 += pow2_rel(f.y, c, k);
+        a2 += pow2_rel(f.z, c, k);
+        a3 += pow2_rel(f.w, c, k);
+      }
+      const float sum = (a0 + a1) + (a2 + a3);
+      if (isfinite(sum)) {
+        if (lp.k != -INFINITY && kn > lp.k) {
+          const float sc = pow2_nonpos(lp.k - kn);
+          lp.s = {lp.s.hi * sc, lp.s.lo * sc};
+        }
+        lp.k = k;
+        lp.s = ff_add_f(lp.s, sum);
+        return;
+      }
+    }
+  }
+  // a partial block, or one with a non-finite value: the masked form
+  float hm = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = (j * 32 + lane) * 4;
+    if (e < nv) {
+      const float4 f = *reinterpret_cast<const float4*>(blk + e);
+      const float v[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float h = expo_hi(v[t], c);
+        if (isfinite(h))
+          hm = fmaxf(hm, h);
+        else
+          lp.bad = 1;
+      }
+    }
+  }
+  if (hm == -INFINITY) return;
+  const float kn = ceilf(hm);
+  if (lp.k == -INFINITY) {
+    lp.k = kn;
+  } else if (kn > lp.k) {
+    const float sc = pow2_nonpos(lp.k - kn);
+    lp.s = {lp.s.hi * sc, lp.s.lo * sc};
+    lp.k = kn;
+  }
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int e = (j * 32 + lane) * 4;
+    if (e < nv) {
+      const float4 f = *reinterpret_cast<const float4*>(blk + e);
+      const float v[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float h = expo_hi(v[t], c);
+        if (isfinite(h)) a[t] += exp2f((h - lp.k) + expo_lo(v[t], h, c));
+      }
+    }
+  }
+  lp.s = ff_add_f(lp.s, (a[0] + a[1]) + (a[2] + a[3]));
+}
+
+__global__ void __launch_bounds__(kBulkThreads, 1)
+    row_stats_bulk_kernel(const float* __restrict__ zp, const float* __restrict__ zq, int M, int V, long long ldp,
+                          Expo c, StatPart* tpart, StatPart* dpart, int P, long long units, int* err,
+                          unsigned* tickets, int n_tickets, int S) {
+  extern __shared__ __align__(16) uint8_t bulk_smem[];
+  float* ring = reinterpret_cast<float*>(bulk_smem);
+  uint64_t* full = reinterpret_cast<uint64_t*>(bulk_smem + static_cast<size_t>(S) * kBulkUnitBytes);
+  uint64_t* empty = full + S;
+  float4* handoff = reinterpret_cast<float4*>(empty + S);  // [S] the second half's partial, per stage
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (blockIdx.x == 0) {
+    if (err && threadIdx.x == 0) *err = 0;
+    for (int i = threadIdx.x; i < n_tickets; i += kBulkThreads) tickets[i] = 0u;
+  }
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 2);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // this CTA's units: u = blockIdx.x + i * gridDim.x
+  const long long mine = units > blockIdx.x ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  auto unit_src = [&](long long u, int& row, int& chunk, int& n) -> const float* {
+    row = static_cast<int>(u / P);
+    chunk = static_cast<int>(u - static_cast<long long>(row) * P);
+    n = min(kChunk, V - chunk * kChunk);
+    const float* z = row < M ? zp + static_cast<size_t>(row) * ldp : zq + static_cast<size_t>(row - M) * V;
+    return z + static_cast<size_t>(chunk) * kChunk;
+  };
+  if (warp == 0) {
+    if (lane == 0) {
+      long long issued = 0;
+      for (long long i = 0; i < mine; ++i) {
+        const int s = static_cast<int>(i % S);
+        const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+        if (!mbar_wait(&empty[s], ph ^ 1u)) {
+          if (err) atomicOr(err, kErrTimeout);
+          break;
+        }
+        int row, chunk, n;
+        const float* src = unit_src(blockIdx.x + i * gridDim.x, row, chunk, n);
+        const uint32_t bytes = static_cast<uint32_t>(n) * 4u;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        bulk_load(ring + static_cast<size_t>(s) * kChunk, src, bytes, &full[s]);
+        ++issued;
+      }
+      // the copies in flight land before the CTA may exit
+      for (long long i = issued > S ? issued - S : 0; i < issued; ++i)
+        if (!mbar_wait(&full[i % S], static_cast<uint32_t>((i / S) & 1))) {
+          if (err) atomicOr(err, kErrTimeout);
+          break;
+        }
+    }
+  } else if ((warp - 1) / 2 < S) {
+    const int st = (warp - 1) / 2;  // this warp's stage
+    const int half = (warp - 1) & 1;  // 0: blocks 0-1 of a unit, 1: blocks 2-3
+    for (long long i = st; i < mine; i += S) {
+      // both warps of the pair take the wait's outcome together (a barrier
+      // with an AND reduction that both always reach), so that neither can
+      // be left at the pair's barriers below by the other's timeout
+      const uint32_t got = mbar_wait(&full[st], static_cast<uint32_t>((i / S) & 1)) ? 1u : 0u;
+      uint32_t both;
+      asm volatile(
+          "{\n\t.reg .pred pin, pout;\n\t"
+          "setp.ne.u32 pin, %1, 0;\n\t"
+          "bar.red.and.pred pout, %2, 64, pin;\n\t"
+          "selp.u32 %0, 1, 0, pout;\n\t}\n"
+          : "=r"(both)
+          : "r"(got), "r"(1 + st)
+          : "memory");
+      if (!both) {
+        if (lane == 0 && err) atomicOr(err, kErrTimeout);
+        break;
+      }
+      int row, chunk, n;
+      unit_src(blockIdx.x + i * gridDim.x, row, chunk, n);
+      const float* stage = ring + static_cast<size_t>(st) * kChunk;
+      Partial lp = partial_empty();
+#pragma unroll 1
+      for (int blk = 2 * half; blk < 2 * half + 2; ++blk)
+        fold_smem32(stage + blk * 1024, n - blk * 1024, lane, c, lp);
+      const Partial wp = warp_merge(lp);
+      // the pair meets on a named barrier of its own (1 + stage): the second
+      // half's partial goes through shared memory to the first
+      if (half == 1 && lane == 0) handoff[st] = make_float4(wp.k, wp.s.hi, wp.s.lo, __int_as_float(wp.bad));
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + st) : "memory");
+      if (half == 0 && lane == 0) {
+        const float4 o = handoff[st];
+        Partial other;
+        other.k = o.x;
+        other.s = {o.y, o.z};
+        other.bad = __float_as_int(o.w);
+        const Partial m = partial_merge(wp, other);
+        StatPart out;
+        out.k = m.k;
+        out.s_hi = m.s.hi;
+        out.s_lo = m.s.lo;
+        out.bad = m.bad;
+        if (row < M)
+          tpart[static_cast<size_t>(row) * P + chunk] = out;
+        else
+          dpart[static_cast<size_t>(row - M) * P + chunk] = out;
+      }
+      // both warps' reads of the stage and of the hand-off are done
+      asm volatile("bar.sync %0, 64;" ::"r"(1 + st) : "memory");
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- decision
 // The decision of one sequence, computed by every CTA of that sequence with
 // identical arithmetic (so identically): merge the softmax partials of its
@@ -1078,8 +1290,31 @@ cudaError_t launch_row_stats(const float* zp, const float* zq, int M, int draft_
       std::min<long long>((units + kStatThreads / 32 - 1) / (kStatThreads / 32), static_cast<long long>(std::max(per_sm, 1)) * sms));
   const Expo c{c_hi, c_lo};
   if (ldp <= 0) ldp = V;
-  if (V % 4 == 0 && ldp % 4 == 0 && (reinterpret_cast<uintptr_t>(zp) & 15u) == 0 &&
-      (reinterpret_cast<uintptr_t>(zq) & 15u) == 0)
+  const bool vec = V % 4 == 0 && ldp % 4 == 0 && (reinterpret_cast<uintptr_t>(zp) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(zq) & 15u) == 0;
+  // large passes (a few units per SM at least) stream through the bulk-copy
+  // ring; small ones are latency-bound and keep the many-warp form
+  if (vec && units >= 4ll * sms) {
+    int smem_optin = 0;
+    e = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    const int S = std::min(12, (smem_optin - 1024) / static_cast<int>(kBulkUnitBytes + 32));
+    if (S >= 4) {
+      const size_t smem = static_cast<size_t>(S) * (kBulkUnitBytes + 32);
+      static bool attr_done[64] = {false};
+      if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+      if (!attr_done[dev]) {
+        e = cudaFuncSetAttribute(row_stats_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+      }
+      const int bgrid = static_cast<int>(std::min<long long>(units, sms));
+      row_stats_bulk_kernel<<<bgrid, kBulkThreads, smem, stream>>>(zp, zq, M, V, ldp, c, tpart, dpart, P, units,
+                                                                    err, tickets, n_tickets, S);
+      return cudaGetLastError();
+    }
+  }
+  if (vec)
     row_stats_kernel<true><<<grid, kStatThreads, 0, stream>>>(zp, zq, M, V, ldp, c, tpart, dpart, P, units, err,
                                                               tickets, n_tickets);
   else
