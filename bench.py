@@ -883,6 +883,96 @@ def run_tree_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_from_logits(args, w):
+    """The tiny workload: the verify step on given target logits (no LM head),
+    spec_verify_from_logits.  Latency-bound (36 KB of inputs); reported in
+    positions/s and microseconds, with the input bytes against the copy peak."""
+    import speculative_decoding_verification_67_gb300 as sv
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    inp = synth.make_inputs(w, device=dev, seed=w.seed + rank)
+    T, B, K, V, M = w.temperature, w.B, w.K, w.V, w.M
+    stream = torch.cuda.current_stream(dev)
+    ws = torch.empty(sv.from_logits_workspace_bytes(B, K, V, T), dtype=torch.uint8, device=dev)
+    tok = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    n = torch.empty((B,), dtype=torch.int32, device=dev)
+
+    def step(zp=inp["target_logits"], zq=inp["draft_logits"], x=inp["draft_tokens"], u=inp["uniforms"]):
+        sv.spec_verify_from_logits(zp, zq, x, u, T, out_tokens=tok, out_num_accepted=n, workspace=ws,
+                                   stream=stream)
+
+    peak_gbs, _, _, peak_kind = load_peaks()
+    clocks = ClockSampler(local)
+    clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.begin_timed()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.end_timed()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    value, ms = job_throughput(ms, world, M, args.steps)
+    ms_per_step = ms / args.steps
+    nbytes = 4 * M * V + 4 * B * K * V + 4 * B * K + 4 * M   # logits, drafts, uniforms read once
+    gbs = nbytes / (ms_per_step * 1e-3) / 1e9
+    # end to end through the same public call: the step's inputs copied in
+    # from pinned host memory, the tokens and counts copied back
+    host = {k: v.cpu().pin_memory() for k, v in inp.items() if isinstance(v, torch.Tensor)}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    tok_h = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    n_h = torch.empty((B,), dtype=torch.int32).pin_memory()
+
+    def e2e_step():
+        for k in dev_in:
+            dev_in[k].copy_(host[k], non_blocking=True)
+        step(dev_in["target_logits"], dev_in["draft_logits"], dev_in["draft_tokens"], dev_in["uniforms"])
+        tok_h.copy_(tok, non_blocking=True)
+        n_h.copy_(n, non_blocking=True)
+        stream.synchronize()
+
+    e2e_steps = max(10, min(args.steps, 500))
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    e2e = {"value": world * M * e2e_steps / e2e_s, "unit": "verified positions/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": (M + B) * 4, "steps": e2e_steps, "ms_per_step": 1e3 * e2e_s / e2e_steps,
+           "timer": "host wall clock around copy-in, spec_verify_from_logits, copy-out, synchronise"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "verified positions/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "us_per_step": 1e3 * ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "K": K, "V": V, "T": T, "positions_per_step": M,
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "latency-bound: 36 KB of inputs, L2-resident between steps"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak_gbs, "unit": "GB/s", "frac": gbs / peak_gbs,
+                     "traffic": None, "peak_kind": peak_kind, "launch_ms": ms_per_step,
+                     "kernel": "row_stats_kernel + the finishing kernel (the whole step, both launches)",
+                     "bytes_per_launch": nbytes,
+                     "note": "a launch-latency-bound step: the fraction only shows how far from bandwidth it is"},
+        "e2e": e2e, "gpu_launches": 2 * args.steps, "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(w, inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -928,6 +1018,8 @@ def main():
     if args.impl == "reference":
         run_reference(args, w)
         return
+    if w.d == 0:
+        return run_from_logits(args, w)
 
     import speculative_decoding_verification_67_gb300 as sv
     rank, world, local = dist_setup(args.gpus)
