@@ -82,7 +82,7 @@ def test_lm_head_is_deterministic():
 
 @pytest.mark.parametrize("B,K,T", [(2, 3, 0.9),      # 16-column precise head, stream-K split tiles
                                    (8, 4, 0.8),      # 48 columns
-                                   (40, 7, 1.1),     # wide precise scheme, three position chunks, statistics pass
+                                   (40, 7, 1.1),     # large-batch head (two chunks of 160), statistics pass
                                    (40, 7, 0.0)])    # large-batch greedy (transposed argmax epilogue)
 def test_whole_step_is_deterministic(B, K, T):
     """The same inputs twice through the whole step (LM head, statistics,
@@ -134,6 +134,49 @@ def test_verify_from_logits_matches_oracle(B, K, V, T):
     st = compare_sampling(np_int(tok), np_int(n), ref, K)
     print(f"\nfrom_logits B={B} K={K} V={V} T={T}: {st}")
     compare_debug(np64(dbg), ref, np_int(n), K, T)
+
+
+# Statistics passes with at least four (row, 4096-token) units per SM and rows
+# on 16-byte boundaries stream through the bulk-copy ring (two warps a stage);
+# smaller ones use the many-warp form.  The ring's cases: a last chunk of 4
+# tokens (a partial block of one vector), exact chunks, a last chunk of one
+# whole 1024-token block.
+@pytest.mark.parametrize("B,K,V,T", [(64, 4, 16388, 0.9), (48, 4, 12288, 1.1), (40, 3, 33792, 1.0),
+                                     (32, 8, 20484, 0.7)])
+def test_statistics_pass_streaming_form(B, K, V, T):
+    zp, zq, x, u = _from_logits_case(B, K, V, T, seed=B * 7 + V)
+    units = (B * (K + 1) + B * K) * ((V + 4095) // 4096)
+    assert units >= 4 * torch.cuda.get_device_properties(0).multi_processor_count and V % 4 == 0
+    outs = []
+    for _ in range(2):
+        dbg = torch.zeros((B, K + 1, sv.SPEC_DEBUG_FIELDS), device="cuda")
+        tok, n = sv.spec_verify_from_logits(zp, zq, x, u, T, out_debug=dbg)
+        torch.cuda.synchronize()
+        outs.append((tok.clone(), n.clone(), dbg.clone()))
+    assert all(torch.equal(outs[0][i], outs[1][i]) for i in range(3))   # deterministic
+    tok, n, dbg = outs[0]
+    ref = oracle.verify_sampling(np64(zp).reshape(B, K + 1, V), np64(zq).reshape(B, K, V), np_int(x), np64(u), t32(T))
+    st = compare_sampling(np_int(tok), np_int(n), ref, K)
+    print(f"\nstreaming statistics B={B} K={K} V={V} T={T}: {st}")
+    compare_debug(np64(dbg), ref, np_int(n), K, T)
+
+
+def test_statistics_pass_streaming_form_nonfinite():
+    """A NaN target logit and an infinite draft logit in the ring form mark
+    only their sequences; the others match the oracle."""
+    B, K, V, T = 64, 4, 16388, 1.0
+    zp, zq, x, u = _from_logits_case(B, K, V, T, seed=77)
+    zp[5 * (K + 1) + 1, 16385] = float("nan")      # in the last, 4-token chunk
+    zq[9 * K + 2, 4097] = float("inf")             # in a whole chunk
+    ws = torch.empty(sv.from_logits_workspace_bytes(B, K, V, T), dtype=torch.uint8, device="cuda")
+    tok, n = sv.spec_verify_from_logits(zp, zq, x, u, T, workspace=ws)
+    assert sv.read_error(ws) & sv.DEVERR_NONFINITE
+    n, tok = np_int(n), np_int(tok)
+    assert n[5] == -1 and n[9] == -1 and (tok[5] == -1).all() and (tok[9] == -1).all()
+    keep = [b for b in range(B) if b not in (5, 9)]
+    z3, q3 = np64(zp).reshape(B, K + 1, V)[keep], np64(zq).reshape(B, K, V)[keep]
+    ref = oracle.verify_sampling(z3, q3, np_int(x)[keep], np64(u)[keep], t32(T))
+    compare_sampling(tok[keep], n[keep], ref, K)
 
 
 def _degenerate_case(kind, B=16, K=4, V=300, T=1.0, seed=0):
@@ -292,10 +335,10 @@ def test_determinism_bits():
                                        (8, 7, 512, 7000, 0.9),      # M = 64: every column used
                                        (2, 3, 256, 3000, 1e-6),     # |z / T| in log2 units around 2^22
                                        (2, 3, 256, 3000, 1e-8),     # ... and beyond 2^24
-                                       (40, 7, 256, 3001, 0.9),     # M = 320: wide precise scheme, chunks of 128 (the last 64)
-                                       (20, 12, 128, 1500, 1.3),    # M = 260: three chunks, the last 4 rows
-                                       (100, 10, 128, 2000, 1.0),   # M = 1100: 9 chunks
-                                       (80, 0, 128, 1000, 1.0)])    # wide precise scheme, bonus draws only
+                                       (40, 7, 256, 3001, 0.9),     # M = 320: large-batch head, two chunks of 160
+                                       (20, 12, 128, 1500, 1.3),    # M = 260: two chunks of 160, the second of 100 rows
+                                       (100, 10, 128, 2000, 1.0),   # M = 1100: 5 chunks of 224
+                                       (80, 0, 128, 1000, 1.0)])    # large-batch head, bonus draws only
 def test_spec_verify_small(B, K, d, V, T):
     w = synth.custom("small", B=B, K=K, d=d, V=V, temperature=T, seed=B + K + d + V)
     inp, tok, n, logits, dbg = _run_head_case(w)
@@ -389,11 +432,12 @@ def test_nonfinite_logit_marks_the_sequence():
     assert np_int(n3)[1] == -1
 
 
-@pytest.mark.parametrize("B,K", [(3, 2), (24, 4)])   # precise and wide precise LM-head schemes
+@pytest.mark.parametrize("B,K", [(3, 2), (24, 4)])   # the small-batch and the large-batch LM head
 def test_nonfinite_hidden_marks_the_sequence(B, K):
     """A NaN or infinite hidden state makes its position's logits non-finite
-    (in the precise head's fused statistics, or in the statistics pass after
-    the wide head): that sequence is flagged, the others are unaffected."""
+    (in the small-batch head's fused statistics, or in the statistics pass
+    after the large-batch head): that sequence is flagged, the others are
+    unaffected."""
     w = synth.custom("nf_head", B=B, K=K, d=256, V=3000, temperature=1.0, seed=21 + B)
     inp = synth.make_inputs(w, device="cuda")
     B, K, V, T = w.B, w.K, w.V, w.temperature
@@ -520,8 +564,8 @@ def test_head_precision_keeps_draws_headline():
 
 def test_head_precision_keeps_draws_large_batch():
     """The same measure on 48 rows of the B=64, d=8192 workload, whose LM head
-    (576 positions) runs the wide precise scheme (an accumulator over the
-    whole hidden size moved ~0.24 % of these draws)."""
+    (576 positions) runs the large-batch kernel's 1024-product groups (an
+    accumulator over the whole hidden size moved ~0.24 % of these draws)."""
     w = synth.WORKLOADS["head_B64_K8_V152064"]
     inp = synth.make_inputs(w, device="cuda")
     rows = 48
