@@ -59,6 +59,7 @@ struct HeadPlan {
   int num_vt = 0;       // vocabulary tiles, ceil(V / 128)
   int num_tiles = 0;    // num_vt * num_chunks
   int num_kb = 0;       // ceil(d / 64)
+  int kbs = 1;          // hidden blocks per pipeline stage (large-batch kernel: 2 when num_kb is even)
   int stages = 0;       // shared-memory pipeline depth
   uint32_t tmem_cols = 0;
   size_t smem_bytes = 0;

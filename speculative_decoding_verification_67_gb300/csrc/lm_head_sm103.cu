@@ -69,6 +69,7 @@ struct HeadParams {
   unsigned long long* flags;    // [grid][4] = epoch once the CTA's quadrant's sums are stored
   unsigned long long epoch;     // unique per launch
   int N, num_chunks, num_vt, num_tiles, num_kb, stages;
+  int kbs;                      // hidden blocks per pipeline stage (large-batch kernel: 1 or 2)
   uint32_t tmem_cols;
   float* logits;
   long long ldz;       // row stride of logits in floats
@@ -821,7 +822,10 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
   const int N = p.N;
   const int NH = N >> 1;                 // columns per epilogue half
   const int NB = kPair ? NH : N;         // hidden rows of this CTA's B tile
-  const uint32_t stage_bytes = kABytes + static_cast<uint32_t>(NB) * 128u;
+  // a stage holds kbs hidden blocks: [A_0 .. A_{kbs-1}][B_0 .. B_{kbs-1}]
+  const int kbs = p.kbs;
+  const uint32_t b_bytes = static_cast<uint32_t>(NB) * 128u;
+  const uint32_t stage_bytes = static_cast<uint32_t>(kbs) * (kABytes + b_bytes);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
   uint64_t* full = bars;              // [S] TMA landed (pair: both CTAs' bytes, on the leader)
   uint64_t* empty = bars + S;         // [S] MMAs reading the stage are done
@@ -889,24 +893,29 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
         const int pc = tile - vt * p.num_chunks;
         const int w_row = vt * kRowsPerTile + static_cast<int>(rank) * kHeadTileV;
         const int h_row = pc * N + static_cast<int>(rank) * NB;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = 0; kb < p.num_kb; kb += kbs) {
           if (!mbar_wait(&empty[s], ph ^ 1u)) {
             report_timeout(p.err);
             ok = false;
             break;
           }
           uint8_t* a_dst = smem + static_cast<size_t>(s) * stage_bytes;
+          uint8_t* b_dst = a_dst + static_cast<size_t>(kbs) * kABytes;
           if constexpr (kPair) {
             // both CTAs' bytes complete on the leader's barrier, which
             // expects them all
             if (rank == 0) mbar_arrive_expect_tx(&full[s], 2u * stage_bytes);
             const uint32_t bar = cluster_map(&full[s], 0);
-            tma_load_2d_pair(a_dst, &tmap_w, bar, kb * kHeadTileK, w_row, pol_w);
-            tma_load_2d_pair(a_dst + kABytes, &tmap_h, bar, kb * kHeadTileK, h_row, pol_h);
+            for (int j = 0; j < kbs; ++j) {
+              tma_load_2d_pair(a_dst + j * kABytes, &tmap_w, bar, (kb + j) * kHeadTileK, w_row, pol_w);
+              tma_load_2d_pair(b_dst + j * b_bytes, &tmap_h, bar, (kb + j) * kHeadTileK, h_row, pol_h);
+            }
           } else {
             mbar_arrive_expect_tx(&full[s], stage_bytes);
-            tma_load_2d(a_dst, &tmap_w, &full[s], kb * kHeadTileK, w_row, pol_w);
-            tma_load_2d(a_dst + kABytes, &tmap_h, &full[s], kb * kHeadTileK, h_row, pol_h);
+            for (int j = 0; j < kbs; ++j) {
+              tma_load_2d(a_dst + j * kABytes, &tmap_w, &full[s], (kb + j) * kHeadTileK, w_row, pol_w);
+              tma_load_2d(b_dst + j * b_bytes, &tmap_h, &full[s], (kb + j) * kHeadTileK, h_row, pol_h);
+            }
           }
           ++issued;
           if (++s == S) {
@@ -937,47 +946,62 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
     // ------------------------------------------------------------ MMA issuer (the leader's)
     if (lane == 0 && rank == 0) {
       const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kHeadTileV : kHeadTileV, static_cast<uint32_t>(N));
+      // The tensor pipe idles whenever this one thread falls behind, so its
+      // loop is kept short: the operand descriptors of stage 0 are built once
+      // and stepped by adding to their start-address field (address >> 4; the
+      // stages are 1024-byte aligned and below 256 KB, so the field never
+      // carries): + stage_bytes >> 4 per stage, + 2 per 16-wide K step.
+      const uint64_t a_desc0 = smem_desc_k_sw128(smem_u32(smem));
+      const uint64_t b_desc0 = smem_desc_k_sw128(smem_u32(smem) + static_cast<uint32_t>(kbs) * kABytes);
+      const uint64_t stage_step = stage_bytes >> 4;
       int s = 0;
       uint32_t ph = 0;
+      uint64_t soff = 0;  // stage s's offset in descriptor units
       int slot = 0;
       uint32_t sph = 0;
       bool ok = true;
       for (int tile = unit0; ok && tile < p.num_tiles; tile += units) {
         int gpos = 0;  // position in the current group (a counter: no division in this thread)
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = 0; kb < p.num_kb; kb += kbs) {
           if (!mbar_wait(&full[s], ph)) {
             report_timeout(p.err);
             ok = false;
             break;
           }
+          // groups are whole stages (kLargeGroup is a multiple of kbs)
           const bool group_first = gpos == 0;
-          const bool group_last = gpos == kLargeGroup - 1 || kb + 1 == p.num_kb;
-          gpos = group_last ? 0 : gpos + 1;
-          if (group_first && !(kPair ? mbar_wait_cluster(&afree[slot], sph ^ 1u) : mbar_wait(&afree[slot], sph ^ 1u))) {
-            report_timeout(p.err);
-            ok = false;
-            break;
+          const bool group_last = gpos + kbs == kLargeGroup || kb + kbs >= p.num_kb;
+          gpos = group_last ? 0 : gpos + kbs;
+          if (group_first) {
+            // the slot the group overwrites has been drained by the epilogue
+            if (!(kPair ? mbar_wait_cluster(&afree[slot], sph ^ 1u) : mbar_wait(&afree[slot], sph ^ 1u))) {
+              report_timeout(p.err);
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
           }
-          tc_fence_after_sync();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(slot * N);
-          const uint32_t a_addr = smem_u32(smem + static_cast<size_t>(s) * stage_bytes);
-          const uint32_t b_addr = a_addr + kABytes;
+          const uint64_t a_desc = a_desc0 + soff, b_desc = b_desc0 + soff;
+          for (int j = 0; j < kbs; ++j) {
+            const uint64_t aj = a_desc + j * (kABytes >> 4), bj = b_desc + j * (b_bytes >> 4);
 #pragma unroll
-          for (int k = 0; k < kHeadTileK / 16; ++k) {
-            const uint32_t accumulate = (group_first && k == 0) ? 0u : 1u;
-            if constexpr (kPair)
-              mma_bf16_ss_pair(d_tmem, smem_desc_k_sw128(a_addr + k * 32), smem_desc_k_sw128(b_addr + k * 32), idesc,
-                               accumulate);
-            else
-              mma_bf16_ss(d_tmem, smem_desc_k_sw128(a_addr + k * 32), smem_desc_k_sw128(b_addr + k * 32), idesc,
-                          accumulate);
+            for (int k = 0; k < kHeadTileK / 16; ++k) {
+              const uint32_t accumulate = (group_first && j == 0 && k == 0) ? 0u : 1u;
+              if constexpr (kPair)
+                mma_bf16_ss_pair(d_tmem, aj + 2 * k, bj + 2 * k, idesc, accumulate);
+              else
+                mma_bf16_ss(d_tmem, aj + 2 * k, bj + 2 * k, idesc, accumulate);
+            }
           }
           if constexpr (kPair)
             mma_commit_pair(&empty[s], 0x3);  // frees the stage in both CTAs
           else
             mma_commit(&empty[s]);
+          soff += stage_step;
           if (++s == S) {
             s = 0;
+            soff = 0;
             ph ^= 1u;
           }
           if (group_last) {
@@ -1301,16 +1325,21 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
   const long long units = h.streamk ? static_cast<long long>(h.num_tiles) * h.groups : h.num_tiles;
   h.grid = static_cast<int>(std::min<long long>(units, std::min(dev.sm_count, kMaxHeadGrid)));
   if (h.large) {
+    // two hidden blocks a stage when the blocks pair up: one barrier wait
+    // and one commit of the MMA thread for every eight MMAs
+    h.kbs = h.num_kb % 2 == 0 ? 2 : 1;
+    fit(static_cast<size_t>(h.kbs) * (kABytes + static_cast<size_t>(h.N) * 128));
+    h.grid = static_cast<int>(std::min<long long>(h.num_tiles, std::min(dev.sm_count, kMaxHeadGrid)));
     // CTA pairs where their clusters fit: tiles of 256 vocabulary rows, each
     // CTA holding half of the chunk's hidden rows
-    fit(kABytes + static_cast<size_t>(h.N / 2) * 128);
+    fit(static_cast<size_t>(h.kbs) * (kABytes + static_cast<size_t>(h.N / 2) * 128));
     const int clusters = large_pair_clusters(dev, h.smem_bytes);
     if (clusters > 0) {
       h.pair = true;
       h.num_tiles = ((V + 2 * kHeadTileV - 1) / (2 * kHeadTileV)) * h.num_chunks;
       h.grid = 2 * std::min(clusters, h.num_tiles);
     } else {
-      fit(kABytes + static_cast<size_t>(h.N) * 128);
+      fit(static_cast<size_t>(h.kbs) * (kABytes + static_cast<size_t>(h.N) * 128));
     }
   }
   // the small-batch statistics: one running partial per CTA and target row
@@ -1340,6 +1369,7 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
   p.num_vt = h.num_vt;
   p.num_tiles = h.num_tiles;
   p.num_kb = h.num_kb;
+  p.kbs = h.kbs;
   p.stages = h.stages;
   p.tmem_cols = h.tmem_cols;
   p.logits = logits;
