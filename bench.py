@@ -68,6 +68,15 @@ def load_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def draft_rows_in_head(M: int, draft_rows: int, d: int, V: int) -> bool:
+    """The library's rule for where the draft rows are reduced above 64
+    positions (capi.cu, draft_fits_side_warps): by the large-batch head's two
+    side warps when ~0.25 TB/s covers them within the head's estimated run,
+    else by a streaming pass after the head (one more launch)."""
+    head_ns = max(2.0 * V * d / 6500.0, 2.0 * M * d * V / 1.3e6)
+    return 4.0 * draft_rows * V <= 250.0 * head_ns
+
+
 def step_bytes(w) -> dict:
     """Algorithmic bytes of one step and of the LM-head launch."""
     M, d, V, B, K = w.M, w.d, w.V, w.B, w.K
@@ -1076,9 +1085,8 @@ def main():
     finish_ms = statistics.mean(t[1].elapsed_time(t[2]) for t in evs)
     nb = step_bytes(w)
     # the timed interval also covers the draft logits' read (by the head's side
-    # warps at M <= 64; above that by the statistics pass after the head, which
-    # also re-reads the target logits the head wrote: traffic beyond the
-    # algorithmic bytes, counted against the path)
+    # warps, or above 64 positions by the pass after the head when they would
+    # outlast it)
     head_bytes = nb["head"] if w.greedy else nb["step"]
     gbs = head_bytes / (head_ms * 1e-3) / 1e9
     tflops = nb["flops"] / (head_ms * 1e-3) / 1e12
@@ -1091,7 +1099,10 @@ def main():
                      "kernel": (("head_kernel" if w.M <= 64 else "head_large_kernel (CTA pairs)") + " (LM head, greedy partials)"
                                 if w.greedy else
                                 "head_kernel (LM head + fused softmax statistics)" if w.M <= 64 else
-                                "head_large_kernel (LM head on CTA pairs) + row_stats_kernel (target and draft statistics)"),
+                                "head_large_kernel (LM head on CTA pairs + fused softmax statistics)"
+                                if draft_rows_in_head(w.M, w.B * w.K, w.d, w.V) else
+                                "head_large_kernel (LM head on CTA pairs + fused target statistics) + "
+                                "row_stats_bulk_kernel (draft rows)"),
                      "bytes_per_launch": head_bytes, "flops_per_launch": nb["flops"],
                      "finish_kernel_ms": finish_ms})
     # the whole step against whichever of the step's bytes or flops binds
@@ -1172,7 +1183,9 @@ def main():
         "tokens_committed_per_s": world * committed * args.steps / (ms / 1e3),
         "mean_accepted": float(n.float().mean().item()),
         "roofline": roofline, "roofline_step": roofline_step,
-        "e2e": e2e, "gpu_launches": args.steps * (2 if w.greedy else 3 if M > 64 else 2), "clocks": clk,
+        "e2e": e2e, "clocks": clk,
+        "gpu_launches": args.steps * (3 if not w.greedy and w.M > 64 and w.K > 0 and
+                                      not draft_rows_in_head(w.M, w.B * w.K, w.d, w.V) else 2),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_sample(w, inp)

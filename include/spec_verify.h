@@ -159,8 +159,7 @@ SPEC_API spec_status spec_verify(const void *hidden, const void *W_lm, const flo
  * spec_verify with per-stage timing: identical arguments and work, plus
  * `stage_events`, an array of 3 cudaEvent_t handles (created by the caller)
  * recorded on `stream` before the LM-head kernel, between the LM head (with
- * its fused softmax statistics, or the head and the statistics pass for
- * large batches) and the finishing kernel, and after it.  The events sit
+ * its fused softmax statistics) and the finishing kernel, and after it.  The events sit
  * between the launches, so the finishing kernel no longer overlaps the
  * head's tail; use it to attribute time, not to measure the step.
  */

@@ -79,11 +79,11 @@ Layout make_layout(int B, int K, int V, bool greedy, bool logits_in_ws, bool fro
     off += round_up(sv::kFixupBytes);
   }
   if (!greedy) {
-    // the LM head writes one partial per CTA (at most kMaxHeadGrid CTAs) or,
-    // with more than a few position chunks, one per vocabulary tile
+    // the LM head writes one partial per CTA (at most kMaxHeadGrid CTAs), the
+    // streaming pass over given logits one per 4096-token chunk
     L.tpart = off;
     const size_t parts = from_logits ? static_cast<size_t>(L.CA)
-                                     : std::max(num_vt, static_cast<size_t>(sv::kMaxHeadGrid));
+                                     : std::max(static_cast<size_t>(L.CA), static_cast<size_t>(sv::kMaxHeadGrid));
     off += round_up(sizeof(sv::StatPart) * M * parts);
     L.dpart = off;
     off += round_up(sizeof(sv::StatPart) * static_cast<size_t>(B) * K * L.CA);
@@ -102,6 +102,19 @@ Layout make_layout(int B, int K, int V, bool greedy, bool logits_in_ws, bool fro
   }
   L.total = off;
   return L;
+}
+
+// Whether the large-batch LM head's two side warps can reduce the draft rows
+// within the head's own run.  Measured on GB300 they stream ~0.25 TB/s in all
+// (two warps per SM beside the epilogue), and the head lasts about the longer
+// of its weight stream (~6.5 TB/s) and its products (~1.3 PFLOP/s): at
+// B = 16, K = 4, V = 128256 (33 MB of draft logits) they fit and save the
+// pass; at B = 64, K = 8, d = 8192, V = 152064 (311 MB) they outlasted the
+// head by ~70 us, against ~55 us for the streaming pass after it.
+bool draft_fits_side_warps(int M, int draft_rows, int d, int V) {
+  const double draft_bytes = 4.0 * draft_rows * V;
+  const double head_ns = std::max(2.0 * V * d / 6500.0, 2.0 * M * static_cast<double>(d) * V / 1.3e6);
+  return draft_bytes <= 250.0 * head_ns;
 }
 
 bool dims_ok(const spec_dims& d, bool need_head) {
@@ -263,32 +276,26 @@ spec_status verify_impl(const void* hidden, const void* W_lm, const float* draft
   sv::exponent_constant(temperature, &hs.c_hi, &hs.c_lo);
   hs.tpart = reinterpret_cast<sv::StatPart*>(ws + L.tpart);
   hs.zq = draft_logits;
-  hs.draft_rows = dims.B * dims.K;
+  const bool draft_in_head = !plan.large || draft_fits_side_warps(M, dims.B * dims.K, dims.d, dims.V);
+  hs.draft_rows = draft_in_head ? dims.B * dims.K : 0;
   hs.dpart = reinterpret_cast<sv::StatPart*>(ws + L.dpart);
   hs.tickets = reinterpret_cast<unsigned*>(reinterpret_cast<int*>(ws) + kCtrlTickets);
   hs.n_tickets = dims.B;
-  // Up to 64 positions the LM head's epilogue produces the target statistics
-  // as it writes the logits (one partial per CTA), and its side warps reduce
-  // the draft rows meanwhile, hidden under the weight stream.  Above that the
-  // head is tensor-bound: it writes logits only, and one streaming pass forms
-  // every target and draft row's partials.
-  int Pt = plan.target_parts;
-  if (plan.large) {
-    e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kLogits, logits, nullptr, nullptr, nullptr, err,
-                        true, dev, s, &enc_fail, ldz, nullptr);
-    if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
-    e = sv::launch_row_stats(logits, draft_logits, M, dims.B * dims.K, dims.V, hs.c_hi, hs.c_lo, hs.tpart, hs.dpart,
-                             err, hs.tickets, hs.n_tickets, s, ldz);
+  // The LM head's epilogue produces the target statistics as it writes the
+  // logits (one partial per CTA and row), and its side warps reduce the draft
+  // rows meanwhile, unless they would outlast the head: then a streaming pass
+  // after it reduces them (keeping the head's error word).
+  e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kStats, logits, nullptr, nullptr, &hs, err,
+                      true, dev, s, &enc_fail, ldz, L.fix ? ws + L.fix : nullptr);
+  if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
+  if (!draft_in_head && dims.K > 0) {
+    e = sv::launch_row_stats(draft_logits, draft_logits, 0, dims.B * dims.K, dims.V, hs.c_hi, hs.c_lo, nullptr,
+                             hs.dpart, err, nullptr, 0, s, 0, false);
     if (e != cudaSuccess) return SPEC_ERR_CUDA;
-    Pt = L.CA;
-  } else {
-    e = sv::launch_head(hidden, W_lm, M, dims.d, dims.V, sv::HeadOut::kStats, logits, nullptr, nullptr, &hs, err,
-                        true, dev, s, &enc_fail, ldz, L.fix ? ws + L.fix : nullptr);
-    if (enc_fail || e != cudaSuccess) return SPEC_ERR_CUDA;
   }
   if (!mark(1)) return SPEC_ERR_CUDA;
   sv::VerifyArgs a = sampling_args(L, dims, temperature, logits, draft_logits, draft_tokens, uniforms,
-                                   out_tokens, out_num_accepted, out_debug, ws, Pt);
+                                   out_tokens, out_num_accepted, out_debug, ws, plan.target_parts);
   a.ldp = ldz;
   e = sv::launch_verify_sampling(a, s);
   return (e == cudaSuccess && mark(2)) ? SPEC_OK : SPEC_ERR_CUDA;

@@ -135,11 +135,11 @@ struct VerifyArgs {
 void exponent_constant(float temperature, float* c_hi, float* c_lo);
 
 // Softmax partials of given target and draft logits (per row and 4096-token
-// chunk); clears *err first when err is given, and the n_tickets tickets.
-// Target row r starts at zp + r * ldp (ldp 0: V).
+// chunk); clears *err first when err is given and zero_err is set, and the
+// n_tickets tickets.  Target row r starts at zp + r * ldp (ldp 0: V).
 cudaError_t launch_row_stats(const float* zp, const float* zq, int M, int draft_rows, int V, float c_hi, float c_lo,
                              StatPart* tpart, StatPart* dpart, int* err, unsigned* tickets, int n_tickets,
-                             cudaStream_t stream, long long ldp = 0);
+                             cudaStream_t stream, long long ldp = 0, bool zero_err = true);
 
 // Decision and residual draw (one launch, chained with programmatic
 // dependent launch after the statistics).

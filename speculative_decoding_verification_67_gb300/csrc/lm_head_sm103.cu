@@ -196,75 +196,139 @@ __device__ __forceinline__ void store_part(StatPart* dst, const Partial& a) {
   *dst = sp;
 }
 
-// Draft-row statistics by warps 6-7: units of (draft row, 4096-token chunk)
-// taken round-robin over CTAs; each lane streams 128 tokens of the unit in 4
-// blocks of 32, keeping a partial against an integer reference that only
-// moves up (exact rescaling), then the warp merges its lanes.
+// One lane's share of a 1024-token block of a draft row, 32 values: the
+// largest finite h = z c, an integer reference k above it (ref_above), the 32
+// terms 2^(z c - k) <= 1 summed in f32, and that sum added to the lane's
+// float-float partial after bringing both to the larger reference (exact
+// powers of two).  `valid` marks the values inside the row; a non-finite value
+// marks the partial and is left out of it.
+template <bool kAll>
+__device__ __forceinline__ void draft_block(const float (&x)[32], unsigned valid, Expo c, Partial& lp) {
+  float hm = -INFINITY;
+  int bad = 0;
+#pragma unroll
+  for (int t = 0; t < 32; ++t) {
+    const float h = expo_hi(x[t], c);
+    const bool in = kAll || ((valid >> t) & 1u);
+    const bool fin = fabsf(h) < INFINITY;
+    bad |= (in && !fin) ? 1 : 0;
+    hm = (in && fin) ? fmaxf(hm, h) : hm;
+  }
+  lp.bad |= bad;
+  if (hm == -INFINITY) return;
+  const float k = ref_above(hm);
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int t = 0; t < 32; t += 2) {
+    const float h0 = expo_hi(x[t], c), h1 = expo_hi(x[t + 1], c);
+    const float e0 = exp2f((h0 - k) + expo_lo(x[t], h0, c));
+    const float e1 = exp2f((h1 - k) + expo_lo(x[t + 1], h1, c));
+    const bool u0 = (kAll || ((valid >> t) & 1u)) && fabsf(h0) < INFINITY;
+    const bool u1 = (kAll || ((valid >> (t + 1)) & 1u)) && fabsf(h1) < INFINITY;
+    s0 += u0 ? e0 : 0.f;
+    s1 += u1 ? e1 : 0.f;
+  }
+  const float sb = s0 + s1;
+  if (lp.k == -INFINITY) {
+    lp.k = k;
+    lp.s = {sb, 0.f};
+  } else {
+    const float kn = fmaxf(lp.k, k);
+    const float fa = pow2_nonpos(lp.k - kn);
+    lp.s = ff_add_f({lp.s.hi * fa, lp.s.lo * fa}, sb * pow2_nonpos(k - kn));
+    lp.k = kn;
+  }
+}
+
+// Draft-row statistics by two side warps (6-7 of the small-batch head, 10-11
+// of the large-batch one): units of (draft row, 4096-token chunk) taken
+// round-robin over CTAs, each streamed as four blocks of 1024 tokens (eight
+// float4 per lane), the next block's loads in flight while the current one is
+// summed (draft_block); the warp merges its lanes per unit.  (Two blocks ahead,
+// or loads that skip L2 retention, measured no faster.)  Rows whose
+// length is not a multiple of 4 floats are read with scalar loads.
 __device__ void draft_stats(const HeadParams& p, int side_warp, int lane) {
+  constexpr int kBlocks = kChunk / 1024;
   const Expo c{p.c_hi, p.c_lo};
   const long long units = static_cast<long long>(p.draft_rows) * p.dparts;
-  const bool vec = (p.V % 4) == 0;
-  for (long long i = side_warp;; i += 2) {
-    const long long u = blockIdx.x + i * gridDim.x;
-    if (u >= units) break;
-    const int row = static_cast<int>(u / p.dparts);
-    const int chunk = static_cast<int>(u - static_cast<long long>(row) * p.dparts);
-    const float* z = p.zq + static_cast<size_t>(row) * p.V;
-    Partial lp = partial_empty();
+  const long long stride = 2LL * gridDim.x;
+  long long u = blockIdx.x + static_cast<long long>(side_warp) * gridDim.x;
+  if (u >= units) return;
+  if (p.V % 4 != 0) {
+    for (; u < units; u += stride) {
+      const int row = static_cast<int>(u / p.dparts);
+      const int chunk = static_cast<int>(u - static_cast<long long>(row) * p.dparts);
+      const float* z = p.zq + static_cast<size_t>(row) * p.V;
+      Partial lp = partial_empty();
 #pragma unroll 1
-    for (int blk = 0; blk < kChunk / 1024; ++blk) {
-      float zv[32];
-      unsigned valid = 0;
-      const int base = chunk * kChunk + blk * 1024;
+      for (int blk = 0; blk < kBlocks; ++blk) {
+        const int base = chunk * kChunk + blk * 1024;
+        float x[32];
+        unsigned valid = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const int e = base + (j * 32 + lane) * 4;
-        if (vec && e + 3 < p.V) {
-          const float4 f = __ldg(reinterpret_cast<const float4*>(z + e));
-          zv[4 * j] = f.x;
-          zv[4 * j + 1] = f.y;
-          zv[4 * j + 2] = f.z;
-          zv[4 * j + 3] = f.w;
-          valid |= 0xfu << (4 * j);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const bool in = e + t < p.V;
-            zv[4 * j + t] = in ? z[e + t] : 0.f;
-            valid |= in ? (1u << (4 * j + t)) : 0u;
-          }
+        for (int t = 0; t < 32; ++t) {
+          const int e = base + t * 32 + lane;
+          x[t] = e < p.V ? z[e] : 0.f;
+          valid |= e < p.V ? (1u << t) : 0u;
         }
+        draft_block<false>(x, valid, c, lp);
       }
-      float hm = -INFINITY;
-      int bad = 0;
-#pragma unroll
-      for (int t = 0; t < 32; ++t) {
-        if (!((valid >> t) & 1u)) continue;
-        const float h = expo_hi(zv[t], c);
-        if (!isfinite(h)) {
-          bad = 1;
-          valid &= ~(1u << t);
-        } else {
-          hm = fmaxf(hm, h);
-        }
-      }
-      lp.bad |= bad;
-      if (hm == -INFINITY) continue;
-      const float kn = ceilf(hm);
-      if (lp.k == -INFINITY) {
-        lp.k = kn;
-      } else if (kn > lp.k) {
-        lp.s = ff_scale2(lp.s, static_cast<int>(lp.k - kn));
-        lp.k = kn;
-      }
-      float sh = lp.s.hi, sl = lp.s.lo;
-#pragma unroll
-      for (int t = 0; t < 32; ++t)
-        if ((valid >> t) & 1u) ff_accumulate(sh, sl, pow2_rel(zv[t], c, lp.k));
-      lp.s = ff_norm(sh, sl);
+      const Partial wp = warp_merge(lp);
+      if (lane == 0) store_part(&p.dpart[u], wp);
     }
-    const Partial wp = warp_merge(lp);
-    if (lane == 0) store_part(&p.dpart[u], wp);
+    return;
+  }
+  auto load = [&](long long uu, int blk, float4 (&dst)[8], unsigned& valid) {
+    const int row = static_cast<int>(uu / p.dparts);
+    const int chunk = static_cast<int>(uu - static_cast<long long>(row) * p.dparts);
+    const float* z = p.zq + static_cast<size_t>(row) * p.V;
+    const int base = chunk * kChunk + blk * 1024;
+    valid = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = base + (j * 32 + lane) * 4;
+      const bool in = e < p.V;
+      dst[j] = in ? __ldg(reinterpret_cast<const float4*>(z + e)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      valid |= in ? (0xfu << (4 * j)) : 0u;
+    }
+  };
+  float4 cur[8], nxt[8];
+  unsigned vcur, vnxt = 0;
+  int blk = 0;
+  load(u, 0, cur, vcur);
+  Partial lp = partial_empty();
+  while (true) {
+    long long nu = u;
+    int nb = blk + 1;
+    if (nb == kBlocks) {
+      nb = 0;
+      nu += stride;
+    }
+    const bool more = nu < units;
+    if (more) load(nu, nb, nxt, vnxt);
+    float x[32];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      x[4 * j] = cur[j].x;
+      x[4 * j + 1] = cur[j].y;
+      x[4 * j + 2] = cur[j].z;
+      x[4 * j + 3] = cur[j].w;
+    }
+    if (vcur == 0xffffffffu)
+      draft_block<true>(x, vcur, c, lp);
+    else
+      draft_block<false>(x, vcur, c, lp);
+    if (blk == kBlocks - 1) {
+      const Partial wp = warp_merge(lp);
+      if (lane == 0) store_part(&p.dpart[u], wp);
+      lp = partial_empty();
+    }
+    if (!more) break;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+    vcur = vnxt;
+    u = nu;
+    blk = nb;
   }
 }
 
@@ -736,12 +800,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 // slot the MMAs fill the other.
 constexpr int kLargeWarps = 10;                  // producer, MMA, 8 epilogue warps
 constexpr int kLargeThreads = 32 * kLargeWarps;
+// With sampling statistics two side warps reduce the draft rows: 384 threads
+// still leave a thread the 168 registers the 320-thread forms use.
+__host__ __device__ constexpr int large_threads(int mode) {
+  return mode == kModeStats ? kLargeThreads + 64 : kLargeThreads;
+}
 constexpr int kLargeGroup = 16;                  // hidden blocks per TMEM slot (1024 products)
 constexpr int kLargeHalfMax = 128;               // columns per epilogue thread at N = 256
 constexpr int kLargePitch = 20;                  // floats per row of a warp's 32 x 16 transpose block
-// greedy scratch: [4 quadrants][256 columns] values and indices, then one
-// 32 x 16 transpose block per epilogue warp
-constexpr uint32_t kLargeArgmaxBytes = (2 * 4 * 256 + 8 * 32 * kLargePitch) * 4;
+// a warp's transpose block: 32 rows at a pitch of kLargePitch, rows 16-31
+// shifted by 16 more floats (for the statistics' column reads)
+constexpr int kLargeTbFloats = 32 * kLargePitch + 16;
+// greedy and statistics scratch: [4 quadrants][256 columns] twice (values and
+// indices, or references and sums), then one transpose block per epilogue warp
+constexpr uint32_t kLargeScratchBytes = (2 * 4 * 256 + 8 * kLargeTbFloats) * 4;
 
 // Greedy partials of 16 columns [col, col + 16) over the warp's 32 rows: the
 // block goes through the warp's own transpose block (128-bit stores at a pitch
@@ -803,7 +875,83 @@ __device__ __forceinline__ void argmax_merge_large(const HeadParams& p, int N, i
   }
 }
 
-// kMode: kModeLogits (f32 logits) or kModeArgmax (per-tile greedy partials).
+// Softmax-normaliser partials of 16 columns [col, col + 16) over the warp's 32
+// rows (the target statistics of a tile).  The block goes through the warp's
+// transpose block (rows 16-31 16 floats further on, which puts the two halves'
+// column reads in distinct banks); lane L then takes column L % 16 over the 16
+// rows of its half L / 16.  Two passes over the block: the largest h = z c of
+// the column, then the sum of 2^(z c - k) against the integer reference
+// k = ref_above(that maximum), shared by both halves.  Rows past V are
+// skipped; a non-finite logit marks the column (reference +inf).
+__device__ __forceinline__ void stats_large16(const HeadParams& p, const float (&val)[16], int col, int v, int q,
+                                              int lane, float* tb, float* red_k, float* red_s) {
+  __syncwarp();  // every lane's reads of the previous block are done
+  float* row_ptr = tb + lane * kLargePitch + (lane >= 16 ? 16 : 0);
+#pragma unroll
+  for (int j = 0; j < 16; j += 4)
+    *reinterpret_cast<float4*>(row_ptr + j) = make_float4(val[j], val[j + 1], val[j + 2], val[j + 3]);
+  __syncwarp();
+  const Expo c{p.c_hi, p.c_lo};
+  const int cc = lane & 15, hf = lane >> 4;
+  const int nrow = min(32, p.V - (v - lane)) - 16 * hf;  // rows of this lane's half inside the vocabulary
+  const float* col_ptr = tb + hf * (16 * kLargePitch + 16) + cc;
+  float hm = -INFINITY;
+  int bad = 0;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const float h = expo_hi(col_ptr[r * kLargePitch], c);
+    const bool use = r < nrow;
+    bad |= (use && !(fabsf(h) < INFINITY)) ? 1 : 0;
+    hm = use ? fmaxf(hm, h) : hm;
+  }
+  hm = fmaxf(hm, __shfl_xor_sync(0xffffffffu, hm, 16));
+  bad |= __shfl_xor_sync(0xffffffffu, bad, 16);
+  const float k = hm == -INFINITY ? -INFINITY : ref_above(hm);
+  float s = 0.f;
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {  // (the values are read again: 16 registers fewer)
+    const float z = col_ptr[r * kLargePitch];
+    const float h = expo_hi(z, c);
+    const float t = exp2f((h - k) + expo_lo(z, h, c));
+    s += r < nrow ? t : 0.f;
+  }
+  s += __shfl_xor_sync(0xffffffffu, s, 16);
+  if (lane < 16) {
+    red_k[q * 256 + col + lane] = bad ? INFINITY : k;
+    red_s[q * 256 + col + lane] = s;
+  }
+}
+
+// The tile's partial of column et (one column per epilogue thread): the four
+// lane quadrants brought to their largest reference (exact powers of two) and
+// added, then merged into this CTA's running partial of the row, which only
+// this thread reads and writes during the launch.
+__device__ __forceinline__ void stats_merge_large(const HeadParams& p, int N, int vt, int m0, int et,
+                                                  const float* red_k, const float* red_s) {
+  if (vt >= p.num_vt || et >= N) return;  // (the peer half of a pair's last tile lies past V)
+  const int m = m0 + et;
+  if (m >= p.M) return;
+  float k = red_k[et];
+#pragma unroll
+  for (int qq = 1; qq < 4; ++qq) k = fmaxf(k, red_k[qq * 256 + et]);
+  Partial t = partial_empty();
+  t.bad = k == INFINITY ? 1 : 0;
+  if (!t.bad && k != -INFINITY) {
+    float sum = 0.f;
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) sum += red_s[qq * 256 + et] * pow2_nonpos(red_k[qq * 256 + et] - k);
+    t.k = k;
+    t.s = {sum, 0.f};
+  }
+  StatPart* dst = &p.tpart[static_cast<size_t>(m) * p.tparts + blockIdx.x];
+  const StatPart old = *dst;
+  const Partial run{old.k, {old.s_hi, old.s_lo}, old.bad};
+  store_part(dst, partial_merge(run, t));
+}
+
+// kMode: kModeLogits (f32 logits), kModeArgmax (per-tile greedy partials) or
+// kModeStats (f32 logits, one softmax partial per CTA and target row, and the
+// draft rows' partials from two side warps).
 // kPair: the MMAs run over a CTA pair (a cluster of two on neighbouring SMs,
 // tcgen05 cta_group::2): a tile is 256 vocabulary rows, each CTA loads its
 // 128 rows of W and half of the chunk's hidden rows, the leader (even rank)
@@ -812,7 +960,7 @@ __device__ __forceinline__ void argmax_merge_large(const HeadParams& p, int N, i
 // that halves the hidden-state operand traffic of a product, the part of
 // shared-memory and L2 bandwidth that bounds the single-CTA MMAs.
 template <int kMode, bool kPair>
-__global__ void __launch_bounds__(kLargeThreads, 1)
+__global__ void __launch_bounds__(large_threads(kMode), 1)
     head_large_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_h,
                       const HeadParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -1021,15 +1169,16 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
         mma_commit(mma_done);
       if (!mbar_wait(mma_done, 0)) report_timeout(p.err);
     }
-  } else {
+  } else if (kMode != kModeStats || warp < kLargeWarps) {
     // ------------------------------------------------------------ epilogue (warps 2..9)
     const int q = warp & 3;               // TMEM lane quadrant this warp may read
     const int half = (warp - 2) >> 2;     // which half of the tile's columns
     const int et = threadIdx.x - 64;      // 0..255 among the epilogue threads
     const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(half * NH);
-    float* red_val = scr;
-    int* red_idx = reinterpret_cast<int*>(scr + 1024);
-    float* tb = scr + 2048 + (warp - 2) * (32 * kLargePitch);
+    float* red_val = scr;                                // greedy: values; statistics: references
+    int* red_idx = reinterpret_cast<int*>(scr + 1024);   // greedy: indices
+    float* red_s = scr + 1024;                           // statistics: sums
+    float* tb = scr + 2048 + (warp - 2) * kLargeTbFloats;
     // a drained slot is reported to the MMA issuer, in the leader CTA
     const uint32_t afree_leader0 = kPair ? cluster_map(&afree[0], 0) : 0u;
     const uint32_t afree_leader1 = kPair ? cluster_map(&afree[1], 0) : 0u;
@@ -1043,6 +1192,15 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
       if (blockIdx.x == 0) {
         if (p.zero_err && et == 0) *p.err = 0;
         for (int i = et; i < p.n_tickets; i += 256) p.tickets[i] = 0u;
+      }
+      if constexpr (kMode == kModeStats) {
+        // this CTA's running partials start empty (thread et owns column et
+        // of every chunk)
+        if (et < N)
+          for (int pc = 0; pc < p.num_chunks; ++pc) {
+            const int m = pc * N + et;
+            if (m < p.M) store_part(&p.tpart[static_cast<size_t>(m) * p.tparts + blockIdx.x], partial_empty());
+          }
       }
     };
     const int groups = (p.num_kb + kLargeGroup - 1) / kLargeGroup;
@@ -1104,13 +1262,26 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
           report_timeout(p.err);
           break;
         }
+        // 16 columns at a time (statistics: their logits are stored first),
+        // so that each block's sums die after it
 #pragma unroll
         for (int j = 0; j < kLargeHalfMax; j += 16) {
           if (j < NH) {
             float v16[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) v16[i] = acc[j + i];
-            argmax_large16(p, v16, c0 + j, v, q, lane, tb, red_val, red_idx);
+            if constexpr (kMode == kModeArgmax) {
+              argmax_large16(p, v16, c0 + j, v, q, lane, tb, red_val, red_idx);
+            } else {
+              if (v < p.V) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const int m = m0 + c0 + j + i;
+                  if (m < p.M) p.logits[static_cast<size_t>(m) * p.ldz + v] = v16[i];
+                }
+              }
+              stats_large16(p, v16, c0 + j, v, q, lane, tb, red_val, red_s);
+            }
           }
         }
         __syncwarp();
@@ -1119,13 +1290,22 @@ __global__ void __launch_bounds__(kLargeThreads, 1)
           report_timeout(p.err);
           break;
         }
-        argmax_merge_large(p, N, vt, m0, et, red_val, red_idx);
+        if constexpr (kMode == kModeArgmax)
+          argmax_merge_large(p, N, vt, m0, et, red_val, red_idx);
+        else
+          stats_merge_large(p, N, vt, m0, et, red_val, red_s);
         __syncwarp();
         if (lane == 0) mbar_arrive(red_free);
         rph ^= 1u;
       }
     }
-    wait_prev();  // (a CTA that finished no tile still clears the error word)
+    wait_prev();  // (a CTA that finished no tile still clears the error word and writes its partials)
+  } else {
+    // ------------------------------------------------------------ draft statistics (warps 10, 11)
+    if constexpr (kMode == kModeStats) {
+      griddep_wait();  // the draft partials may still be read by the kernel before this one
+      draft_stats(p, warp - kLargeWarps, lane);
+    }
   }
 
   tc_fence_before_sync();
@@ -1157,7 +1337,7 @@ cudaError_t launch_large(const CUtensorMap& map_w, const CUtensorMap& map_h, con
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(h.grid);
-  cfg.blockDim = dim3(kLargeThreads);
+  cfg.blockDim = dim3(large_threads(kMode));
   cfg.dynamicSmemBytes = h.smem_bytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -1171,7 +1351,8 @@ cudaError_t launch_large(const CUtensorMap& map_w, const CUtensorMap& map_h, con
 }
 
 // Clusters of two large-batch CTAs that fit the device at once (0 if the
-// pair form cannot be resident), probed once per device.
+// pair form cannot be resident), probed once per device and block size.
+template <int kMode>
 int large_pair_clusters(const DeviceInfo& dev, size_t smem_bytes) {
   static int cached[64] = {0};
   static size_t cached_smem[64] = {0};
@@ -1180,11 +1361,11 @@ int large_pair_clusters(const DeviceInfo& dev, size_t smem_bytes) {
   std::lock_guard<std::mutex> lock(mu);
   if (cached_smem[dev.device] == smem_bytes) return cached[dev.device];
   int n = 0;
-  if (cudaFuncSetAttribute(head_large_kernel<kModeLogits, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(head_large_kernel<kMode, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            dev.max_smem_optin) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * static_cast<unsigned>(dev.sm_count / 2));
-    cfg.blockDim = dim3(kLargeThreads);
+    cfg.blockDim = dim3(large_threads(kMode));
     cfg.dynamicSmemBytes = smem_bytes;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1193,7 +1374,7 @@ int large_pair_clusters(const DeviceInfo& dev, size_t smem_bytes) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaOccupancyMaxActiveClusters(&n, head_large_kernel<kModeLogits, true>, &cfg) != cudaSuccess) n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, head_large_kernel<kMode, true>, &cfg) != cudaSuccess) n = 0;
   }
   cudaGetLastError();  // a failed probe leaves no sticky error
   cached[dev.device] = n;
@@ -1310,9 +1491,11 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
   h.num_vt = (V + kHeadTileV - 1) / kHeadTileV;
   h.num_tiles = h.num_vt * h.num_chunks;
   h.num_kb = (d + kHeadTileK - 1) / kHeadTileK;
-  // the cross-quadrant scratch is used by the greedy epilogues only
+  // cross-quadrant scratch: the greedy epilogues, and the large-batch
+  // statistics epilogue
   size_t scratch = 0;
-  if (mode == HeadOut::kArgmax) scratch = h.large ? kLargeArgmaxBytes : kArgmaxSmallBytes;
+  if (mode == HeadOut::kArgmax) scratch = h.large ? kLargeScratchBytes : kArgmaxSmallBytes;
+  if (mode == HeadOut::kStats && h.large) scratch = kLargeScratchBytes;
   const size_t fixed = 1024 + kBarrierBytes + scratch;
   const size_t budget = static_cast<size_t>(dev.max_smem_optin);
   auto fit = [&](size_t stage) {
@@ -1333,7 +1516,8 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
     // CTA pairs where their clusters fit: tiles of 256 vocabulary rows, each
     // CTA holding half of the chunk's hidden rows
     fit(static_cast<size_t>(h.kbs) * (kABytes + static_cast<size_t>(h.N / 2) * 128));
-    const int clusters = large_pair_clusters(dev, h.smem_bytes);
+    const int clusters = mode == HeadOut::kStats ? large_pair_clusters<kModeStats>(dev, h.smem_bytes)
+                                                 : large_pair_clusters<kModeLogits>(dev, h.smem_bytes);
     if (clusters > 0) {
       h.pair = true;
       h.num_tiles = ((V + 2 * kHeadTileV - 1) / (2 * kHeadTileV)) * h.num_chunks;
@@ -1342,7 +1526,7 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
       fit(static_cast<size_t>(h.kbs) * (kABytes + static_cast<size_t>(h.N) * 128));
     }
   }
-  // the small-batch statistics: one running partial per CTA and target row
+  // the statistics: one running partial per CTA and target row
   h.target_parts = h.grid;
   return h;
 }
@@ -1400,15 +1584,14 @@ cudaError_t launch_head(const void* hidden, const void* W, int M, int d, int V, 
     p.n_tickets = stats->n_tickets;
   }
   if (h.large) {
-    // the large-batch kernel writes logits or greedy partials; its callers
-    // form the softmax statistics in a streaming pass over the logits
+    if (mode == HeadOut::kStats)
+      return h.pair ? launch_large<kModeStats, true>(map_w, map_h, p, h, dev, stream)
+                    : launch_large<kModeStats, false>(map_w, map_h, p, h, dev, stream);
     if (mode == HeadOut::kLogits)
       return h.pair ? launch_large<kModeLogits, true>(map_w, map_h, p, h, dev, stream)
                     : launch_large<kModeLogits, false>(map_w, map_h, p, h, dev, stream);
-    if (mode == HeadOut::kArgmax)
-      return h.pair ? launch_large<kModeArgmax, true>(map_w, map_h, p, h, dev, stream)
-                    : launch_large<kModeArgmax, false>(map_w, map_h, p, h, dev, stream);
-    return cudaErrorInvalidValue;
+    return h.pair ? launch_large<kModeArgmax, true>(map_w, map_h, p, h, dev, stream)
+                  : launch_large<kModeArgmax, false>(map_w, map_h, p, h, dev, stream);
   }
   if (h.N == 16) return launch_mode<16>(mode, map_w, map_h, p, h, dev, stream);
   if (h.N == 32) return launch_mode<32>(mode, map_w, map_h, p, h, dev, stream);

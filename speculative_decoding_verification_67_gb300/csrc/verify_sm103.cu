@@ -262,10 +262,10 @@ __global__ void __launch_bounds__(kStatThreads, 3) row_stats_kernel(const float*
                                                              const float* __restrict__ zq, int M, int V,
                                                              long long ldp, Expo c, StatPart* tpart, StatPart* dpart,
                                                              int P, long long units, int* err, unsigned* tickets,
-                                                             int n_tickets) {
+                                                             int n_tickets, int zero_err) {
   const int lane = threadIdx.x & 31;
   if (blockIdx.x == 0) {
-    if (err && threadIdx.x == 0) *err = 0;
+    if (zero_err && err && threadIdx.x == 0) *err = 0;
     for (int i = threadIdx.x; i < n_tickets; i += kStatThreads) tickets[i] = 0u;
   }
   constexpr int kStatWarps = kStatThreads / 32;
@@ -408,7 +408,7 @@ __device__ __forceinline__ void fold_smem32(const float* blk, int nv, int lane, 
 __global__ void __launch_bounds__(kBulkThreads, 1)
     row_stats_bulk_kernel(const float* __restrict__ zp, const float* __restrict__ zq, int M, int V, long long ldp,
                           Expo c, StatPart* tpart, StatPart* dpart, int P, long long units, int* err,
-                          unsigned* tickets, int n_tickets, int S) {
+                          unsigned* tickets, int n_tickets, int S, int zero_err) {
   extern __shared__ __align__(16) uint8_t bulk_smem[];
   float* ring = reinterpret_cast<float*>(bulk_smem);
   uint64_t* full = reinterpret_cast<uint64_t*>(bulk_smem + static_cast<size_t>(S) * kBulkUnitBytes);
@@ -416,7 +416,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
   float4* handoff = reinterpret_cast<float4*>(empty + S);  // [S] the second half's partial, per stage
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (blockIdx.x == 0) {
-    if (err && threadIdx.x == 0) *err = 0;
+    if (zero_err && err && threadIdx.x == 0) *err = 0;
     for (int i = threadIdx.x; i < n_tickets; i += kBulkThreads) tickets[i] = 0u;
   }
   if (threadIdx.x == 0) {
@@ -1274,7 +1274,7 @@ void exponent_constant(float temperature, float* c_hi, float* c_lo) {
 
 cudaError_t launch_row_stats(const float* zp, const float* zq, int M, int draft_rows, int V, float c_hi, float c_lo,
                              StatPart* tpart, StatPart* dpart, int* err, unsigned* tickets, int n_tickets,
-                             cudaStream_t stream, long long ldp) {
+                             cudaStream_t stream, long long ldp, bool zero_err) {
   const int P = (V + kChunk - 1) / kChunk;
   const long long units = static_cast<long long>(M + draft_rows) * P;
   if (units == 0) return cudaSuccess;
@@ -1310,16 +1310,16 @@ cudaError_t launch_row_stats(const float* zp, const float* zq, int M, int draft_
       }
       const int bgrid = static_cast<int>(std::min<long long>(units, sms));
       row_stats_bulk_kernel<<<bgrid, kBulkThreads, smem, stream>>>(zp, zq, M, V, ldp, c, tpart, dpart, P, units,
-                                                                    err, tickets, n_tickets, S);
+                                                                    err, tickets, n_tickets, S, zero_err ? 1 : 0);
       return cudaGetLastError();
     }
   }
   if (vec)
     row_stats_kernel<true><<<grid, kStatThreads, 0, stream>>>(zp, zq, M, V, ldp, c, tpart, dpart, P, units, err,
-                                                              tickets, n_tickets);
+                                                              tickets, n_tickets, zero_err ? 1 : 0);
   else
     row_stats_kernel<false><<<grid, kStatThreads, 0, stream>>>(zp, zq, M, V, ldp, c, tpart, dpart, P, units, err,
-                                                               tickets, n_tickets);
+                                                               tickets, n_tickets, zero_err ? 1 : 0);
   return cudaGetLastError();
 }
 

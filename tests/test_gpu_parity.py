@@ -336,6 +336,7 @@ def test_determinism_bits():
                                        (2, 3, 256, 3000, 1e-6),     # |z / T| in log2 units around 2^22
                                        (2, 3, 256, 3000, 1e-8),     # ... and beyond 2^24
                                        (40, 7, 256, 3001, 0.9),     # M = 320: large-batch head, two chunks of 160
+                                       (16, 4, 4096, 32000, 0.9),   # M = 80: large-batch head, draft rows by its side warps
                                        (20, 12, 128, 1500, 1.3),    # M = 260: two chunks of 160, the second of 100 rows
                                        (100, 10, 128, 2000, 1.0),   # M = 1100: 5 chunks of 224
                                        (80, 0, 128, 1000, 1.0)])    # large-batch head, bonus draws only
@@ -448,6 +449,29 @@ def test_nonfinite_hidden_marks_the_sequence(B, K):
         h[1 * (K + 1) + 2, 5] = bad
         ws = torch.empty(sv.workspace_bytes(B, K, V, T), dtype=torch.uint8, device="cuda")
         tok, n = sv.spec_verify(h, inp["W"], inp["draft_logits"], inp["draft_tokens"], inp["uniforms"], T,
+                                workspace=ws)
+        assert sv.read_error(ws) & sv.DEVERR_NONFINITE, bad
+        n, tok = np_int(n), np_int(tok)
+        assert n[1] == -1 and (tok[1] == -1).all(), bad
+        keep = [b for b in range(B) if b != 1]
+        compare_sampling(tok[keep], n[keep], {k: v[keep] for k, v in ref.items() if k != "target_logits"}, K)
+
+
+@pytest.mark.parametrize("B,K,d,V", [(3, 2, 256, 3000),      # small-batch head: its side warps
+                                     (16, 4, 4096, 32000),  # large-batch head: its side warps
+                                     (24, 4, 256, 3000)])   # large-batch head, then the draft-row pass
+def test_nonfinite_draft_logit_in_the_whole_step(B, K, d, V):
+    """A NaN, +inf or -inf draft logit, wherever the draft rows are reduced
+    in the whole step, flags its sequence; the others are unaffected."""
+    w = synth.custom("nf_draft", B=B, K=K, d=d, V=V, temperature=1.0, seed=31 + B)
+    inp = synth.make_inputs(w, device="cuda")
+    ref = oracle.spec_verify(np64(inp["hidden"]), np64(inp["W"]), np64(inp["draft_logits"]),
+                             np_int(inp["draft_tokens"]), np64(inp["uniforms"]), t32(w.temperature), B, K)
+    for bad in (float("nan"), float("inf"), float("-inf")):
+        zq = inp["draft_logits"].clone()
+        zq[1 * K + 1, V - 7] = bad   # sequence 1, draft row 1, in the last chunk
+        ws = torch.empty(sv.workspace_bytes(B, K, V, w.temperature), dtype=torch.uint8, device="cuda")
+        tok, n = sv.spec_verify(inp["hidden"], inp["W"], zq, inp["draft_tokens"], inp["uniforms"], w.temperature,
                                 workspace=ws)
         assert sv.read_error(ws) & sv.DEVERR_NONFINITE, bad
         n, tok = np_int(n), np_int(tok)
