@@ -53,7 +53,7 @@ METRIC = "verified positions/sec at V=128256; achieved HBM GB/s vs GB300 peak"
 # DRAM bytes (read + write) of one launch of the dominant kernel, from the ncu
 # capture summarised in profiles/head_kernel_stats_B8_K4_V128256.md (rounded to
 # 0.1 MB).  Valid only while head_kernel is unchanged since that capture.
-NCU_TRAFFIC = {"head_B8_K4_V128256": 1_073_230_000}
+NCU_TRAFFIC = {"head_B8_K4_V128256": 1_072_681_000}
 
 
 def load_peaks():
