@@ -1521,7 +1521,7 @@ HeadPlan plan_head(int M, int d, int V, HeadOut mode, const DeviceInfo& dev, boo
     if (clusters > 0) {
       h.pair = true;
       h.num_tiles = ((V + 2 * kHeadTileV - 1) / (2 * kHeadTileV)) * h.num_chunks;
-      h.grid = 2 * std::min(clusters, h.num_tiles);
+      h.grid = 2 * std::min(std::min(clusters, h.num_tiles), kMaxHeadGrid / 2);  // (target partials: one per CTA)
     } else {
       fit(static_cast<size_t>(h.kbs) * (kABytes + static_cast<size_t>(h.N) * 128));
     }
