@@ -20,11 +20,12 @@
 //    L2 hint, hidden tile Nx64 with evict-last), warp 1 allocates TMEM and
 //    issues tcgen05.mma from one thread, the epilogue warps drain TMEM
 //    (tcgen05.ld) and write the f32 logits, per-tile (max, lowest argmax)
-//    partials for the greedy path, or -- up to 64 positions -- the logits
-//    plus the softmax(z/T) normaliser partials of every target row (the
-//    epilogue holds each logit in a register already, so the statistics
-//    cost no extra pass over the logits), while warps 6-7 reduce the draft
-//    logits to the same partials, hidden under the weight stream;
+//    partials for the greedy path, or the logits plus the softmax(z/T)
+//    normaliser partials of every target row (the epilogue holds each logit
+//    in a register already, so the statistics cost no extra pass over the
+//    logits), while two side warps reduce the draft logits to the same
+//    partials, hidden under the weight stream (or under the MMAs, above 64
+//    positions, when they fit the head's run);
 //  * precise accumulation everywhere: the tensor core never accumulates
 //    over the whole hidden size.  Up to 64 positions (head_kernel) every
 //    four 64-wide hidden blocks go into a fresh TMEM slot (4 slots rotate)

@@ -121,8 +121,8 @@ def test_repeated_draws_full_size():
 
 
 def test_strided_slot_above_the_fused_statistics_batch():
-    """More rows than the fused-statistics LM head takes (the logits pass,
-    then a statistics pass), writing slot 1 of a [B][3][V] buffer."""
+    """More rows than the small-batch LM head takes (the large-batch head,
+    its statistics in the epilogue), writing slot 1 of a [B][3][V] buffer."""
     B, d, V, T = 100, 256, 5003, 0.9
     w = synth.custom("draft_strided", B=B, K=1, d=d, V=V, temperature=T, seed=21)
     inp = synth.make_draft_inputs(w, device="cuda")

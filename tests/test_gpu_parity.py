@@ -82,7 +82,7 @@ def test_lm_head_is_deterministic():
 
 @pytest.mark.parametrize("B,K,T", [(2, 3, 0.9),      # 16-column precise head, stream-K split tiles
                                    (8, 4, 0.8),      # 48 columns
-                                   (40, 7, 1.1),     # large-batch head (two chunks of 160), statistics pass
+                                   (40, 7, 1.1),     # large-batch head (two chunks of 160), draft-row pass
                                    (40, 7, 0.0)])    # large-batch greedy (transposed argmax epilogue)
 def test_whole_step_is_deterministic(B, K, T):
     """The same inputs twice through the whole step (LM head, statistics,
@@ -436,9 +436,8 @@ def test_nonfinite_logit_marks_the_sequence():
 @pytest.mark.parametrize("B,K", [(3, 2), (24, 4)])   # the small-batch and the large-batch LM head
 def test_nonfinite_hidden_marks_the_sequence(B, K):
     """A NaN or infinite hidden state makes its position's logits non-finite
-    (in the small-batch head's fused statistics, or in the statistics pass
-    after the large-batch head): that sequence is flagged, the others are
-    unaffected."""
+    (in either head's fused statistics): that sequence is flagged, the others
+    are unaffected."""
     w = synth.custom("nf_head", B=B, K=K, d=256, V=3000, temperature=1.0, seed=21 + B)
     inp = synth.make_inputs(w, device="cuda")
     B, K, V, T = w.B, w.K, w.V, w.temperature
