@@ -80,16 +80,17 @@ def test_lm_head_is_deterministic():
     assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("B,K,T", [(2, 3, 0.9),      # 16-column precise head, stream-K split tiles
-                                   (8, 4, 0.8),      # 48 columns
-                                   (40, 7, 1.1),     # large-batch head (two chunks of 160), draft-row pass
-                                   (40, 7, 0.0)])    # large-batch greedy (transposed argmax epilogue)
-def test_whole_step_is_deterministic(B, K, T):
+@pytest.mark.parametrize("B,K,T,d", [(2, 3, 0.9, 512),      # 16-column precise head, stream-K split tiles
+                                     (8, 4, 0.8, 512),      # 48 columns
+                                     (40, 7, 1.1, 512),     # large-batch head (two chunks of 160), draft-row pass
+                                     (16, 4, 0.9, 4096),    # large-batch head, draft rows on its side warps
+                                     (40, 7, 0.0, 512)])    # large-batch greedy (transposed argmax epilogue)
+def test_whole_step_is_deterministic(B, K, T, d):
     """The same inputs twice through the whole step (LM head, statistics,
     decision, draw): identical logits, tokens, counts and debug fields.  The
     schedules fix every summation order (stream-K splits, per-CTA running
     partials, the merges), so nothing may depend on timing."""
-    w = synth.custom("det_step", B=B, K=K, d=512, V=7001, temperature=T, seed=B + K)
+    w = synth.custom("det_step", B=B, K=K, d=d, V=7001, temperature=T, seed=B + K)
     inp = synth.make_inputs(w, device="cuda")
     outs = []
     for _ in range(2):
@@ -337,6 +338,7 @@ def test_determinism_bits():
                                        (2, 3, 256, 3000, 1e-8),     # ... and beyond 2^24
                                        (40, 7, 256, 3001, 0.9),     # M = 320: large-batch head, two chunks of 160
                                        (16, 4, 4096, 32000, 0.9),   # M = 80: large-batch head, draft rows by its side warps
+                                       (16, 4, 4096, 32003, 1.0),   # ... V % 4 != 0 (scalar draft loads), last pair tile past V
                                        (20, 12, 128, 1500, 1.3),    # M = 260: two chunks of 160, the second of 100 rows
                                        (100, 10, 128, 2000, 1.0),   # M = 1100: 5 chunks of 224
                                        (80, 0, 128, 1000, 1.0)])    # large-batch head, bonus draws only
