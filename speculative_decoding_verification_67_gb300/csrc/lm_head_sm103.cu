@@ -31,10 +31,11 @@
 //    four 64-wide hidden blocks go into a fresh TMEM slot (4 slots rotate)
 //    and the epilogue adds the slot results in f32 registers, so the tensor
 //    core's own accumulation spans 256 products; above 64 positions
-//    (head_large_kernel, further down) groups of 16 blocks (1024 products)
+//    (head_large_kernel, further down) groups of 32 blocks (2048 products)
 //    alternate between two slots.  An accumulator over the whole hidden size
 //    moved ~0.24 % of the sampling step's inverse-CDF draws at d = 8192
-//    against fp64 logits; 1024-product groups keep that ~0.01 %;
+//    against fp64 logits; 1024-product groups kept that ~0.02 %, 2048-product
+//    groups (2.5 % faster on the tensor-bound shapes) ~0.03 %;
 //  * every wait is bounded; a timeout sets the error word, drains the copies
 //    in flight and frees TMEM before returning.
 #include <cudaTypedefs.h>
@@ -794,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // B = 256, K = 4 five of 256), the same operand shapes as one accumulator over
 // the whole hidden size would use, so the tensor core sees the same operand
 // traffic per product.  The accumulation is precise: groups of kLargeGroup
-// hidden blocks (1024 products) go into two TMEM slots of N columns in turn,
+// hidden blocks (2048 products) go into two TMEM slots of N columns in turn,
 // and the epilogue adds the slots in f32 registers.  Eight epilogue warps
 // share the work: warp w reads TMEM lane quadrant w % 4 and one half of the
 // columns, so that a thread keeps N/2 <= 128 running sums; while it drains one
@@ -806,7 +807,7 @@ constexpr int kLargeThreads = 32 * kLargeWarps;
 __host__ __device__ constexpr int large_threads(int mode) {
   return mode == kModeStats ? kLargeThreads + 64 : kLargeThreads;
 }
-constexpr int kLargeGroup = 16;                  // hidden blocks per TMEM slot (1024 products)
+constexpr int kLargeGroup = 32;                  // hidden blocks per TMEM slot (2048 products)
 constexpr int kLargeHalfMax = 128;               // columns per epilogue thread at N = 256
 constexpr int kLargePitch = 20;                  // floats per row of a warp's 32 x 16 transpose block
 // a warp's transpose block: 32 rows at a pitch of kLargePitch, rows 16-31

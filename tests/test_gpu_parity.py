@@ -589,7 +589,7 @@ def test_head_precision_keeps_draws_headline():
 
 def test_head_precision_keeps_draws_large_batch():
     """The same measure on 48 rows of the B=64, d=8192 workload, whose LM head
-    (576 positions) runs the large-batch kernel's 1024-product groups (an
+    (576 positions) runs the large-batch kernel's 2048-product groups (an
     accumulator over the whole hidden size moved ~0.24 % of these draws)."""
     w = synth.WORKLOADS["head_B64_K8_V152064"]
     inp = synth.make_inputs(w, device="cuda")
